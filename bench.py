@@ -1,0 +1,560 @@
+#!/usr/bin/env python3
+"""Benchmark of the depthwise causal conv1d decode update on GB300.
+
+One step = one decode update (ccu_conv1d_update through the C-ABI) over the
+large-batch decode workload: N=4096 rows, D=16384 channels, W=4, L=3, S=4096 slots,
+BF16, bias, SiLU, slot indices a permutation with 5% padding rows. Inputs are seeded
+and synthetic (the cuDNN page "Causal Conv1d Decode Update" publishes no dataset).
+
+Metric: achieved HBM GB/s = algorithmic bytes / time, where the algorithmic bytes of
+one update are, per active (row, channel): 2 B x read + 2L B state read + 2L B state
+write + 2 B out write; per padding (row, channel): 2 B out write; plus weight, bias and
+indices read once (1,026,899,968 B for this workload).
+
+Printed: ONE JSON line (rank 0). ``value`` is device-resident throughput (inputs in
+HBM, CUDA events on the launching stream); ``e2e`` adds, every step, the host->device
+copy of that step's x and indices from pinned memory and the device->host copy of its
+output; ``roofline`` reports the update kernel against the measured HBM copy peak;
+``cpu_baseline`` times the single-threaded CPU oracle on a bounded sample;
+``per_workload`` gives eager / CUDA-graph / cold-L2 µs per call for every workload.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Under torchrun (N > 1) each rank runs its own copy of the workload on its own GPU
+(independent decode batches: weak scaling, no collective on the data path).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synthetic  # noqa: E402
+
+METRIC = "conv1d_update HBM GB/s (% of GB300 peak) and µs/call vs N·D, 1 GPU"
+UNIT = "GB/s"
+L2_BYTES = 129 * 1024 * 1024
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "update_vector_large_n4096_d16384.txt")
+KERNEL_SOURCES = [os.path.join(ROOT, "depthwise_causal_conv1d_gb300", "csrc", f)
+                  for f in ("k_vector.cu", "ccu_internal.cuh")]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=synthetic.BENCH_WORKLOAD, choices=sorted(synthetic.WORKLOADS))
+    ap.add_argument("--rows", type=int, default=None,
+                    help="run a smaller case of the same kernel: first ROWS rows (profiling)")
+    ap.add_argument("--route", default="auto", choices=["auto", "scalar", "vector", "staged", "bulk"])
+    ap.add_argument("--layout", default="compact", choices=["compact", "channel_last"])
+    ap.add_argument("--quick", action="store_true",
+                    help="device-resident timing only: no e2e, table, CPU baseline or clocks")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args()
+
+
+def workload_for(args) -> synthetic.Workload:
+    wl = synthetic.WORKLOADS[args.workload]
+    if args.rows is not None and args.rows < wl.N:
+        changes = dict(N=args.rows)
+        if wl.indices.startswith("perm"):
+            changes["S"] = args.rows
+        wl = synthetic.variant(wl, **changes)
+    if args.layout != "compact":
+        wl = synthetic.variant(wl, layout=args.layout)
+    return wl
+
+
+def config_of(wl: synthetic.Workload, extra=None) -> dict:
+    cfg = {"workload": wl.name, "N": wl.N, "D": wl.D, "W": wl.W, "L": wl.L, "S": wl.S, "ld": wl.ld,
+           "activation": wl.act, "bias": wl.has_bias, "indices": wl.indices, "pad_frac": wl.pad_frac,
+           "state_layout": wl.layout, "N_x_D": wl.N * wl.D, "seed": wl.seed}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# --------------------------------------------------------------------------- distributed
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            import torch
+
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+        self.marks = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_id}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        self.marks.append(time.time())
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        def parse(rows):
+            out = []
+            for _, ln in rows:
+                f = [x.strip() for x in ln.split(",")]
+                if len(f) < 8:
+                    continue
+                try:
+                    out.append(dict(sm=float(f[0]), smax=float(f[1]), reasons=f[4:8]))
+                except ValueError:
+                    continue
+            return out
+
+        inside = parse([r for r in self.lines if t0 <= r[0] <= t1])
+        scope = "timed region"
+        if not inside:
+            inside = parse(self.lines)
+            scope = "whole GPU phase (timed region shorter than one 200 ms sample)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"],
+                    "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        seen = sorted({names[i] for s in inside for i, v in enumerate(s["reasons"]) if v == "Active"})
+        return {"sm_mhz": statistics.median(s["sm"] for s in inside),
+                "sm_max_mhz": max(s["smax"] for s in inside), "reasons": seen,
+                "samples": len(inside), "scope": scope}
+
+
+def gpu_id_for(dev_index: int) -> str:
+    import torch
+
+    try:
+        u = str(torch.cuda.get_device_properties(dev_index).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        parts = [p for p in vis.split(",") if p.strip()]
+        return parts[dev_index] if dev_index < len(parts) else str(dev_index)
+
+
+# --------------------------------------------------------------------------- profile summary
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(full_units: int):
+    """DRAM bytes per launch from the committed ncu summary, scaled to this launch's
+    (row, channel) units; None if the kernel source changed since the capture."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None, "no ncu summary"
+    kv = dict(ln.split("=", 1) for ln in text.splitlines() if "=" in ln and not ln.startswith("#"))
+    try:
+        if kv.get("kernel_source_sha256_16") != kernel_source_hash():
+            return None, "kernel changed since the ncu capture"
+        traffic = float(kv["dram_bytes_per_launch"])
+        units = float(kv["units_per_launch"])
+    except (KeyError, ValueError):
+        return None, "ncu summary unreadable"
+    return traffic * full_units / units, kv.get("capture_case", "")
+
+
+# --------------------------------------------------------------------------- our arm
+
+def to_dev(a, dev):
+    import torch
+
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+
+class Resident:
+    """Device copies of one workload's tensors plus the C-ABI call on them."""
+
+    def __init__(self, inp, dev, stream, route="auto", layout="compact"):
+        import torch
+
+        import depthwise_causal_conv1d_gb300 as ccu
+
+        self.ccu = ccu
+        wl = inp.wl
+        self.wl = wl
+        self.x_full = to_dev(inp.x, dev)
+        self.x = self.x_full[:, :wl.D] if wl.ld != wl.D else self.x_full
+        if layout == "compact":
+            self.state = to_dev(inp.conv_state, dev)
+        else:
+            self.state = to_dev(synthetic.to_channel_last(inp.conv_state), dev).permute(0, 2, 1)
+        self.w = to_dev(inp.weight, dev)
+        self.b = to_dev(inp.bias, dev) if inp.bias is not None else None
+        self.idx = torch.from_numpy(inp.indices).to(dev) if inp.indices is not None else None
+        self.out = torch.empty((wl.N, wl.D), dtype=torch.bfloat16, device=dev)
+        self.stream = stream
+        self.route = ccu.ROUTES[route]
+        ss, sd, sl = self.state.stride()
+        self.args = (self.x.data_ptr(), wl.ld, self.state.data_ptr(), ss, sd, sl, self.w.data_ptr(),
+                     None if self.b is None else self.b.data_ptr(),
+                     ccu.CCU_ACT_SILU if wl.act == "silu" else ccu.CCU_ACT_IDENTITY,
+                     None if self.idx is None else self.idx.data_ptr(), None,
+                     wl.N, wl.D, wl.S, wl.L, wl.W, self.out.data_ptr(), None, self.route,
+                     stream.cuda_stream)
+        st, chosen = ccu.ccu_conv1d_select_route(*self.args[:17], self.route)
+        ccu.raise_for_status(st)
+        self.route_name = ccu.ccu_route_name(chosen)
+
+    def call(self):
+        st = self.ccu.lib.ccu_conv1d_update_ex(*self.args)
+        if st != 0:
+            self.ccu.raise_for_status(st)
+
+
+def time_device_resident(res: Resident, steps: int, warmup: int, world: int, dev):
+    """Returns (total seconds over ranks, mean per-launch seconds)."""
+    import torch
+
+    s = res.stream
+    for _ in range(warmup):
+        res.call()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    t_begin.record(s)
+    for i in range(steps):
+        starts[i].record(s)
+        res.call()
+        ends[i].record(s)
+    t_end.record(s)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    barrier(world)
+    total = t_begin.elapsed_time(t_end) / 1e3
+    per_launch = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / steps / 1e3
+    total = max_over_ranks(total, world, dev)
+    return total, per_launch, (wall0, wall1)
+
+
+def time_e2e(res: Resident, inp, steps: int, warmup: int, world: int, dev):
+    """Every step: pinned x (+indices) host->device, the C-ABI call, out device->host."""
+    import torch
+
+    wl = inp.wl
+    s = res.stream
+    h_x = torch.from_numpy(np.ascontiguousarray(inp.x).view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_idx = torch.from_numpy(inp.indices).pin_memory() if inp.indices is not None else None
+    h_out = torch.empty((wl.N, wl.D), dtype=torch.bfloat16, pin_memory=True)
+    bytes_in = h_x.numel() * 2 + (h_idx.numel() * 4 if h_idx is not None else 0)
+    bytes_out = h_out.numel() * 2
+
+    def step():
+        with torch.cuda.stream(s):
+            res.x_full.copy_(h_x, non_blocking=True)
+            if h_idx is not None:
+                res.idx.copy_(h_idx, non_blocking=True)
+            res.call()
+            h_out.copy_(res.out, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    e0.record(s)
+    for _ in range(steps):
+        step()
+    e1.record(s)
+    torch.cuda.synchronize()
+    barrier(world)
+    total = max_over_ranks(e0.elapsed_time(e1) / 1e3, world, dev)
+    return total, bytes_in, bytes_out
+
+
+def per_workload_table(dev, stream, reps=50):
+    """µs per call for every workload: eager (warm), CUDA-graph replay, and cold L2."""
+    import torch
+
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+    rows = {}
+    for name, wl in synthetic.WORKLOADS.items():
+        inp = synthetic.generate(wl)
+        res = Resident(inp, dev, stream)
+        nbytes = synthetic.algorithmic_bytes(wl, inp.indices)
+        for _ in range(5):
+            res.call()
+        torch.cuda.synchronize()
+        # eager, back to back
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            res.call()
+        b.record(stream)
+        torch.cuda.synchronize()
+        eager_us = a.elapsed_time(b) * 1e3 / reps
+        # cold: flush L2 before every call, time the call alone
+        cold = []
+        for _ in range(reps):
+            with torch.cuda.stream(stream):
+                flush.fill_(1)
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            c0.record(stream)
+            res.call()
+            c1.record(stream)
+            cold.append((c0, c1))
+        torch.cuda.synchronize()
+        cold_us = statistics.median(c0.elapsed_time(c1) * 1e3 for c0, c1 in cold)
+        # CUDA graph: 100 calls captured, replayed 20 times
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(100):
+                res.call()
+        g.replay()
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(20):
+            g.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        graph_us = g0.elapsed_time(g1) * 1e3 / 2000
+        rows[name] = {"N_x_D": wl.N * wl.D, "bytes": nbytes, "route": res.route_name,
+                      "eager_us": round(eager_us, 3), "graph_us": round(graph_us, 3),
+                      "cold_us": round(cold_us, 3),
+                      "cold_GBps": round(nbytes / (cold_us * 1e-6) / 1e9, 1)}
+        del g, res
+    del flush
+    return rows
+
+
+def cpu_baseline_sample(inp, target_s: float):
+    """Time the single-threaded C oracle on a bounded sample of the workload's rows."""
+    import oracle
+
+    wl = inp.wl
+    lib = oracle.load()
+    # first a small probe to size the sample
+    rows = max(1, min(wl.N, 64))
+    t_probe = _oracle_rows(oracle, lib, inp, rows)
+    per_row = t_probe / rows
+    rows = int(max(1, min(wl.N, (target_s / 3) / max(per_row, 1e-9))))
+    times = [_oracle_rows(oracle, lib, inp, rows) for _ in range(3)]
+    t = statistics.median(times)
+    sub_idx = inp.indices[:rows] if inp.indices is not None else None
+    sub_wl = synthetic.variant(wl, N=rows)
+    nbytes = synthetic.algorithmic_bytes(sub_wl, sub_idx)
+    return {"value": round(nbytes / t / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"first {rows} of {wl.N} rows (all {wl.D} channels, full state), "
+                      f"median of 3 runs of {t:.2f} s each; {nbytes} algorithmic bytes per run",
+            "seconds_per_run": round(t, 3), "cores_available": os.cpu_count()}
+
+
+def _oracle_rows(oracle, lib, inp, rows):
+    wl = inp.wl
+    state = inp.conv_state.copy()  # outside the timed region
+    x = np.ascontiguousarray(inp.x[:rows])
+    idx = inp.indices[:rows].copy() if inp.indices is not None else None
+    t0 = time.perf_counter()
+    oracle.conv1d_update(x, wl.ld, state, (wl.D * wl.L, wl.L, 1), inp.weight, inp.bias, wl.act,
+                         idx, rows, wl.D, wl.S, wl.L, wl.W, lib=lib)
+    return time.perf_counter() - t0
+
+
+def run_ours(args):
+    import torch
+
+    world, rank, local = dist_setup(args)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = workload_for(args)
+    inp = synthetic.generate(wl)
+    nbytes = synthetic.algorithmic_bytes(wl, inp.indices)
+    stream = torch.cuda.Stream(device=dev)
+    res = Resident(inp, dev, stream, route=args.route, layout=wl.layout)
+
+    sampler = None
+    if not args.quick:
+        sampler = ClockSampler(gpu_id_for(local))
+        sampler.start()
+        time.sleep(0.3)
+
+    total, per_launch, (w0, w1) = time_device_resident(res, args.steps, args.warmup, world, dev)
+    value = nbytes * world * args.steps / total / 1e9
+    achieved = nbytes / per_launch / 1e9
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        peak, peak_src = float(peaks["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        peak, peak_src = 6800.0, "fallback"
+    traffic, traffic_note = ncu_traffic(wl.N * wl.D)
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; the pages publish no dataset)",
+        "config": config_of(wl, {"route": res.route_name,
+                                 "l2": f"inputs larger than L2: {nbytes / 1e9:.3f} GB touched per "
+                                       f"step vs {L2_BYTES / 2**20:.0f} MiB L2",
+                                 "us_per_call": round(total / args.steps * 1e6, 2),
+                                 "parallelism": f"independent decode batch per GPU x{world}"}),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} (hbm_gbs)",
+                     "bytes_per_launch": nbytes,
+                     "launch_us": round(per_launch * 1e6, 2),
+                     "frac_of_nominal_8TBps": round(achieved / 8000.0, 4),
+                     "traffic": None if traffic is None else round(traffic),
+                     "traffic_note": traffic_note},
+        "gpu_launches": args.steps,
+    }
+    if not args.quick:
+        e2e_total, bi, bo = time_e2e(res, inp, max(10, args.steps // 20), 3, world, dev)
+        e2e_steps = max(10, args.steps // 20)
+        line["e2e"] = {"value": round(nbytes * world * e2e_steps / e2e_total / 1e9, 1), "unit": UNIT,
+                       "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+                       "ms_per_step": round(e2e_total / e2e_steps * 1e3, 4), "steps": e2e_steps,
+                       "path": "pinned host x/indices -> device, C-ABI update, out -> pinned host; "
+                               "conv_state and weights stay resident (they are the decode cache)"}
+        sampler.stop()
+        line["clocks"] = sampler.summary(w0, w1)
+        if rank == 0 and world == 1:
+            line["per_workload"] = per_workload_table(dev, stream)
+        if rank == 0:
+            line["cpu_baseline"] = cpu_baseline_sample(inp, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle, as it stands, on the host cores (rank 0 only)."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+
+    wl = workload_for(args)
+    inp = synthetic.generate(wl)
+    lib = oracle.load()
+    # each step: a bounded sample of the workload's rows, sized so the run takes minutes
+    probe = _oracle_rows(oracle, lib, inp, min(wl.N, 16)) / min(wl.N, 16)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    rows = int(max(1, min(wl.N, budget / max(probe, 1e-9))))
+    for _ in range(args.warmup):
+        _oracle_rows(oracle, lib, inp, rows)
+    times = [_oracle_rows(oracle, lib, inp, rows) for _ in range(args.steps)]
+    total = sum(times)
+    sub_wl = synthetic.variant(wl, N=rows)
+    nbytes = synthetic.algorithmic_bytes(sub_wl, inp.indices[:rows] if inp.indices is not None else None)
+    value = nbytes * args.steps / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; the pages publish no dataset)",
+        "config": config_of(wl, {"rows_per_step": rows}),
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"first {rows} of {wl.N} rows per step (all {wl.D} channels)",
+                         "cores_available": os.cpu_count()},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3  # at least three untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

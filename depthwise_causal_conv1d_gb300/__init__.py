@@ -1,0 +1,251 @@
+"""Python binding of ``libccu_conv1d.so``: the depthwise causal conv1d decode update on GB300.
+
+Argument marshalling only. Every step of the update runs in the library's CUDA
+kernels; PyTorch supplies device memory and the current stream. There is no CPU
+path: if the library is missing, importing the binding fails.
+
+Two layers:
+
+* ``ccu_conv1d_update`` and the other ``ccu_*`` functions mirror the C entry points
+  of ``include/ccu_conv1d.h`` one to one (raw device pointers as ints).
+* ``causal_conv1d_update(x, conv_state, weight, bias=None, activation=None, *,
+  cache_seqlens=None, conv_state_indices=None)`` follows the signature of the cuDNN
+  page "Causal Conv1d Decode Update" (section "Python API"): it mutates
+  ``conv_state`` in place and returns a newly allocated BF16 ``[N, D]`` tensor.
+  Declines are typed: ``NotImplementedError`` for valid but unserved requests,
+  ``ValueError`` for contract violations (cuDNN page "Composing multi-kernel
+  blocks", section "The shape of a block").
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+LIB_PATH = _build.LIB_PATH
+
+CCU_OK = 0
+CCU_ERR_INVALID_ARGUMENT = 1
+CCU_ERR_NOT_IMPLEMENTED = 2
+CCU_ERR_CUDA = 3
+
+CCU_ACT_IDENTITY = 0
+CCU_ACT_SILU = 1
+
+ROUTES = {"auto": 0, "scalar": 1, "vector": 2, "staged": 3, "bulk": 4}
+CCU_DEVERR_RANGE = 1
+CCU_DEVERR_DUPLICATE = 2
+
+_ACTIVATIONS = {None: CCU_ACT_IDENTITY, "identity": CCU_ACT_IDENTITY,
+                "silu": CCU_ACT_SILU, "swish": CCU_ACT_SILU}
+
+
+class CudaError(RuntimeError):
+    """A CUDA launch failed inside the library."""
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with `python -c \"import __graft_entry__ as g; g.build()\"` "
+            "(there is no CPU fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+    upd = [vp, i64, vp, i64, i64, i64, vp, vp, ctypes.c_int, vp, vp, i64, i64, i64, i64, i64, vp]
+    lib.ccu_conv1d_update.argtypes = upd + [vp]
+    lib.ccu_conv1d_update_checked.argtypes = upd + [vp, vp]
+    lib.ccu_conv1d_update_ex.argtypes = upd + [vp, i32, vp]
+    lib.ccu_conv1d_select_route.argtypes = upd + [i32, ctypes.POINTER(i32)]
+    for f in ("ccu_conv1d_update", "ccu_conv1d_update_checked", "ccu_conv1d_update_ex",
+              "ccu_conv1d_select_route", "ccu_conv1d_check_indices"):
+        getattr(lib, f).restype = ctypes.c_int
+    lib.ccu_conv1d_check_indices.argtypes = [vp, i64, i64, vp, vp, vp]
+    lib.ccu_conv1d_check_indices_scratch_bytes.argtypes = [i64]
+    lib.ccu_conv1d_check_indices_scratch_bytes.restype = i64
+    lib.ccu_status_string.argtypes = [ctypes.c_int]
+    lib.ccu_status_string.restype = ctypes.c_char_p
+    lib.ccu_route_name.argtypes = [i32]
+    lib.ccu_route_name.restype = ctypes.c_char_p
+    lib.ccu_conv1d_last_error.argtypes = []
+    lib.ccu_conv1d_last_error.restype = ctypes.c_char_p
+    lib.ccu_conv1d_abi_version.argtypes = []
+    lib.ccu_conv1d_abi_version.restype = i32
+    return lib
+
+
+lib = _load()
+
+
+# ------------------------------------------------------------------ raw C entry points
+
+def ccu_conv1d_update(x, ld, conv_state, stride_s, stride_d, stride_l, weight, bias, act, indices,
+                      cache_seqlens, N, D, S, L, W, out, stream) -> int:
+    return lib.ccu_conv1d_update(x, ld, conv_state, stride_s, stride_d, stride_l, weight, bias, act,
+                                 indices, cache_seqlens, N, D, S, L, W, out, stream)
+
+
+def ccu_conv1d_update_checked(x, ld, conv_state, stride_s, stride_d, stride_l, weight, bias, act,
+                              indices, cache_seqlens, N, D, S, L, W, out, status_dev, stream) -> int:
+    return lib.ccu_conv1d_update_checked(x, ld, conv_state, stride_s, stride_d, stride_l, weight,
+                                         bias, act, indices, cache_seqlens, N, D, S, L, W, out,
+                                         status_dev, stream)
+
+
+def ccu_conv1d_update_ex(x, ld, conv_state, stride_s, stride_d, stride_l, weight, bias, act, indices,
+                         cache_seqlens, N, D, S, L, W, out, status_dev, route, stream) -> int:
+    return lib.ccu_conv1d_update_ex(x, ld, conv_state, stride_s, stride_d, stride_l, weight, bias,
+                                    act, indices, cache_seqlens, N, D, S, L, W, out, status_dev,
+                                    route, stream)
+
+
+def ccu_conv1d_select_route(x, ld, conv_state, stride_s, stride_d, stride_l, weight, bias, act,
+                            indices, cache_seqlens, N, D, S, L, W, out, route):
+    """Returns (status, chosen_route)."""
+    chosen = ctypes.c_int32(-1)
+    st = lib.ccu_conv1d_select_route(x, ld, conv_state, stride_s, stride_d, stride_l, weight, bias,
+                                     act, indices, cache_seqlens, N, D, S, L, W, out, route,
+                                     ctypes.byref(chosen))
+    return st, chosen.value
+
+
+def ccu_conv1d_check_indices(indices, N, S, bitmap_scratch, status_dev, stream) -> int:
+    return lib.ccu_conv1d_check_indices(indices, N, S, bitmap_scratch, status_dev, stream)
+
+
+def ccu_conv1d_check_indices_scratch_bytes(S) -> int:
+    return lib.ccu_conv1d_check_indices_scratch_bytes(S)
+
+
+def ccu_status_string(status) -> str:
+    return lib.ccu_status_string(status).decode()
+
+
+def ccu_route_name(route) -> str:
+    return lib.ccu_route_name(route).decode()
+
+
+def ccu_conv1d_last_error() -> str:
+    return lib.ccu_conv1d_last_error().decode()
+
+
+def ccu_conv1d_abi_version() -> int:
+    return lib.ccu_conv1d_abi_version()
+
+
+def raise_for_status(status: int) -> None:
+    """Map a ccu_status_t to the page's typed declines."""
+    if status == CCU_OK:
+        return
+    msg = f"{ccu_status_string(status)}: {ccu_conv1d_last_error()}"
+    if status == CCU_ERR_NOT_IMPLEMENTED:
+        raise NotImplementedError(msg)
+    if status == CCU_ERR_INVALID_ARGUMENT:
+        raise ValueError(msg)
+    raise CudaError(msg)
+
+
+# ------------------------------------------------------------------ torch-level op
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _check_tensor(name, t, dtype, torch):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.requires_grad:
+        raise ValueError(f"{name} requires grad: the update is inference-only (autograd unsupported)")
+
+
+def causal_conv1d_update(x, conv_state, weight, bias=None, activation=None, *, cache_seqlens=None,
+                         conv_state_indices=None, out=None, route: str = "auto", status=None):
+    """One decode step: mutate ``conv_state`` in place and return the BF16 output ``[N, D]``.
+
+    Follows the cuDNN page "Causal Conv1d Decode Update" ("Python API" and "Semantic
+    tensor contract"): ``x`` BF16 ``[N, D]`` with strides ``(ld, 1)``; ``conv_state`` BF16
+    ``[S, D, L]``, compact or channel-last ``(L*D, 1, D)``; ``weight`` BF16 ``[D, 4]``;
+    ``bias`` BF16 ``[D]`` or None; ``activation`` None/"identity" or "silu"/"swish";
+    ``conv_state_indices`` int32 ``[N]`` (``-1`` = padding row) or None; ``cache_seqlens``
+    must be None. ``out`` (optional, preallocated ``[N, D]`` BF16), ``route`` (kernel
+    family) and ``status`` (int32 device word: turns on the device range check) are
+    extensions of this binding. Runs on the current CUDA stream.
+    """
+    import torch
+
+    if cache_seqlens is not None:
+        raise NotImplementedError("cache_seqlens must be None: circular-buffer state is not served")
+    if activation not in _ACTIVATIONS:
+        raise ValueError(f"activation must be one of None, 'identity', 'silu', 'swish'; got {activation!r}")
+    _check_tensor("x", x, torch.bfloat16, torch)
+    if x.dim() == 3:
+        raise NotImplementedError("3D x [N, D, Tstep] (multi-token update) is not served")
+    if x.dim() != 2:
+        raise ValueError(f"x must be 2D [N, D], got {x.dim()}D")
+    if x.stride(1) != 1:
+        raise ValueError("x must have unit stride along D")
+    _check_tensor("conv_state", conv_state, torch.bfloat16, torch)
+    if conv_state.dim() != 3:
+        raise ValueError("conv_state must be 3D [S, D, L]")
+    _check_tensor("weight", weight, torch.bfloat16, torch)
+    if weight.dim() != 2 or not weight.is_contiguous():
+        raise ValueError("weight must be a contiguous 2D [D, W] tensor")
+    N, D = x.shape
+    S, Ds, L = conv_state.shape
+    Dw, W = weight.shape
+    if Ds != D or Dw != D:
+        raise ValueError(f"channel counts differ: x {D}, conv_state {Ds}, weight {Dw}")
+    if bias is not None:
+        _check_tensor("bias", bias, torch.bfloat16, torch)
+        if bias.shape != (D,) or not bias.is_contiguous():
+            raise ValueError("bias must be a contiguous [D] tensor")
+    if conv_state_indices is not None:
+        _check_tensor("conv_state_indices", conv_state_indices, torch.int32, torch)
+        if conv_state_indices.shape != (N,) or not conv_state_indices.is_contiguous():
+            raise ValueError("conv_state_indices must be a contiguous int32 [N] tensor")
+    if out is None:
+        out = torch.empty((N, D), dtype=torch.bfloat16, device=x.device)
+    else:
+        _check_tensor("out", out, torch.bfloat16, torch)
+        if out.shape != (N, D) or not out.is_contiguous():
+            raise ValueError("out must be a contiguous [N, D] tensor")
+    if route not in ROUTES:
+        raise ValueError(f"route must be one of {sorted(ROUTES)}")
+    if status is not None:
+        _check_tensor("status", status, torch.int32, torch)
+    ld = x.stride(0) if N > 1 else D  # a single row's stride is never used
+    ss, sd, sl = conv_state.stride()
+    stream = torch.cuda.current_stream(x.device).cuda_stream
+    st = lib.ccu_conv1d_update_ex(
+        _ptr(x), ld, _ptr(conv_state), ss, sd, sl, _ptr(weight), _ptr(bias),
+        _ACTIVATIONS[activation], _ptr(conv_state_indices), None, N, D, S, L, W, _ptr(out),
+        _ptr(status), ROUTES[route], stream)
+    raise_for_status(st)
+    return out
+
+
+def check_indices(conv_state_indices, S: int, status=None, scratch=None):
+    """Validate slot indices on the device (range and uniqueness) without trapping.
+
+    Returns the int32 status word tensor (device); 0 means valid. Allocates the status
+    word and the bitmap scratch with torch when not given.
+    """
+    import torch
+
+    _check_tensor("conv_state_indices", conv_state_indices, torch.int32, torch)
+    dev = conv_state_indices.device
+    if status is None:
+        status = torch.zeros((1,), dtype=torch.int32, device=dev)
+    nbytes = ccu_conv1d_check_indices_scratch_bytes(S)
+    if scratch is None:
+        scratch = torch.empty((max(nbytes // 4, 1),), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    st = lib.ccu_conv1d_check_indices(_ptr(conv_state_indices), conv_state_indices.numel(), S,
+                                      _ptr(scratch), _ptr(status), stream)
+    raise_for_status(st)
+    return status

@@ -1,0 +1,318 @@
+// C-ABI entry points: argument checks (typed declines), kernel-family selection, launch.
+//
+// The contract checked here is the one of the cuDNN page "Causal Conv1d Decode Update":
+// "Semantic tensor contract" (shapes, ld rule, L >= W - 1, the two state layouts) and
+// "Current native implementation" (width four, 16-byte pointer alignment for BF16
+// tensors, 4 bytes for indices, cache_seqlens must be None). The declines follow the
+// cuDNN page "Composing multi-kernel blocks", section "The shape of a block": a contract
+// violation is CCU_ERR_INVALID_ARGUMENT, a valid but unserved request
+// CCU_ERR_NOT_IMPLEMENTED, and nothing is launched or changed in either case.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+
+#include "ccu_conv1d.h"
+#include "ccu_internal.cuh"
+
+namespace ccu {
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+thread_local char g_last_error[512];
+
+ccu_status_t fail(ccu_status_t st, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// a * b <= limit for non-negative a, b, without overflow.
+bool mul_le(int64_t a, int64_t b, int64_t limit) { return a == 0 || b <= limit / a; }
+
+struct Args {
+  const void *x;
+  int64_t ld;
+  const void *state;
+  int64_t ss, sd, sl;
+  const void *w;
+  const void *bias;
+  int act;
+  const int32_t *idx;
+  const int32_t *cache_seqlens;
+  int64_t N, D, S, L, W;
+  const void *out;
+  const int32_t *status;
+};
+
+// Every check of the contract. On CCU_OK, *noop says whether there is nothing to launch
+// and *layout which state layout the strides describe.
+ccu_status_t validate(const Args &a, bool *noop, Layout *layout) {
+  g_last_error[0] = '\0';
+  if (a.cache_seqlens != nullptr)
+    return fail(CCU_ERR_NOT_IMPLEMENTED,
+                "cache_seqlens must be NULL: circular-buffer state updates are not served");
+  if (a.act != CCU_ACT_IDENTITY && a.act != CCU_ACT_SILU)
+    return fail(CCU_ERR_INVALID_ARGUMENT, "act must be CCU_ACT_IDENTITY or CCU_ACT_SILU, got %d",
+                a.act);
+  if (a.N < 0 || a.D < 0 || a.S < 0)
+    return fail(CCU_ERR_INVALID_ARGUMENT, "N, D and S must be >= 0");
+  if (a.W < 1) return fail(CCU_ERR_INVALID_ARGUMENT, "W must be >= 1, got %lld", (long long)a.W);
+  if (a.L < a.W - 1)
+    return fail(CCU_ERR_INVALID_ARGUMENT, "L must be >= W - 1 (L=%lld, W=%lld)", (long long)a.L,
+                (long long)a.W);
+  if (a.W != kW)
+    return fail(CCU_ERR_NOT_IMPLEMENTED, "only width W == 4 is served, got W=%lld",
+                (long long)a.W);
+  if (a.status != nullptr && !aligned(a.status, 4))
+    return fail(CCU_ERR_INVALID_ARGUMENT, "status word must be 4-byte aligned");
+  if (a.N == 0 || a.D == 0) {
+    *noop = true;  // nothing to read or write, whatever the strides
+    return CCU_OK;
+  }
+  *noop = false;
+  if (a.ld < a.D)
+    return fail(CCU_ERR_INVALID_ARGUMENT, "ld must be >= D (ld=%lld, D=%lld)", (long long)a.ld,
+                (long long)a.D);
+  if (a.ld > a.D && a.ld % 8 != 0)
+    return fail(CCU_ERR_INVALID_ARGUMENT,
+                "a padded row stride ld > D must be a multiple of 8, got ld=%lld", (long long)a.ld);
+  if (a.x == nullptr || a.w == nullptr || a.out == nullptr || (a.state == nullptr && a.S > 0))
+    return fail(CCU_ERR_INVALID_ARGUMENT, "x, conv_state, weight and out must not be NULL");
+  if (!aligned(a.x, 16) || !aligned(a.state, 16) || !aligned(a.w, 16) || !aligned(a.out, 16) ||
+      (a.bias != nullptr && !aligned(a.bias, 16)))
+    return fail(CCU_ERR_INVALID_ARGUMENT, "BF16 tensors must be 16-byte aligned");
+  if (a.idx != nullptr && !aligned(a.idx, 4))
+    return fail(CCU_ERR_INVALID_ARGUMENT, "conv_state_indices must be 4-byte aligned");
+  if (a.idx == nullptr && a.S < a.N)
+    return fail(CCU_ERR_INVALID_ARGUMENT,
+                "without conv_state_indices row n uses slot n, so S must be >= N (S=%lld, N=%lld)",
+                (long long)a.S, (long long)a.N);
+  const int64_t lim = INT64_MAX / 4;
+  if (!mul_le(a.N, a.ld, lim) || !mul_le(a.D, a.L, lim) || !mul_le(a.S, a.D * a.L, lim))
+    return fail(CCU_ERR_INVALID_ARGUMENT, "tensor sizes overflow 64-bit indexing");
+  if (a.ss == a.D * a.L && a.sd == a.L && a.sl == 1) {
+    *layout = Layout::Compact;
+  } else if (a.ss == a.L * a.D && a.sd == 1 && a.sl == a.D) {
+    *layout = Layout::ChannelLast;
+  } else {
+    return fail(CCU_ERR_NOT_IMPLEMENTED,
+                "conv_state strides (%lld, %lld, %lld) are neither compact (D*L, L, 1) nor "
+                "channel-last (L*D, 1, D)",
+                (long long)a.ss, (long long)a.sd, (long long)a.sl);
+  }
+  return CCU_OK;
+}
+
+bool route_serves(int route, const Args &a, Layout layout) {
+  const bool vec8 = (a.D % 8 == 0) && (a.ld % 8 == 0);
+  switch (route) {
+    case CCU_ROUTE_SCALAR: return true;
+    case CCU_ROUTE_VECTOR: return vec8 && a.L <= kVectorMaxL;
+    case CCU_ROUTE_STAGED: return vec8 && a.L <= kStagedMaxL;
+    case CCU_ROUTE_BULK: return false;  // not built
+    default: return false;
+  }
+  (void)layout;
+}
+
+ccu_status_t choose(int requested, const Args &a, Layout layout, int *chosen) {
+  if (requested < 0 || requested >= CCU_ROUTE_COUNT)
+    return fail(CCU_ERR_INVALID_ARGUMENT, "unknown route %d", requested);
+  if (requested == CCU_ROUTE_AUTO) {
+    if (route_serves(CCU_ROUTE_VECTOR, a, layout)) {
+      *chosen = CCU_ROUTE_VECTOR;
+    } else if (route_serves(CCU_ROUTE_STAGED, a, layout)) {
+      *chosen = CCU_ROUTE_STAGED;
+    } else {
+      *chosen = CCU_ROUTE_SCALAR;
+    }
+    return CCU_OK;
+  }
+  if (!route_serves(requested, a, layout))
+    return fail(CCU_ERR_NOT_IMPLEMENTED, "route '%s' does not serve these arguments",
+                ccu_route_name(requested));
+  *chosen = requested;
+  return CCU_OK;
+}
+
+ccu_status_t run(const Args &a, int route, cudaStream_t stream) {
+  bool noop = false;
+  Layout layout = Layout::Compact;
+  ccu_status_t st = validate(a, &noop, &layout);
+  if (st != CCU_OK || noop) return st;
+  int chosen = CCU_ROUTE_AUTO;
+  st = choose(route, a, layout, &chosen);
+  if (st != CCU_OK) return st;
+
+  UpdateParams p;
+  p.x = static_cast<const uint16_t *>(a.x);
+  p.ld = a.ld;
+  p.state = static_cast<uint16_t *>(const_cast<void *>(a.state));
+  p.w = static_cast<const uint16_t *>(a.w);
+  p.bias = static_cast<const uint16_t *>(a.bias);
+  p.idx = a.idx;
+  p.out = static_cast<uint16_t *>(const_cast<void *>(a.out));
+  p.status = const_cast<int32_t *>(a.status);
+  p.N = a.N;
+  p.D = a.D;
+  p.S = a.S;
+  p.L = a.L;
+  p.ss = a.ss;
+  p.sd = a.sd;
+  p.sl = a.sl;
+  p.layout = (int)layout;
+  p.rows_per_cta = 1;
+
+  cudaError_t e = cudaErrorInvalidValue;
+  switch (chosen) {
+    case CCU_ROUTE_SCALAR: e = launch_scalar(p, a.act, stream); break;
+    case CCU_ROUTE_VECTOR: e = launch_vector(p, a.act, stream); break;
+    case CCU_ROUTE_STAGED: e = launch_staged(p, a.act, stream); break;
+    default: break;
+  }
+  if (e != cudaSuccess)
+    return fail(CCU_ERR_CUDA, "launch of the %s kernel failed: %s", ccu_route_name(chosen),
+                cudaGetErrorString(e));
+  return CCU_OK;
+}
+
+}  // namespace
+
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  return dev;
+}
+
+int device_sm_count() {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return 1;
+  int v = g_sm_count[dev].load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+    return 1;
+  g_sm_count[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
+}  // namespace ccu
+
+using ccu::Args;
+
+extern "C" {
+
+ccu_status_t ccu_conv1d_update_ex(const void *x, int64_t ld, void *conv_state, int64_t stride_s,
+                                  int64_t stride_d, int64_t stride_l, const void *weight,
+                                  const void *bias, ccu_act_t act, const int32_t *indices,
+                                  const int32_t *cache_seqlens, int64_t N, int64_t D, int64_t S,
+                                  int64_t L, int64_t W, void *out, int32_t *status_dev,
+                                  int32_t route, ccu_stream_t stream) {
+  const Args a{x,    ld,      conv_state, stride_s,      stride_d, stride_l, weight, bias,
+               (int)act, indices, cache_seqlens, N, D, S, L, W, out, status_dev};
+  return ccu::run(a, route, reinterpret_cast<cudaStream_t>(stream));
+}
+
+ccu_status_t ccu_conv1d_update(const void *x, int64_t ld, void *conv_state, int64_t stride_s,
+                               int64_t stride_d, int64_t stride_l, const void *weight,
+                               const void *bias, ccu_act_t act, const int32_t *indices,
+                               const int32_t *cache_seqlens, int64_t N, int64_t D, int64_t S,
+                               int64_t L, int64_t W, void *out, ccu_stream_t stream) {
+  return ccu_conv1d_update_ex(x, ld, conv_state, stride_s, stride_d, stride_l, weight, bias, act,
+                              indices, cache_seqlens, N, D, S, L, W, out, nullptr,
+                              CCU_ROUTE_AUTO, stream);
+}
+
+ccu_status_t ccu_conv1d_update_checked(const void *x, int64_t ld, void *conv_state,
+                                       int64_t stride_s, int64_t stride_d, int64_t stride_l,
+                                       const void *weight, const void *bias, ccu_act_t act,
+                                       const int32_t *indices, const int32_t *cache_seqlens,
+                                       int64_t N, int64_t D, int64_t S, int64_t L, int64_t W,
+                                       void *out, int32_t *status_dev, ccu_stream_t stream) {
+  if (status_dev == nullptr)
+    return ccu::fail(CCU_ERR_INVALID_ARGUMENT, "status_dev must not be NULL");
+  return ccu_conv1d_update_ex(x, ld, conv_state, stride_s, stride_d, stride_l, weight, bias, act,
+                              indices, cache_seqlens, N, D, S, L, W, out, status_dev,
+                              CCU_ROUTE_AUTO, stream);
+}
+
+ccu_status_t ccu_conv1d_select_route(const void *x, int64_t ld, const void *conv_state,
+                                     int64_t stride_s, int64_t stride_d, int64_t stride_l,
+                                     const void *weight, const void *bias, ccu_act_t act,
+                                     const int32_t *indices, const int32_t *cache_seqlens,
+                                     int64_t N, int64_t D, int64_t S, int64_t L, int64_t W,
+                                     const void *out, int32_t route, int32_t *chosen_route) {
+  if (chosen_route == nullptr)
+    return ccu::fail(CCU_ERR_INVALID_ARGUMENT, "chosen_route must not be NULL");
+  const Args a{x,    ld,      conv_state, stride_s,      stride_d, stride_l, weight, bias,
+               (int)act, indices, cache_seqlens, N, D, S, L, W, out, nullptr};
+  bool noop = false;
+  ccu::Layout layout = ccu::Layout::Compact;
+  ccu_status_t st = ccu::validate(a, &noop, &layout);
+  if (st != CCU_OK) return st;
+  if (noop) {
+    *chosen_route = CCU_ROUTE_AUTO;
+    return CCU_OK;
+  }
+  int chosen = CCU_ROUTE_AUTO;
+  st = ccu::choose(route, a, layout, &chosen);
+  if (st == CCU_OK) *chosen_route = chosen;
+  return st;
+}
+
+int64_t ccu_conv1d_check_indices_scratch_bytes(int64_t S) {
+  if (S <= 0) return 0;
+  return ((S + 31) / 32) * 4;
+}
+
+ccu_status_t ccu_conv1d_check_indices(const int32_t *indices, int64_t N, int64_t S,
+                                      uint32_t *bitmap_scratch, int32_t *status_dev,
+                                      ccu_stream_t stream) {
+  ccu::g_last_error[0] = '\0';
+  if (N < 0 || S < 0) return ccu::fail(CCU_ERR_INVALID_ARGUMENT, "N and S must be >= 0");
+  if (N == 0) return CCU_OK;
+  if (indices == nullptr || status_dev == nullptr || (S > 0 && bitmap_scratch == nullptr))
+    return ccu::fail(CCU_ERR_INVALID_ARGUMENT, "indices, bitmap_scratch and status_dev must not be NULL");
+  if (!ccu::aligned(indices, 4) || !ccu::aligned(status_dev, 4) ||
+      !ccu::aligned(bitmap_scratch, 4))
+    return ccu::fail(CCU_ERR_INVALID_ARGUMENT, "indices, bitmap_scratch and status_dev must be 4-byte aligned");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  const int64_t bytes = ccu_conv1d_check_indices_scratch_bytes(S);
+  if (bytes > 0) e = cudaMemsetAsync(bitmap_scratch, 0, (size_t)bytes, s);
+  if (e == cudaSuccess) e = ccu::launch_check_indices(indices, N, S, bitmap_scratch, status_dev, s);
+  if (e != cudaSuccess)
+    return ccu::fail(CCU_ERR_CUDA, "index check failed to launch: %s", cudaGetErrorString(e));
+  return CCU_OK;
+}
+
+const char *ccu_status_string(ccu_status_t status) {
+  switch (status) {
+    case CCU_OK: return "ok";
+    case CCU_ERR_INVALID_ARGUMENT: return "invalid argument (contract violation)";
+    case CCU_ERR_NOT_IMPLEMENTED: return "not implemented (valid but not served)";
+    case CCU_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+const char *ccu_route_name(int32_t route) {
+  switch (route) {
+    case CCU_ROUTE_AUTO: return "auto";
+    case CCU_ROUTE_SCALAR: return "scalar";
+    case CCU_ROUTE_VECTOR: return "vector";
+    case CCU_ROUTE_STAGED: return "staged";
+    case CCU_ROUTE_BULK: return "bulk";
+    default: return "unknown";
+  }
+}
+
+const char *ccu_conv1d_last_error(void) { return ccu::g_last_error; }
+
+int32_t ccu_conv1d_abi_version(void) { return CCU_CONV1D_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,94 @@
+// Scalar kernels: the correctness anchor of the update (any D, any ld, any L >= 3, both
+// state layouts through explicit strides) and the index checker.
+//
+// Update definition: cuDNN page "Causal Conv1d Decode Update", introduction (update
+// block) and the conv_state_indices paragraph.
+#include "ccu_internal.cuh"
+
+namespace ccu {
+
+int device_sm_count();
+
+namespace {
+
+// One thread per (row, channel), grid-stride. Each thread reads the three newest state
+// entries and x, computes the output, then shifts its own channel's state in place.
+template <int ACT>
+__global__ void __launch_bounds__(256) k_update_scalar(UpdateParams p) {
+  const int64_t total = p.N * p.D;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t n = i / p.D;
+    const int64_t d = i - n * p.D;
+    const int64_t s = resolve_slot(p, n);
+    if (s < 0) {
+      p.out[n * p.D + d] = 0;  // padding row: +0, no state access
+      continue;
+    }
+    uint16_t *st = p.state + s * p.ss + d * p.sd;
+    const int64_t L = p.L;
+    const uint16_t xv = p.x[n * p.ld + d];
+    // history = [st[0], ..., st[L-1], x]; the width-4 window is its last four entries.
+    const uint16_t h0 = st[(L - 3) * p.sl];
+    const uint16_t h1 = st[(L - 2) * p.sl];
+    const uint16_t h2 = st[(L - 1) * p.sl];
+    const uint16_t *w = p.w + d * kW;
+    float acc = 0.0f;
+    acc = __fmaf_rn(bf16_bits(h0), bf16_bits(w[0]), acc);
+    acc = __fmaf_rn(bf16_bits(h1), bf16_bits(w[1]), acc);
+    acc = __fmaf_rn(bf16_bits(h2), bf16_bits(w[2]), acc);
+    acc = __fmaf_rn(bf16_bits(xv), bf16_bits(w[3]), acc);
+    if (p.bias != nullptr) acc = acc + bf16_bits(p.bias[d]);
+    p.out[n * p.D + d] = round_bf16(activate<ACT>(acc));
+    // conv_state[s, d, :] = history[1:], ascending so every entry is read before overwritten
+    for (int64_t l = 0; l + 1 < L; ++l) st[l * p.sl] = st[(l + 1) * p.sl];
+    st[(L - 1) * p.sl] = xv;
+  }
+}
+
+// Marks each non-padding slot in a bitmap; a slot seen twice, or out of range, raises a
+// bit in *status. No trap, no wait.
+__global__ void __launch_bounds__(256) k_check_indices(const int32_t *idx, int64_t N, int64_t S,
+                                                       uint32_t *bitmap, int32_t *status) {
+  for (int64_t n = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; n < N;
+       n += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t s = idx[n];
+    if (s == -1) continue;
+    if (s < -1 || s >= S) {
+      atomicOr(status, 1);  // CCU_DEVERR_RANGE
+      continue;
+    }
+    const uint32_t bit = 1u << (s & 31);
+    const uint32_t old = atomicOr(bitmap + (s >> 5), bit);
+    if (old & bit) atomicOr(status, 2);  // CCU_DEVERR_DUPLICATE
+  }
+}
+
+int64_t grid_for(int64_t work, int threads) {
+  const int64_t blocks = (work + threads - 1) / threads;
+  const int64_t cap = (int64_t)device_sm_count() * 16;
+  return blocks < cap ? (blocks > 0 ? blocks : 1) : cap;
+}
+
+}  // namespace
+
+cudaError_t launch_scalar(const UpdateParams &p, int act, cudaStream_t stream) {
+  const int threads = 256;
+  const dim3 grid((unsigned)grid_for(p.N * p.D, threads));
+  if (act == 1) {
+    k_update_scalar<1><<<grid, threads, 0, stream>>>(p);
+  } else {
+    k_update_scalar<0><<<grid, threads, 0, stream>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_check_indices(const int32_t *idx, int64_t N, int64_t S, uint32_t *bitmap,
+                                 int32_t *status, cudaStream_t stream) {
+  const int threads = 256;
+  const dim3 grid((unsigned)grid_for(N, threads));
+  k_check_indices<<<grid, threads, 0, stream>>>(idx, N, S, bitmap, status);
+  return cudaGetLastError();
+}
+
+}  // namespace ccu

@@ -1,0 +1,217 @@
+/*
+ * ccu_conv1d -- depthwise causal conv1d decode update for NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the decode step of a depthwise causal convolution with a
+ * mutable state cache, as defined on the cuDNN page "Causal Conv1d Decode Update"
+ * (introduction, update block). For every row n and channel d with slot s:
+ *
+ *     history            = concat(conv_state[s, d, :], x[n, d])        (L + 1 values)
+ *     conv_state[s, d, :] = history[-L:]                                 (in place)
+ *     acc                = sum_{j=0}^{W-1} history[-W + j] * weight[d, j] + bias[d]
+ *     out[n, d]          = activation(acc)
+ *
+ * s = n when indices is NULL, else s = indices[n]; s == -1 marks a padding row whose
+ * output is +0 and which reads and writes no state (same page, paragraph on
+ * conv_state_indices). The bias is zero when omitted; identity and SiLU are the two
+ * activations and are compiled as separate kernels (paragraph after the update block).
+ *
+ * Numerics: BF16 storage, FP32 accumulation in ascending tap order (j = 0..W-1, each
+ * term a product of the two widened BF16 values, fused multiply-add allowed because a
+ * BF16 x BF16 product is exact in FP32), bias added last, SiLU as a / (1 + exp(-a)) in
+ * FP32, output rounded to BF16 to nearest-even. The state update is a bit copy.
+ *
+ * Conventions shared by every entry point below:
+ *  - All tensor pointers are DEVICE memory owned by the caller. The library never
+ *    allocates, frees, copies between host and device or synchronizes; every call only
+ *    enqueues kernels (and, for ccu_conv1d_check_indices, one memset) on `stream`, so a
+ *    call can be captured in a CUDA graph. Launch errors are reported as CCU_ERR_CUDA;
+ *    errors of the asynchronous execution surface at the caller's next synchronization.
+ *  - `stream` is a cudaStream_t; NULL is the legacy default stream.
+ *  - BF16 tensors are passed as `const void*` / `void*` to 16-bit storage.
+ *  - Every argument check happens before any launch; a declined call changes nothing.
+ *  - Sizes are elements, not bytes. Strides are elements.
+ *  - The functions are thread-safe; ccu_conv1d_last_error() is per calling thread.
+ */
+#ifndef CCU_CONV1D_H
+#define CCU_CONV1D_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CCU_CONV1D_ABI_VERSION 1
+
+/* Every entry point is exported from the shared library (the rest is hidden). */
+#if defined(__GNUC__)
+#define CCU_API __attribute__((visibility("default")))
+#else
+#define CCU_API
+#endif
+
+/* Same type as cudaStream_t; declared here so this header needs no CUDA header. */
+typedef struct CUstream_st *ccu_stream_t;
+
+/* Status of a call. The two declines mirror the typed declines of the cuDNN page
+ * "Composing multi-kernel blocks" (section "The shape of a block"): a contract
+ * violation versus a valid request that this library does not serve. */
+typedef enum ccu_status {
+  CCU_OK = 0,
+  CCU_ERR_INVALID_ARGUMENT = 1, /* the arguments break the tensor contract */
+  CCU_ERR_NOT_IMPLEMENTED = 2,  /* valid, but not served (e.g. cache_seqlens != NULL) */
+  CCU_ERR_CUDA = 3              /* a CUDA launch or runtime call failed */
+} ccu_status_t;
+
+/* Activation. "identity" (or none) and "silu"/"swish" on the page map to these. */
+typedef enum ccu_act { CCU_ACT_IDENTITY = 0, CCU_ACT_SILU = 1 } ccu_act_t;
+
+/* Kernel families, for ccu_conv1d_update_ex and ccu_conv1d_select_route. AUTO lets the
+ * library choose; the others force one family and decline (CCU_ERR_NOT_IMPLEMENTED)
+ * when it cannot serve the arguments. */
+typedef enum ccu_route {
+  CCU_ROUTE_AUTO = 0,
+  CCU_ROUTE_SCALAR = 1, /* one thread per (row, channel); any D, ld, L and layout */
+  CCU_ROUTE_VECTOR = 2, /* 8 channels per thread, 16-byte vectors; D % 8 == 0, L <= 8 */
+  CCU_ROUTE_STAGED = 3, /* shared-memory staged tiles; D % 8 == 0, any L <= 256 */
+  CCU_ROUTE_BULK = 4,   /* persistent CTAs, bulk async copies through shared memory;
+                           compact layout, D % 8 == 0, L <= 8 */
+  CCU_ROUTE_COUNT = 5
+} ccu_route_t;
+
+/* Bits ORed into the device status word by the checked entry points. */
+#define CCU_DEVERR_RANGE 1     /* a slot index < -1 or >= S */
+#define CCU_DEVERR_DUPLICATE 2 /* a non-padding slot used by more than one row */
+
+/*
+ * ccu_conv1d_update -- one decode step, in place on conv_state.
+ *
+ * Defined by the update block in the introduction of "Causal Conv1d Decode Update";
+ * argument meanings follow its "Semantic tensor contract" and the served subset in
+ * "Current native implementation".
+ *
+ *   x           BF16, logical [N, D], element (n, d) at x[n * ld + d]. 16-byte aligned.
+ *   ld          row stride of x in elements: ld == D (any D), or ld > D with ld % 8 == 0.
+ *               Columns D..ld-1 are never read.
+ *   conv_state  BF16, logical [S, D, L], element (s, d, l) at
+ *               conv_state[s * stride_s + d * stride_d + l * stride_l]; updated in place.
+ *               Two layouts are served: compact (stride_s, stride_d, stride_l) =
+ *               (D * L, L, 1), and channel-last (L * D, 1, D), the layout of the final
+ *               state of a full-sequence prefill. 16-byte aligned.
+ *   weight      BF16, contiguous [D, W]. 16-byte aligned.
+ *   bias        BF16, contiguous [D], or NULL for no bias. 16-byte aligned.
+ *   act         CCU_ACT_IDENTITY or CCU_ACT_SILU.
+ *   indices     int32 [N] slot per row, or NULL (row n uses slot n, which needs S >= N).
+ *               -1 marks a padding row. Every other value must lie in [0, S) and appear
+ *               at most once: these two preconditions are NOT checked here (use
+ *               ccu_conv1d_update_checked / ccu_conv1d_check_indices). A repeated slot
+ *               gives an unspecified state for that slot; an out-of-range one is
+ *               undefined behaviour. 4-byte aligned.
+ *   cache_seqlens  reserved for a circular-buffer state; must be NULL (otherwise
+ *               CCU_ERR_NOT_IMPLEMENTED, as on the page).
+ *   N, D, S     rows, channels, cache slots. N == 0 or D == 0 is a no-op.
+ *   L, W        state length and filter width, L >= W - 1. Served: W == 4, any L >= 3.
+ *   out         BF16, contiguous [N, D], written for every row (+0 for padding rows).
+ *               16-byte aligned; must not overlap any input.
+ *
+ * Returns CCU_OK after enqueueing, CCU_ERR_INVALID_ARGUMENT / CCU_ERR_NOT_IMPLEMENTED
+ * without enqueueing anything, or CCU_ERR_CUDA if the launch failed.
+ */
+CCU_API ccu_status_t ccu_conv1d_update(const void *x, int64_t ld, void *conv_state, int64_t stride_s,
+                               int64_t stride_d, int64_t stride_l, const void *weight,
+                               const void *bias, ccu_act_t act, const int32_t *indices,
+                               const int32_t *cache_seqlens, int64_t N, int64_t D, int64_t S,
+                               int64_t L, int64_t W, void *out, ccu_stream_t stream);
+
+/*
+ * ccu_conv1d_update_checked -- ccu_conv1d_update that range-checks every slot on the
+ * device instead of trusting it.
+ *
+ * The page's kernel traps on an index below -1 or past the cache ("Current native
+ * implementation", last paragraph); a trap kills the CUDA context, so this library
+ * reports instead: a row whose slot is < -1 or >= S is treated as a padding row (output
+ * +0, no state access) and CCU_DEVERR_RANGE is ORed into *status_dev. Duplicate slots
+ * are not detected here (see ccu_conv1d_check_indices).
+ *
+ *   status_dev  device int32 word, not cleared by the call: errors accumulate until the
+ *               caller resets it. 4-byte aligned, must not be NULL.
+ * Other arguments and returns as ccu_conv1d_update.
+ */
+CCU_API ccu_status_t ccu_conv1d_update_checked(const void *x, int64_t ld, void *conv_state,
+                                       int64_t stride_s, int64_t stride_d, int64_t stride_l,
+                                       const void *weight, const void *bias, ccu_act_t act,
+                                       const int32_t *indices, const int32_t *cache_seqlens,
+                                       int64_t N, int64_t D, int64_t S, int64_t L, int64_t W,
+                                       void *out, int32_t *status_dev, ccu_stream_t stream);
+
+/*
+ * ccu_conv1d_update_ex -- the update with an explicit kernel family (for tests and A/B
+ * benchmarks of the families on the same inputs).
+ *
+ *   status_dev  NULL for the unchecked update, else as in ccu_conv1d_update_checked.
+ *   route       a ccu_route_t; a forced family that cannot serve the arguments returns
+ *               CCU_ERR_NOT_IMPLEMENTED without launching.
+ * Other arguments and returns as ccu_conv1d_update.
+ */
+CCU_API ccu_status_t ccu_conv1d_update_ex(const void *x, int64_t ld, void *conv_state, int64_t stride_s,
+                                  int64_t stride_d, int64_t stride_l, const void *weight,
+                                  const void *bias, ccu_act_t act, const int32_t *indices,
+                                  const int32_t *cache_seqlens, int64_t N, int64_t D, int64_t S,
+                                  int64_t L, int64_t W, void *out, int32_t *status_dev,
+                                  int32_t route, ccu_stream_t stream);
+
+/*
+ * ccu_conv1d_select_route -- run every argument check of ccu_conv1d_update_ex and report,
+ * in *chosen_route, the kernel family a call with these arguments would launch. Touches no
+ * memory behind the pointers and makes no CUDA call, so it also works without a GPU.
+ *
+ *   chosen_route  host int32 out-parameter; set only when CCU_OK is returned (to
+ *                 CCU_ROUTE_AUTO for a no-op call with N == 0 or D == 0).
+ */
+CCU_API ccu_status_t ccu_conv1d_select_route(const void *x, int64_t ld, const void *conv_state,
+                                     int64_t stride_s, int64_t stride_d, int64_t stride_l,
+                                     const void *weight, const void *bias, ccu_act_t act,
+                                     const int32_t *indices, const int32_t *cache_seqlens,
+                                     int64_t N, int64_t D, int64_t S, int64_t L, int64_t W,
+                                     const void *out, int32_t route, int32_t *chosen_route);
+
+/*
+ * ccu_conv1d_check_indices -- validate a slot-index vector on the device without trapping.
+ *
+ * Checks the two preconditions of the conv_state_indices paragraph of "Causal Conv1d
+ * Decode Update": every non-padding slot in [0, S) (else CCU_DEVERR_RANGE) and used by
+ * one row only (else CCU_DEVERR_DUPLICATE); any number of -1 rows is allowed.
+ *
+ *   indices         device int32 [N], 4-byte aligned.
+ *   bitmap_scratch  device scratch of ccu_conv1d_check_indices_scratch_bytes(S) bytes,
+ *                   4-byte aligned, owned by the caller; the call clears it itself
+ *                   (cudaMemsetAsync on `stream`) before use and leaves it dirty.
+ *   status_dev      device int32 word; error bits are ORed in, never cleared.
+ * N == 0 is a no-op. Calls that share a scratch buffer must not overlap on the GPU.
+ */
+CCU_API ccu_status_t ccu_conv1d_check_indices(const int32_t *indices, int64_t N, int64_t S,
+                                      uint32_t *bitmap_scratch, int32_t *status_dev,
+                                      ccu_stream_t stream);
+
+/* Bytes of scratch ccu_conv1d_check_indices needs for S slots (one bit per slot, rounded
+ * up to whole 32-bit words); 0 for S <= 0. */
+CCU_API int64_t ccu_conv1d_check_indices_scratch_bytes(int64_t S);
+
+/* Static English text for a status code. Never NULL. */
+CCU_API const char *ccu_status_string(ccu_status_t status);
+
+/* Static name of a kernel family ("auto", "scalar", "vector", "staged", "bulk"). */
+CCU_API const char *ccu_route_name(int32_t route);
+
+/* Message of the last failed call on the calling thread (empty string if none). The
+ * pointer stays valid until the thread's next call into this library. */
+CCU_API const char *ccu_conv1d_last_error(void);
+
+/* CCU_CONV1D_ABI_VERSION of the loaded library. */
+CCU_API int32_t ccu_conv1d_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CCU_CONV1D_H */

@@ -160,14 +160,16 @@ def run_workload(inp, layout: str = "compact", *, with_acc: bool = False, lib=No
         state = inp.conv_state.copy()
         strides = (D * L, L, 1)
     elif layout == "channel_last":
-        state = np.ascontiguousarray(np.transpose(inp.conv_state, (0, 2, 1)))
+        # np.array(copy=True): never a view, even when a size-1 axis makes the transpose
+        # look contiguous (the oracle writes into this array)
+        state = np.array(np.transpose(inp.conv_state, (0, 2, 1)), order="C", copy=True)
         strides = (L * D, 1, D)
     else:
         raise ValueError(layout)
     res = conv1d_update(inp.x, wl.ld, state, strides, inp.weight, inp.bias, wl.act, inp.indices,
                         wl.N, D, S, L, wl.W, with_acc=with_acc, lib=lib)
     if layout == "channel_last":
-        state = np.ascontiguousarray(np.transpose(state, (0, 2, 1)))
+        state = np.array(np.transpose(state, (0, 2, 1)), order="C", copy=True)
     if with_acc:
         return res[0], state, res[1]
     return res, state

@@ -137,13 +137,16 @@ def make_indices(rng: np.random.Generator, kind: str, N: int, S: int, pad_frac: 
 
 
 def to_channel_last(state: np.ndarray) -> np.ndarray:
-    """Store a logical [S, D, L] state as [S, L, D] memory: element strides (L*D, 1, D)."""
-    return np.ascontiguousarray(np.transpose(state, (0, 2, 1)))
+    """Store a logical [S, D, L] state as [S, L, D] memory: element strides (L*D, 1, D).
+
+    Always a fresh array (a transpose with a size-1 axis would otherwise come back as a
+    view sharing memory with ``state``)."""
+    return np.array(np.transpose(state, (0, 2, 1)), order="C", copy=True)
 
 
 def from_channel_last(storage: np.ndarray) -> np.ndarray:
-    """Inverse of to_channel_last: [S, L, D] memory back to a logical [S, D, L] array."""
-    return np.ascontiguousarray(np.transpose(storage, (0, 2, 1)))
+    """Inverse of to_channel_last: [S, L, D] memory back to a logical [S, D, L] array (a copy)."""
+    return np.array(np.transpose(storage, (0, 2, 1)), order="C", copy=True)
 
 
 @dataclasses.dataclass

@@ -1,0 +1,186 @@
+"""The C-ABI library without a GPU: exports, typed declines, route selection.
+
+The argument checks are host code that runs before any CUDA call, so they are tested
+here through ccu_conv1d_select_route, which never launches. Calls of the launching
+entry points with placeholder pointers are made only when no GPU is visible (the
+launch then fails with CCU_ERR_CUDA and touches nothing).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def ccu():
+    import __graft_entry__ as g
+
+    g.build()
+    import depthwise_causal_conv1d_gb300 as ccu
+
+    return ccu
+
+
+def declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"^CCU_API\s+[\w\s\*]+?\b(ccu_\w+)\s*\(", text, flags=re.M)
+    return names
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for must in ("ccu_conv1d_update", "ccu_conv1d_update_checked", "ccu_conv1d_update_ex",
+                 "ccu_conv1d_select_route", "ccu_conv1d_check_indices", "ccu_status_string"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(ccu):
+    lib = ctypes.CDLL(ccu.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, f"declared but not exported: {missing}"
+
+
+def test_binding_has_same_names(ccu):
+    for n in declared_functions():
+        assert callable(getattr(ccu, n)), n
+
+
+def test_header_compiles_as_c(tmp_path):
+    src = tmp_path / "t.c"
+    src.write_text('#include "ccu_conv1d.h"\nint main(void){return CCU_OK;}\n')
+    import subprocess
+
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    "-c", str(src), "-o", str(tmp_path / "t.o")], check=True)
+
+
+def test_status_strings(ccu):
+    assert ccu.ccu_status_string(0) == "ok"
+    assert "invalid" in ccu.ccu_status_string(1)
+    assert "not implemented" in ccu.ccu_status_string(2)
+    assert ccu.ccu_status_string(99) == "unknown status"
+    assert [ccu.ccu_route_name(r) for r in range(5)] == ["auto", "scalar", "vector", "staged", "bulk"]
+    assert ccu.ccu_conv1d_abi_version() == 1
+    assert ccu.ccu_conv1d_check_indices_scratch_bytes(0) == 0
+    assert ccu.ccu_conv1d_check_indices_scratch_bytes(1) == 4
+    assert ccu.ccu_conv1d_check_indices_scratch_bytes(32) == 4
+    assert ccu.ccu_conv1d_check_indices_scratch_bytes(33) == 8
+
+
+# placeholder device addresses: aligned, never dereferenced (select_route does not launch)
+X, ST, WT, BS, OUT, IDX = 0x100000, 0x200000, 0x300000, 0x400000, 0x500000, 0x600000
+
+
+def args(**kw):
+    a = dict(x=X, ld=None, conv_state=ST, stride_s=None, stride_d=None, stride_l=None, weight=WT,
+             bias=BS, act=0, indices=None, cache_seqlens=None, N=4, D=64, S=4, L=3, W=4, out=OUT)
+    a.update(kw)
+    if a["ld"] is None:
+        a["ld"] = a["D"]
+    if a["stride_s"] is None:
+        a["stride_s"], a["stride_d"], a["stride_l"] = a["D"] * a["L"], a["L"], 1
+    return a
+
+
+def select(ccu, route=0, **kw):
+    a = args(**kw)
+    return ccu.ccu_conv1d_select_route(*a.values(), route)
+
+
+DECLINES = [
+    ("cache_seqlens", dict(cache_seqlens=0x700000), 2, "cache_seqlens"),
+    ("width 3", dict(W=3, L=3), 2, "W == 4"),
+    ("width 2", dict(W=2, L=1), 2, "W == 4"),
+    ("L < W-1", dict(L=2), 1, "L must be >= W - 1"),
+    ("ld < D", dict(ld=32), 1, "ld must be >= D"),
+    ("padded ld not multiple of 8", dict(ld=68), 1, "multiple of 8"),
+    ("act out of range", dict(act=2), 1, "act"),
+    ("negative N", dict(N=-1), 1, ">= 0"),
+    ("W = 0", dict(W=0), 1, "W must be >= 1"),
+    ("null x", dict(x=None), 1, "NULL"),
+    ("null weight", dict(weight=None), 1, "NULL"),
+    ("null out", dict(out=None), 1, "NULL"),
+    ("misaligned x", dict(x=X + 2), 1, "16-byte"),
+    ("misaligned state", dict(conv_state=ST + 8), 1, "16-byte"),
+    ("misaligned weight", dict(weight=WT + 4), 1, "16-byte"),
+    ("misaligned bias", dict(bias=BS + 2), 1, "16-byte"),
+    ("misaligned out", dict(out=OUT + 14), 1, "16-byte"),
+    ("misaligned indices", dict(indices=IDX + 2), 1, "4-byte"),
+    ("S < N without indices", dict(S=3), 1, "S must be >= N"),
+    ("strides of another layout", dict(stride_s=64 * 3, stride_d=1, stride_l=128), 2, "strides"),
+    ("transposed slots", dict(stride_s=3, stride_d=12, stride_l=1), 2, "strides"),
+]
+
+
+@pytest.mark.parametrize("name,kw,code,msg", DECLINES, ids=[d[0] for d in DECLINES])
+def test_decline(ccu, name, kw, code, msg):
+    st, _ = select(ccu, **kw)
+    assert st == code, (name, st, ccu.ccu_conv1d_last_error())
+    assert msg in ccu.ccu_conv1d_last_error()
+
+
+def test_decline_from_launching_entry_points_without_gpu(ccu):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("launching entries are exercised with real tensors by the GPU tests")
+    for name, kw, code, msg in DECLINES:
+        a = args(**kw)
+        assert ccu.ccu_conv1d_update(*a.values(), None) == code, name
+        assert ccu.ccu_conv1d_update_checked(*a.values(), 0x800000, None) == code, name
+        assert msg in ccu.ccu_conv1d_last_error()
+    # a valid call cannot launch without a GPU: CUDA error, nothing else
+    assert ccu.ccu_conv1d_update(*args().values(), None) == 3
+    assert ccu.ccu_conv1d_update_checked(*args().values(), None, None) == 1  # NULL status word
+
+
+def test_noop_sizes(ccu):
+    assert select(ccu, N=0) == (0, 0)
+    assert select(ccu, D=0, x=None, weight=None) == (0, 0)
+
+
+def test_indices_allow_S_below_N(ccu):
+    st, r = select(ccu, S=2, indices=IDX)
+    assert st == 0 and r == 2
+
+
+ROUTE_CASES = [
+    ("L3 compact D%8", dict(), "vector"),
+    ("L8 compact", dict(L=8), "vector"),
+    ("L9 compact", dict(L=9), "staged"),
+    ("L256 compact", dict(L=256), "staged"),
+    ("L257 compact", dict(L=257), "scalar"),
+    ("D not multiple of 8", dict(D=63), "scalar"),
+    ("channel-last L3", dict(stride_s=192, stride_d=1, stride_l=64), "vector"),
+    ("channel-last L12", dict(L=12, stride_s=768, stride_d=1, stride_l=64), "staged"),
+    ("padded ld", dict(ld=72), "vector"),
+]
+
+
+@pytest.mark.parametrize("name,kw,route", ROUTE_CASES, ids=[c[0] for c in ROUTE_CASES])
+def test_auto_route(ccu, name, kw, route):
+    st, r = select(ccu, **kw)
+    assert st == 0, ccu.ccu_conv1d_last_error()
+    assert ccu.ccu_route_name(r) == route
+
+
+def test_forced_routes(ccu):
+    assert select(ccu, route=1) == (0, 1)
+    assert select(ccu, route=2) == (0, 2)
+    assert select(ccu, route=3) == (0, 3)
+    assert select(ccu, route=2, D=63)[0] == 2  # vector needs D % 8 == 0
+    assert select(ccu, route=2, L=9)[0] == 2   # vector is compiled for L <= 8
+    assert select(ccu, route=7)[0] == 1        # unknown route
+
+
+def test_check_indices_declines(ccu):
+    assert ccu.ccu_conv1d_check_indices(IDX, 0, 4, None, None, None) == 0  # N == 0: no-op
+    assert ccu.ccu_conv1d_check_indices(None, 4, 4, 0x900000, 0x800000, None) == 1
+    assert ccu.ccu_conv1d_check_indices(IDX + 1, 4, 4, 0x900000, 0x800000, None) == 1
+    assert ccu.ccu_conv1d_check_indices(IDX, -1, 4, 0x900000, 0x800000, None) == 1

@@ -1,0 +1,379 @@
+"""GPU parity: the CUDA kernels (through the C-ABI) against the CPU oracle.
+
+Pass criteria (from the update definition on the cuDNN page "Causal Conv1d Decode
+Update" and the precision reading of this library): the updated conv_state bit-exact;
+the BF16 output within one BF16 ulp of the oracle (bit-exact for identity, where the
+FP32 accumulation order is the same on both sides); canary guard bands around x, state
+and out unchanged; unselected slots and padding rows' state untouched (part of the
+full-state comparison).
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic
+from gpu_util import Guarded, assert_parity, from_dev_u16, oracle_ref, run_gpu, to_dev_u16
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import depthwise_causal_conv1d_gb300  # noqa: F401
+
+
+def _check(inp, layout="compact", route="auto", what=""):
+    want_out, want_state = oracle_ref(inp, layout)
+    got_out, got_state, _, ok = run_gpu(inp, layout, route)
+    assert ok, f"{what}: a guard band was overwritten"
+    assert_parity(inp, got_out, got_state, want_out, want_state, what)
+
+
+# ----------------------------------------------------------------------------- full workloads
+
+@pytest.mark.parametrize("name", list(synthetic.WORKLOADS))
+def test_workload_full_size(name):
+    """Every workload at full size, in the launch configuration the benchmark times."""
+    inp = synthetic.generate(synthetic.WORKLOADS[name])
+    _check(inp, what=name)
+
+
+@pytest.mark.parametrize("name", list(synthetic.WORKLOADS))
+def test_workload_channel_last(name):
+    wl = synthetic.WORKLOADS[name]
+    if wl.N * wl.D > 4_000_000:
+        wl = synthetic.variant(wl, N=256, S=max(256, wl.S // 16) if wl.indices.startswith("distinct") else 256)
+    inp = synthetic.generate(wl)
+    _check(inp, layout="channel_last", what=name + " channel-last")
+
+
+# ----------------------------------------------------------------------------- every route
+
+SMALL = [
+    dict(N=5, D=24, L=3, S=5, act="identity", bias_std=None, indices="none"),
+    dict(N=7, D=264, L=4, S=9, act="silu", bias_std=0.1, indices="distinct_pad", pad_frac=0.3),
+    dict(N=33, D=2056, L=3, S=33, act="silu", bias_std=0.1, indices="perm_pad", pad_frac=0.1),
+    dict(N=3, D=4104, L=8, S=3, act="identity", bias_std=None, indices="perm", ld=4112),
+    dict(N=4, D=64, L=5, S=6, act="silu", bias_std=None, indices="distinct"),
+    dict(N=4, D=128, L=6, S=4, act="identity", bias_std=0.1, indices="none"),
+    dict(N=2, D=16, L=7, S=2, act="silu", bias_std=0.1, indices="none"),
+    dict(N=6, D=520, L=9, S=8, act="silu", bias_std=0.1, indices="distinct_pad", pad_frac=0.34),
+    dict(N=3, D=72, L=16, S=3, act="identity", bias_std=None, indices="perm"),
+    dict(N=2, D=40, L=33, S=4, act="silu", bias_std=0.1, indices="distinct"),
+]
+
+
+def _small(i, **over):
+    base = synthetic.WORKLOADS["decode_n8_d2048_l4_bias_silu"]
+    kw = dict(SMALL[i])
+    kw.setdefault("ld", kw["D"])
+    kw.update(over)
+    return synthetic.variant(base, name=f"small{i}", **kw)
+
+
+@pytest.mark.parametrize("route", ["scalar", "vector", "staged"])
+@pytest.mark.parametrize("layout", ["compact", "channel_last"])
+@pytest.mark.parametrize("i", range(len(SMALL)))
+def test_routes(route, layout, i):
+    wl = _small(i)
+    if route == "vector" and wl.L > 8:
+        pytest.skip("vector kernels are compiled for L <= 8")
+    inp = synthetic.generate(wl, seed=100 + i)
+    _check(inp, layout=layout, route=route, what=f"{wl} {route} {layout}")
+
+
+# ----------------------------------------------------------------------------- sweeps
+
+SWEEP_D = [1, 7, 8, 9, 24, 255, 256, 257, 2048, 2050, 2056, 4104]
+SWEEP_N = [1, 2, 3, 33]
+
+
+@pytest.mark.parametrize("D", SWEEP_D)
+@pytest.mark.parametrize("L", [3, 4, 5, 8, 12])
+def test_sweep_channels_and_lengths(D, L):
+    # rotate N, act, bias, indices and layout with the case so all combinations appear
+    k = SWEEP_D.index(D) + L
+    N = SWEEP_N[k % 4]
+    act = ["identity", "silu"][k % 2]
+    bias = [None, 0.1][(k // 2) % 2]
+    ind = ["none", "perm_pad", "distinct", "distinct_pad"][(k // 3) % 4]
+    S = N if ind.startswith("perm") or ind == "none" else N + 3
+    wl = synthetic.variant(synthetic.WORKLOADS["decode_n8_d2048_l4_bias_silu"], name="sweep", N=N,
+                           D=D, ld=D, L=L, S=S, act=act, bias_std=bias, indices=ind, pad_frac=0.34)
+    inp = synthetic.generate(wl, seed=1000 + D + L)
+    for layout in ("compact", "channel_last"):
+        _check(inp, layout=layout, what=f"sweep D={D} L={L} N={N} {layout}")
+
+
+@pytest.mark.parametrize("D,ld", [(8, 16), (24, 32), (2050, 2056), (6144, 6152), (7, 8), (1, 8)])
+def test_padded_row_stride(D, ld):
+    wl = synthetic.variant(synthetic.WORKLOADS["strided_n64_d6144_ld6152_l8_perm_identity"],
+                           name="ld", N=9, S=9, D=D, ld=ld)
+    inp = synthetic.generate(wl, seed=7)
+    assert np.all(inp.x[:, D:] == synthetic.BF16_NAN_BITS)  # canaries that must never be read
+    _check(inp, what=f"ld D={D} ld={ld}")
+
+
+# ----------------------------------------------------------------------------- edge cases
+
+def test_all_rows_padding():
+    wl = synthetic.variant(synthetic.WORKLOADS["paged_n256_d8192_l3_s1024_pad10_silu"], name="allpad",
+                           N=16, D=512, S=64, indices="distinct_pad", pad_frac=1.0)
+    inp = synthetic.generate(wl)
+    assert np.all(inp.indices == -1)
+    want_out, want_state = oracle_ref(inp)
+    assert np.array_equal(want_state, inp.conv_state)
+    got_out, got_state, _, ok = run_gpu(inp)
+    assert ok and np.all(got_out == 0) and np.array_equal(got_state, inp.conv_state)
+
+
+def test_empty_batch_is_a_noop():
+    import depthwise_causal_conv1d_gb300 as ccu
+
+    x = torch.zeros((0, 64), dtype=torch.bfloat16, device=DEV)
+    st = torch.randn((4, 64, 3), device=DEV).to(torch.bfloat16)
+    before = st.clone()
+    w = torch.randn((64, 4), device=DEV).to(torch.bfloat16)
+    out = ccu.causal_conv1d_update(x, st, w)
+    torch.cuda.synchronize()
+    assert out.shape == (0, 64) and torch.equal(st, before)
+    x = torch.zeros((3, 0), dtype=torch.bfloat16, device=DEV)
+    st = torch.zeros((3, 0, 3), dtype=torch.bfloat16, device=DEV)
+    out = ccu.causal_conv1d_update(x, st, torch.zeros((0, 4), dtype=torch.bfloat16, device=DEV))
+    assert out.shape == (3, 0)
+
+
+def test_unselected_slots_untouched_large_cache():
+    wl = synthetic.variant(synthetic.WORKLOADS["paged_n256_d8192_l3_s1024_pad10_silu"], name="cache",
+                           N=20, D=1024, S=500)
+    inp = synthetic.generate(wl, seed=3)
+    _check(inp, what="S >> N")
+
+
+def test_extreme_values():
+    """Large magnitudes: SiLU saturates (-0/+0 and x), identity keeps big sums exact."""
+    wl = synthetic.variant(synthetic.WORKLOADS["decode_n8_d2048_l4_bias_silu"], name="extreme",
+                           x_dist=("normal", 60.0), w_dist=("normal", 4.0))
+    for act in ("silu", "identity"):
+        inp = synthetic.generate(dataclasses.replace(wl, act=act), seed=11)
+        _check(inp, what=f"extreme {act}")
+
+
+# ----------------------------------------------------------------------------- chained decode
+
+@pytest.mark.parametrize("L,act,layout", [(3, "identity", "compact"), (3, "silu", "channel_last"),
+                                          (4, "silu", "compact"), (8, "identity", "channel_last"),
+                                          (10, "silu", "compact")])
+def test_chained_decode_equals_full_convolution(L, act, layout):
+    """T GPU updates from a seeded state equal one full causal convolution of the sequence."""
+    import depthwise_causal_conv1d_gb300 as ccu
+
+    rng = np.random.default_rng(L)
+    T, D = 16, 264
+    x_seq = synthetic.f64_to_bf16_bits(rng.standard_normal((T, D)))
+    weight = synthetic.f64_to_bf16_bits(rng.standard_normal((D, 4)) * 0.5)
+    bias = synthetic.f64_to_bf16_bits(rng.standard_normal(D) * 0.1)
+    init = synthetic.f64_to_bf16_bits(rng.standard_normal((D, L)))
+    want_y, want_state = oracle.full_causal_conv(x_seq, weight, bias, act, init, L)
+    w, b = to_dev_u16(weight, DEV), to_dev_u16(bias, DEV)
+    if layout == "compact":
+        st = to_dev_u16(init.reshape(1, D, L), DEV)
+    else:
+        st = to_dev_u16(np.ascontiguousarray(init.T).reshape(1, L, D), DEV).permute(0, 2, 1)
+    ys = []
+    for t in range(T):
+        xt = to_dev_u16(x_seq[t:t + 1], DEV)
+        ys.append(from_dev_u16(ccu.causal_conv1d_update(xt, st, w, b, act)))
+    got_y = np.concatenate(ys)
+    got_state = from_dev_u16(st.contiguous())[0]
+    assert np.array_equal(got_state, want_state)
+    from oracle_pins import bf16_ulp_distance
+
+    assert bf16_ulp_distance(got_y, want_y).max() <= (0 if act == "identity" else 1)
+
+
+# ----------------------------------------------------------------------------- behaviour
+
+def test_deterministic():
+    inp = synthetic.generate(synthetic.WORKLOADS["paged_n256_d8192_l3_s1024_pad10_silu"])
+    a = run_gpu(inp)
+    b = run_gpu(inp)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_side_stream_with_default_stream_parked():
+    """The op runs on the ambient stream: with the default stream busy, a side stream's
+    result is complete when that side stream alone is synchronized."""
+    import depthwise_causal_conv1d_gb300 as ccu
+
+    inp = synthetic.generate(synthetic.WORKLOADS["paged_n256_d8192_l3_s1024_pad10_silu"])
+    want_out, want_state = oracle_ref(inp)
+    x, st = to_dev_u16(inp.x, DEV), to_dev_u16(inp.conv_state, DEV)
+    w, b = to_dev_u16(inp.weight, DEV), to_dev_u16(inp.bias, DEV)
+    idx = torch.from_numpy(inp.indices).to(DEV)
+    out = torch.empty((inp.wl.N, inp.wl.D), dtype=torch.bfloat16, device=DEV)
+    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    host_state = torch.empty(st.shape, dtype=st.dtype, pin_memory=True)
+    side = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    # nothing below allocates device or pinned memory, which could synchronize the device
+    torch.cuda._sleep(200_000_000)  # parks the default stream for ~0.1 s (bounded spin)
+    with torch.cuda.stream(side):
+        ccu.causal_conv1d_update(x, st, w, b, "silu", conv_state_indices=idx, out=out)
+        host_out.copy_(out, non_blocking=True)
+        host_state.copy_(st, non_blocking=True)
+    side.synchronize()
+    default_busy = not torch.cuda.default_stream().query()
+    got_out = host_out.view(torch.int16).numpy().view(np.uint16)
+    got_state = host_state.view(torch.int16).numpy().view(np.uint16)
+    torch.cuda.synchronize()
+    assert default_busy, "the default stream finished first: the test did not park it"
+    assert_parity(inp, got_out, got_state, want_out, want_state, "side stream")
+
+
+def test_cuda_graph_replay_matches_eager():
+    import depthwise_causal_conv1d_gb300 as ccu
+
+    inp = synthetic.generate(synthetic.WORKLOADS["strided_n64_d6144_ld6152_l8_perm_identity"])
+    wl = inp.wl
+
+    def setup():
+        x = to_dev_u16(inp.x, DEV)[:, :wl.D]
+        st = to_dev_u16(inp.conv_state, DEV)
+        w = to_dev_u16(inp.weight, DEV)
+        idx = torch.from_numpy(inp.indices).to(DEV)
+        out = torch.empty((wl.N, wl.D), dtype=torch.bfloat16, device=DEV)
+        return x, st, w, idx, out
+
+    steps = 5
+    x, st, w, idx, out = setup()
+    eager = []
+    for _ in range(steps):
+        ccu.causal_conv1d_update(x, st, w, None, "identity", conv_state_indices=idx, out=out)
+        eager.append(out.clone())
+    eager_state = st.clone()
+
+    x, st, w, idx, out = setup()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # warm the exact signature before capture
+        ccu.causal_conv1d_update(x, st, w, None, "identity", conv_state_indices=idx, out=out)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    x, st2, w, idx, out = setup()
+    st.copy_(st2)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        ccu.causal_conv1d_update(x, st, w, None, "identity", conv_state_indices=idx, out=out)
+    graphed = []
+    for _ in range(steps):
+        g.replay()
+        graphed.append(out.clone())
+    torch.cuda.synchronize()
+    for a, b in zip(eager, graphed):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert torch.equal(eager_state.view(torch.int16), st.view(torch.int16))
+
+
+# ----------------------------------------------------------------------------- checked path
+
+@pytest.mark.parametrize("route", ["scalar", "vector", "staged"])
+def test_checked_path_flags_bad_slots_without_trapping(route):
+    wl = synthetic.variant(synthetic.WORKLOADS["paged_n256_d8192_l3_s1024_pad10_silu"], name="chk",
+                           N=12, D=1024, S=16, indices="distinct_pad", pad_frac=0.2)
+    inp = synthetic.generate(wl, seed=5)
+    bad_rows = [1, 4, 9]
+    bad_vals = [-2, wl.S, 10 ** 6]
+    idx = inp.indices.copy()
+    for r, v in zip(bad_rows, bad_vals):
+        idx[r] = v
+    # the oracle's view: bad rows behave as padding rows (zero output, no state access)
+    ref_idx = idx.copy()
+    ref_idx[bad_rows] = -1
+    want_out, want_state = oracle_ref(dataclasses.replace(inp, indices=ref_idx))
+    got_out, got_state, status, ok = run_gpu(dataclasses.replace(inp, indices=idx), route=route,
+                                             checked=True)
+    assert ok
+    assert status & 1, "range error not reported"
+    assert_parity(inp, got_out, got_state, want_out, want_state, "checked")
+    # the context is still usable
+    got_out2, _, status2, _ = run_gpu(inp, checked=True)
+    assert status2 == 0
+
+
+def test_checked_path_clean_inputs_report_nothing():
+    inp = synthetic.generate(synthetic.WORKLOADS["paged_n256_d8192_l3_s1024_pad10_silu"])
+    want_out, want_state = oracle_ref(inp)
+    got_out, got_state, status, ok = run_gpu(inp, checked=True)
+    assert ok and status == 0
+    assert_parity(inp, got_out, got_state, want_out, want_state, "checked clean")
+
+
+@pytest.mark.parametrize("case", ["valid", "padding", "range_low", "range_high", "duplicate", "both"])
+def test_check_indices_matches_oracle(case):
+    import depthwise_causal_conv1d_gb300 as ccu
+
+    rng = np.random.default_rng(["valid", "padding", "range_low", "range_high", "duplicate",
+                                 "both"].index(case))
+    S, N = 4099, 3000
+    idx = rng.permutation(S)[:N].astype(np.int32)
+    if case == "padding":
+        idx[::7] = -1
+    elif case == "range_low":
+        idx[17] = -5
+    elif case == "range_high":
+        idx[100] = S
+    elif case == "duplicate":
+        idx[2999] = idx[0]
+    elif case == "both":
+        idx[5] = idx[6]
+        idx[7] = S + 10
+    want = oracle.check_indices(idx, N, S)
+    dev_idx = torch.from_numpy(idx).to(DEV)
+    status = torch.zeros((1,), dtype=torch.int32, device=DEV)
+    scratch = torch.full((ccu.ccu_conv1d_check_indices_scratch_bytes(S) // 4,), -1, dtype=torch.int32,
+                         device=DEV)  # dirty on purpose: the call clears it
+    for _ in range(2):
+        ccu.check_indices(dev_idx, S, status=status, scratch=scratch)
+    assert int(status.item()) == want
+
+
+# ----------------------------------------------------------------------------- declines (typed)
+
+def test_typed_declines_through_binding():
+    import depthwise_causal_conv1d_gb300 as ccu
+
+    x = torch.randn((4, 64), device=DEV).to(torch.bfloat16)
+    st = torch.randn((4, 64, 3), device=DEV).to(torch.bfloat16)
+    w = torch.randn((64, 4), device=DEV).to(torch.bfloat16)
+    seq = torch.zeros((4,), dtype=torch.int32, device=DEV)
+    with pytest.raises(NotImplementedError, match="cache_seqlens"):
+        ccu.causal_conv1d_update(x, st, w, cache_seqlens=seq)
+    with pytest.raises(NotImplementedError, match="3D x"):
+        ccu.causal_conv1d_update(x.view(4, 64, 1), st, w)
+    with pytest.raises(NotImplementedError, match="W == 4"):
+        ccu.causal_conv1d_update(x, st, w[:, :3].contiguous())
+    with pytest.raises(ValueError, match="L must be >= W - 1"):
+        ccu.causal_conv1d_update(x, st[:, :, :2].contiguous(), w)
+    base = torch.randn((4 * 72 + 8,), device=DEV).to(torch.bfloat16)
+    with pytest.raises(ValueError, match="16-byte"):
+        ccu.causal_conv1d_update(base[1:1 + 4 * 72].view(4, 72)[:, :64], st, w)
+    with pytest.raises(ValueError, match="multiple of 8"):
+        ccu.causal_conv1d_update(torch.randn((4, 68), device=DEV).to(torch.bfloat16)[:, :64], st, w)
+    with pytest.raises(ValueError, match="autograd"):
+        ccu.causal_conv1d_update(x.clone().requires_grad_(), st, w)
+    with pytest.raises(NotImplementedError, match="strides"):
+        ccu.causal_conv1d_update(x, torch.randn((64, 4, 3), device=DEV).to(torch.bfloat16).transpose(0, 1), w)
+    with pytest.raises(ValueError, match="activation"):
+        ccu.causal_conv1d_update(x, st, w, activation="gelu")
+    with pytest.raises(ValueError, match="S must be >= N"):
+        ccu.causal_conv1d_update(x, st[:3].contiguous(), w)
+    # nothing was launched by any decline
+    torch.cuda.synchronize()
