@@ -37,6 +37,7 @@ CCU_ACT_SILU = 1
 ROUTES = {"auto": 0, "scalar": 1, "vector": 2, "staged": 3, "bulk": 4}
 CCU_DEVERR_RANGE = 1
 CCU_DEVERR_DUPLICATE = 2
+CCU_DEVERR_TIMEOUT = 4
 
 _ACTIVATIONS = {None: CCU_ACT_IDENTITY, "identity": CCU_ACT_IDENTITY,
                 "silu": CCU_ACT_SILU, "swish": CCU_ACT_SILU}
@@ -70,6 +71,8 @@ def _load() -> ctypes.CDLL:
     lib.ccu_route_name.restype = ctypes.c_char_p
     lib.ccu_conv1d_last_error.argtypes = []
     lib.ccu_conv1d_last_error.restype = ctypes.c_char_p
+    lib.ccu_conv1d_take_device_error.argtypes = [ctypes.POINTER(i32)]
+    lib.ccu_conv1d_take_device_error.restype = ctypes.c_int
     lib.ccu_conv1d_abi_version.argtypes = []
     lib.ccu_conv1d_abi_version.restype = i32
     return lib
@@ -128,6 +131,13 @@ def ccu_route_name(route) -> str:
 
 def ccu_conv1d_last_error() -> str:
     return lib.ccu_conv1d_last_error().decode()
+
+
+def ccu_conv1d_take_device_error():
+    """Returns (status, bits); synchronizes the current device."""
+    bits = ctypes.c_int32(0)
+    st = lib.ccu_conv1d_take_device_error(ctypes.byref(bits))
+    return st, bits.value
 
 
 def ccu_conv1d_abi_version() -> int:

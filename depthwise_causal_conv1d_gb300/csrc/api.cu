@@ -114,17 +114,22 @@ bool route_serves(int route, const Args &a, Layout layout) {
     case CCU_ROUTE_SCALAR: return true;
     case CCU_ROUTE_VECTOR: return vec8 && a.L <= kVectorMaxL;
     case CCU_ROUTE_STAGED: return vec8 && a.L <= kStagedMaxL;
-    case CCU_ROUTE_BULK: return false;  // not built
+    case CCU_ROUTE_BULK: return vec8 && a.L <= kVectorMaxL && layout == Layout::Compact;
     default: return false;
   }
-  (void)layout;
 }
+
+// Below this many (row, channel) elements a call is launch-bound and the plain vector
+// kernel's shorter start-up wins; above it the bulk-copy pipeline keeps more bytes in flight.
+constexpr int64_t kBulkMinElements = 1 << 22;
 
 ccu_status_t choose(int requested, const Args &a, Layout layout, int *chosen) {
   if (requested < 0 || requested >= CCU_ROUTE_COUNT)
     return fail(CCU_ERR_INVALID_ARGUMENT, "unknown route %d", requested);
   if (requested == CCU_ROUTE_AUTO) {
-    if (route_serves(CCU_ROUTE_VECTOR, a, layout)) {
+    if (a.N * a.D >= kBulkMinElements && route_serves(CCU_ROUTE_BULK, a, layout)) {
+      *chosen = CCU_ROUTE_BULK;
+    } else if (route_serves(CCU_ROUTE_VECTOR, a, layout)) {
       *chosen = CCU_ROUTE_VECTOR;
     } else if (route_serves(CCU_ROUTE_STAGED, a, layout)) {
       *chosen = CCU_ROUTE_STAGED;
@@ -173,6 +178,7 @@ ccu_status_t run(const Args &a, int route, cudaStream_t stream) {
     case CCU_ROUTE_SCALAR: e = launch_scalar(p, a.act, stream); break;
     case CCU_ROUTE_VECTOR: e = launch_vector(p, a.act, stream); break;
     case CCU_ROUTE_STAGED: e = launch_staged(p, a.act, stream); break;
+    case CCU_ROUTE_BULK: e = launch_bulk(p, a.act, stream); break;
     default: break;
   }
   if (e != cudaSuccess)
@@ -309,6 +315,15 @@ const char *ccu_route_name(int32_t route) {
     case CCU_ROUTE_BULK: return "bulk";
     default: return "unknown";
   }
+}
+
+ccu_status_t ccu_conv1d_take_device_error(int32_t *bits) {
+  ccu::g_last_error[0] = '\0';
+  if (bits == nullptr) return ccu::fail(CCU_ERR_INVALID_ARGUMENT, "bits must not be NULL");
+  cudaError_t e = ccu::take_async_error(bits);
+  if (e != cudaSuccess)
+    return ccu::fail(CCU_ERR_CUDA, "reading the device error word failed: %s", cudaGetErrorString(e));
+  return CCU_OK;
 }
 
 const char *ccu_conv1d_last_error(void) { return ccu::g_last_error; }

@@ -58,10 +58,20 @@ __device__ __forceinline__ uint16_t round_bf16(float v) {
 }
 
 // The activation, a compile-time choice: identity kernels carry no SiLU code.
+// SiLU is a * sigmoid(a). With e = exp(-|a|) in (0, 1], sigmoid(a) = 1 / (1 + e) for
+// a >= 0 and e / (1 + e) for a < 0, so a * sigmoid(a) = (a >= 0 ? a : a * e) / (1 + e):
+// no overflow for any finite a (a / (1 + exp(-a)) overflows to -0 below a ~ -88.7, where
+// the true value is still a representable float). The exponential and the division use
+// the hardware approximations (__expf, __fdividef with a denominator in [1, 2]): a few
+// float ulps of error, far below the half BF16 ulp (2^15 float ulps) the result keeps, so
+// the rounded output stays within one BF16 ulp of the exact value. The accurate library
+// versions made this path issue-bound on the large batch.
 template <int ACT>
 __device__ __forceinline__ float activate(float a) {
   if constexpr (ACT == 1) {
-    return a / (1.0f + expf(-a));  // SiLU: a * sigmoid(a)
+    const float e = __expf(-fabsf(a));
+    const float num = a >= 0.0f ? a : a * e;
+    return __fdividef(num, 1.0f + e);
   } else {
     return a;
   }
@@ -91,6 +101,43 @@ __device__ __forceinline__ int64_t resolve_slot(const UpdateParams &p, int64_t n
   return s;
 }
 
+__device__ __forceinline__ uint32_t get16(const uint32_t *w, int pos) {
+  return (w[pos >> 1] >> ((pos & 1) * 16)) & 0xffffu;
+}
+
+// The update of 8 consecutive channels whose compact state [8][L] sits in 4*L words `ow`
+// (two BF16 per word, flat position c*L + l) and whose inputs sit in 4 words `xw`:
+//   out[c]      = act(sum_j h_c[L-3+j] * w[c][j] + bias[c]),  h_c = (state[c][0..L-1], x[c])
+//   new state   = state[c][1..L-1] followed by x[c]   (written to `nw`, same packing)
+// `wv` holds weight[8][4] (16 words), `bv` bias[8] (4 words). Returns the packed outputs.
+template <int L, int ACT>
+__device__ __forceinline__ uint4 update8_compact(const uint32_t (&xw)[4], const uint32_t (&ow)[4 * L],
+                                                 const uint32_t (&wv)[16], const uint32_t (&bv)[4],
+                                                 bool has_bias, uint32_t (&nw)[4 * L]) {
+  float y[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    float acc = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kW; ++j) {
+      const int hidx = L - (kW - 1) + j;  // index into the L + 1 history entries
+      const uint32_t h = (hidx == L) ? get16(xw, c) : get16(ow, c * L + hidx);
+      acc = __fmaf_rn(bf16_bits(h), bf16_bits(get16(wv, c * kW + j)), acc);
+    }
+    if (has_bias) acc = acc + bf16_bits(get16(bv, c));
+    y[c] = activate<ACT>(acc);
+  }
+#pragma unroll
+  for (int i = 0; i < 4 * L; ++i) {
+    const int e0 = 2 * i, e1 = 2 * i + 1;  // flat positions c*L + l
+    const uint32_t v0 = (e0 % L == L - 1) ? get16(xw, e0 / L) : get16(ow, e0 + 1);
+    const uint32_t v1 = (e1 % L == L - 1) ? get16(xw, e1 / L) : get16(ow, e1 + 1);
+    nw[i] = v0 | (v1 << 16);
+  }
+  return make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                    pack_bf16x2(y[6], y[7]));
+}
+
 // ---------------------------------------------------------------------------------------
 // Kernel launchers (one per family). Each returns the cudaError_t of its launch.
 
@@ -98,9 +145,13 @@ cudaError_t launch_scalar(const UpdateParams &p, int act, cudaStream_t stream);
 cudaError_t launch_vector(const UpdateParams &p, int act, cudaStream_t stream);
 cudaError_t launch_staged(const UpdateParams &p, int act, cudaStream_t stream);
 cudaError_t launch_bulk(const UpdateParams &p, int act, cudaStream_t stream);
+// Reads and clears the device error word that kernels without a status word report into.
+cudaError_t take_async_error(int32_t *bits);
 cudaError_t launch_check_indices(const int32_t *idx, int64_t N, int64_t S, uint32_t *bitmap,
                                  int32_t *status, cudaStream_t stream);
 
+// CCU_DEVERR_TIMEOUT: a bounded wait inside a kernel gave up.
+constexpr int32_t kDevErrTimeout = 4;
 // Largest L the register-resident vector and bulk kernels are compiled for.
 constexpr int64_t kVectorMaxL = 8;
 // Largest L the shared-memory staged kernel accepts.

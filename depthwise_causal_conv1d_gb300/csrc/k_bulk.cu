@@ -1,0 +1,343 @@
+// Bulk-copy kernel for large batches (compact state layout, L = 3..8, D % 8 == 0).
+//
+// Every warp is an independent pipeline. Its work items are slices (row n, 256*G
+// consecutive channels); lane 0 moves whole slices between global and shared memory with
+// the bulk-copy engine (cp.async.bulk): the x slice (512*G bytes) and the slot's state
+// slab (512*G*L bytes, contiguous in the compact layout) land in one stage of the warp's
+// own ring of P stages and complete on that stage's mbarrier. The 32 lanes then update 8
+// channels per group in shared memory (the new state in place over the old, the output
+// over x), and lane 0 writes the output slice and the state slab back with bulk stores.
+// Loads run P-1 slices ahead. No barrier spans more than one warp, so warps drift freely
+// and one warp's arithmetic overlaps other warps' copies.
+//
+// Every mbarrier wait has an iteration limit: on expiry the warp records
+// CCU_DEVERR_TIMEOUT, waits (again bounded) for its own copies in flight and returns.
+//
+// Update definition: cuDNN page "Causal Conv1d Decode Update", introduction (update
+// block) and the conv_state_indices paragraph; compact state layout from its "Semantic
+// tensor contract".
+#include <atomic>
+
+#include "ccu_internal.cuh"
+
+namespace ccu {
+
+int device_sm_count();
+int current_device();
+
+__device__ int32_t g_async_error = 0;  // CCU_DEVERR_* bits raised by a kernel with no status word
+
+namespace {
+
+constexpr int kThreads = 256;              // 8 warps per CTA
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxStages = 8;
+constexpr int kBarrierBytes = 64;           // a warp's P mbarriers, padded
+constexpr uint32_t kMaxSpins = 1u << 22;    // try_wait rounds before a wait is declared failed
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Bounded wait for the phase with the given parity to complete.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kMaxSpins; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+// global -> shared bulk copy; completes `bytes` of transaction count on `bar`.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// shared -> global bulk copy, tracked by bulk async-groups.
+__device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+               "r"(smem_addr(src)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// All but the newest N committed store groups have finished reading shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Generic-proxy writes to shared memory become visible to the bulk-copy (async) proxy.
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+struct Slice {
+  int64_t n, c_base, cn, s;
+};
+
+template <int G>
+__device__ __forceinline__ Slice slice_of(const UpdateParams &p, int64_t t, int64_t slices, bool report) {
+  constexpr int64_t kSlice = 256 * G;
+  Slice sl;
+  sl.n = t / slices;
+  sl.c_base = (t - sl.n * slices) * kSlice;
+  const int64_t rem = p.D - sl.c_base;
+  sl.cn = rem < kSlice ? rem : kSlice;
+  if (p.idx == nullptr) {
+    sl.s = sl.n;
+  } else {
+    sl.s = __ldg(p.idx + sl.n);
+    if (p.status != nullptr && (sl.s < -1 || sl.s >= p.S)) {
+      if (report) atomicOr(p.status, 1);  // CCU_DEVERR_RANGE
+      sl.s = -1;
+    }
+  }
+  return sl;
+}
+
+// Shared memory per warp: kBarrierBytes of mbarriers, then P stages of stage_bytes.
+template <int L, int ACT, int G>
+__global__ void __launch_bounds__(kThreads) k_update_bulk(UpdateParams p, int stages, int64_t stage_bytes) {
+  constexpr int64_t kSlice = 256 * G;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int P = stages;
+  unsigned char *wbase = smem + (int64_t)warp * (kBarrierBytes + P * stage_bytes);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(wbase);
+  unsigned char *bufs = wbase + kBarrierBytes;
+
+  const int64_t slices = (p.D + kSlice - 1) / kSlice;
+  const int64_t items = p.N * slices;
+  const int64_t first = (int64_t)blockIdx.x * kWarps + warp;
+  const int64_t stride = (int64_t)gridDim.x * kWarps;
+  const int64_t mine = items > first ? (items - first + stride - 1) / stride : 0;
+
+  if (lane == 0) {
+    for (int k = 0; k < P; ++k) mbar_init(&bars[k], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  // Lane 0: put this warp's k-th slice into stage k % P.
+  auto issue = [&](int64_t k) {
+    const Slice sl = slice_of<G>(p, first + k * stride, slices, true);
+    uint64_t *bar = &bars[k % P];
+    unsigned char *buf = bufs + (k % P) * stage_bytes;
+    if (sl.s < 0) {
+      mbar_arrive(bar);  // padding row: nothing to load
+    } else {
+      const uint32_t bx = (uint32_t)(sl.cn * 2), bs = (uint32_t)(sl.cn * L * 2);
+      mbar_arrive_expect_tx(bar, bx + bs);
+      bulk_load(buf, p.x + sl.n * p.ld + sl.c_base, bx, bar);
+      bulk_load(buf + 2 * kSlice, p.state + sl.s * (p.D * L) + sl.c_base * L, bs, bar);
+    }
+  };
+
+  const int64_t prologue = mine < P ? mine : P;
+  if (lane == 0)
+    for (int64_t k = 0; k < prologue; ++k) issue(k);
+
+  const bool has_bias = p.bias != nullptr;
+  uint32_t wv[G][16], bv[G][4];
+  int64_t w_base = -1;
+  bool failed = false;
+  int64_t k = 0;
+
+  for (; k < mine; ++k) {
+    const int st = (int)(k % P);
+    const uint32_t parity = (uint32_t)((k / P) & 1);
+    const Slice sl = slice_of<G>(p, first + k * stride, slices, false);
+    unsigned char *buf = bufs + st * stage_bytes;
+
+    if (sl.c_base != w_base) {  // weights of this slice, kept while it repeats
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const int64_t c = sl.c_base + 8 * (lane + 32 * g);
+        if (8 * (lane + 32 * g) < sl.cn) {
+          const uint16_t *wp = p.w + c * kW;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 t = ld_keep(wp + 8 * q);
+            wv[g][4 * q] = t.x; wv[g][4 * q + 1] = t.y; wv[g][4 * q + 2] = t.z; wv[g][4 * q + 3] = t.w;
+          }
+          if (has_bias) {
+            const uint4 t = ld_keep(p.bias + c);
+            bv[g][0] = t.x; bv[g][1] = t.y; bv[g][2] = t.z; bv[g][3] = t.w;
+          } else {
+            bv[g][0] = bv[g][1] = bv[g][2] = bv[g][3] = 0u;
+          }
+        }
+      }
+      w_base = sl.c_base;
+    }
+
+    // Every lane waits (bounded); the verdict is made warp-uniform.
+    const bool ok = mbar_wait(&bars[st], parity);
+    if (!__all_sync(kFull, ok)) {
+      failed = true;
+      break;
+    }
+
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const int q8 = lane + 32 * g;  // 8-channel group within the slice
+      if (8 * q8 >= sl.cn) continue;
+      if (sl.s < 0) {
+        st_stream(p.out + sl.n * p.D + sl.c_base + 8 * q8, make_uint4(0u, 0u, 0u, 0u));
+        continue;
+      }
+      uint4 *sx = reinterpret_cast<uint4 *>(buf) + q8;
+      uint4 *ss = reinterpret_cast<uint4 *>(buf + 2 * kSlice) + q8 * L;
+      const uint4 xv = *sx;
+      const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
+      uint32_t ow[4 * L], nw[4 * L];
+#pragma unroll
+      for (int q = 0; q < L; ++q) {
+        const uint4 t = ss[q];
+        ow[4 * q] = t.x; ow[4 * q + 1] = t.y; ow[4 * q + 2] = t.z; ow[4 * q + 3] = t.w;
+      }
+      const uint4 outv = update8_compact<L, ACT>(xw, ow, wv[g], bv[g], has_bias, nw);
+#pragma unroll
+      for (int q = 0; q < L; ++q) ss[q] = make_uint4(nw[4 * q], nw[4 * q + 1], nw[4 * q + 2], nw[4 * q + 3]);
+      *sx = outv;
+    }
+    fence_proxy_async();
+    __syncwarp();
+
+    if (lane == 0) {
+      if (sl.s >= 0) {
+        bulk_store(p.out + sl.n * p.D + sl.c_base, buf, (uint32_t)(sl.cn * 2));
+        bulk_store(p.state + sl.s * (p.D * L) + sl.c_base * L, buf + 2 * kSlice,
+                   (uint32_t)(sl.cn * L * 2));
+      }
+      bulk_commit();
+      // Refill the previous stage once its stores have read their shared memory.
+      if (k >= 1 && k - 1 + P < mine) {
+        bulk_wait_read<1>();
+        issue(k - 1 + P);
+      }
+    }
+    __syncwarp();
+  }
+
+  if (failed && lane == 0) {
+    // Record the error, then let this warp's own loads land before shared memory goes away.
+    atomicOr(p.status != nullptr ? p.status : &g_async_error, kDevErrTimeout);
+    const int64_t issued = (k - 1 + P < mine) ? k - 1 + P : mine;
+    for (int64_t q = k; q < issued; ++q) mbar_wait(&bars[q % P], (uint32_t)((q / P) & 1));
+  }
+  if (lane == 0) bulk_wait_all();  // stores complete before the warp retires
+}
+
+constexpr int kMaxDevices = 64;
+std::atomic<bool> g_opted_in[kMaxDevices][kVectorMaxL + 1][2];
+
+constexpr int kGroups = 2;  // 8-channel groups per lane: slices of 512 channels
+
+int64_t stage_bytes_for(int64_t L) {
+  const int64_t b = (int64_t)256 * kGroups * 2 * (L + 1);
+  return (b + 127) / 128 * 128;
+}
+
+template <int L, int ACT>
+cudaError_t launch_LA(const UpdateParams &p, cudaStream_t stream) {
+  const int64_t sb = stage_bytes_for(L);
+  // About 8 KB of stages per warp (two 4 KB stages at L = 3): 3 CTAs of 8 warps fit an SM.
+  // Measured on the large batch: slices of 512 channels with two stages beat 256-channel
+  // slices with four (larger bulk copies) and deeper rings with fewer resident warps.
+  int P = (int)(8 * 1024 / sb);
+  P = P < 2 ? 2 : (P > kMaxStages ? kMaxStages : P);
+  const size_t smem = (size_t)kWarps * (kBarrierBytes + (size_t)P * sb);
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!g_opted_in[dev][L][ACT].load(std::memory_order_acquire)) {
+    cudaError_t e = cudaFuncSetAttribute(k_update_bulk<L, ACT, kGroups>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    g_opted_in[dev][L][ACT].store(true, std::memory_order_release);
+  }
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_update_bulk<L, ACT, kGroups>,
+                                                                kThreads, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  const int64_t slices = (p.D + 256 * kGroups - 1) / (256 * kGroups);
+  const int64_t items = p.N * slices;
+  int64_t warps = (int64_t)device_sm_count() * per_sm * kWarps;
+  // A warp count that is a multiple of the slice count keeps every warp on one slice, so
+  // its weights stay in registers.
+  if (warps >= slices) warps = warps / slices * slices;
+  if (warps > items) warps = items;
+  int64_t grid = (warps + kWarps - 1) / kWarps;
+  if (grid < 1) grid = 1;
+  k_update_bulk<L, ACT, kGroups><<<(unsigned)grid, kThreads, smem, stream>>>(p, P, sb);
+  return cudaGetLastError();
+}
+
+template <int ACT>
+cudaError_t launch_A(const UpdateParams &p, cudaStream_t stream) {
+  switch (p.L) {
+    case 3: return launch_LA<3, ACT>(p, stream);
+    case 4: return launch_LA<4, ACT>(p, stream);
+    case 5: return launch_LA<5, ACT>(p, stream);
+    case 6: return launch_LA<6, ACT>(p, stream);
+    case 7: return launch_LA<7, ACT>(p, stream);
+    case 8: return launch_LA<8, ACT>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t take_async_error(int32_t *bits) {
+  int32_t zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(bits, g_async_error, sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_async_error, &zero, sizeof(int32_t));
+  return e;
+}
+
+cudaError_t launch_bulk(const UpdateParams &p, int act, cudaStream_t stream) {
+  if (p.layout != (int)Layout::Compact) return cudaErrorInvalidValue;
+  return act == 1 ? launch_A<1>(p, stream) : launch_A<0>(p, stream);
+}
+
+}  // namespace ccu

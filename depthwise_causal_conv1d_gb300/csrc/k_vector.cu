@@ -23,10 +23,6 @@ __device__ __forceinline__ constexpr int elem_pos(int c, int l) {
   return LAYOUT == (int)Layout::Compact ? c * L + l : l * 8 + c;
 }
 
-__device__ __forceinline__ uint32_t get16(const uint32_t *w, int pos) {
-  return (w[pos >> 1] >> ((pos & 1) * 16)) & 0xffffu;
-}
-
 template <int L, int ACT, int LAYOUT>
 __global__ void __launch_bounds__(256) k_update_vector(UpdateParams p) {
   const int64_t groups = p.D >> 3;  // 8-channel groups per row (D % 8 == 0)
@@ -94,35 +90,31 @@ __global__ void __launch_bounds__(256) k_update_vector(UpdateParams p) {
         }
       }
 
-      // acc = sum_j history[L-3+j] * w[j] (j = 0..3, history[L] = x), then bias.
-      float y[8];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        float acc = 0.0f;
-#pragma unroll
-        for (int j = 0; j < kW; ++j) {
-          const int hidx = L - (kW - 1) + j;
-          const uint32_t h = (hidx == L) ? get16(xw, c) : get16(ow, elem_pos<L, LAYOUT>(c, hidx));
-          acc = __fmaf_rn(bf16_bits(h), bf16_bits(get16(wv, c * kW + j)), acc);
-        }
-        if (has_bias) acc = acc + bf16_bits(get16(bv, c));
-        y[c] = activate<ACT>(acc);
-      }
-
-      // New state: entry l takes old entry l+1; the newest entry takes x.
       uint32_t nw[4 * L];
+      uint4 outv;
       if constexpr (LAYOUT == (int)Layout::Compact) {
-#pragma unroll
-        for (int i = 0; i < 4 * L; ++i) {
-          const int e0 = 2 * i, e1 = 2 * i + 1;  // flat positions c*L + l
-          const uint32_t v0 = (e0 % L == L - 1) ? get16(xw, e0 / L) : get16(ow, e0 + 1);
-          const uint32_t v1 = (e1 % L == L - 1) ? get16(xw, e1 / L) : get16(ow, e1 + 1);
-          nw[i] = v0 | (v1 << 16);
-        }
+        outv = update8_compact<L, ACT>(xw, ow, wv, bv, has_bias, nw);
 #pragma unroll
         for (int k = 0; k < L; ++k)
           st_stream(sp + 8 * k, make_uint4(nw[4 * k], nw[4 * k + 1], nw[4 * k + 2], nw[4 * k + 3]));
       } else {
+        // acc = sum_j history[L-3+j] * w[j] (j = 0..3, history[L] = x), then bias.
+        float y[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          float acc = 0.0f;
+#pragma unroll
+          for (int j = 0; j < kW; ++j) {
+            const int hidx = L - (kW - 1) + j;
+            const uint32_t h = (hidx == L) ? get16(xw, c) : get16(ow, elem_pos<L, LAYOUT>(c, hidx));
+            acc = __fmaf_rn(bf16_bits(h), bf16_bits(get16(wv, c * kW + j)), acc);
+          }
+          if (has_bias) acc = acc + bf16_bits(get16(bv, c));
+          y[c] = activate<ACT>(acc);
+        }
+        outv = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                          pack_bf16x2(y[6], y[7]));
+        // New state: plane l takes old plane l+1; the newest plane takes x.
 #pragma unroll
         for (int l = 0; l + 1 < L; ++l)
 #pragma unroll
@@ -134,9 +126,7 @@ __global__ void __launch_bounds__(256) k_update_vector(UpdateParams p) {
           st_stream(sp + (int64_t)l * p.D,
                     make_uint4(nw[4 * l], nw[4 * l + 1], nw[4 * l + 2], nw[4 * l + 3]));
       }
-
-      st_stream(outp, make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
-                                 pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7])));
+      st_stream(outp, outv);
     }
   }
 }

@@ -79,9 +79,12 @@ typedef enum ccu_route {
   CCU_ROUTE_COUNT = 5
 } ccu_route_t;
 
-/* Bits ORed into the device status word by the checked entry points. */
+/* Bits ORed into a device status word (the caller's, or the library's own, see
+ * ccu_conv1d_take_device_error). */
 #define CCU_DEVERR_RANGE 1     /* a slot index < -1 or >= S */
 #define CCU_DEVERR_DUPLICATE 2 /* a non-padding slot used by more than one row */
+#define CCU_DEVERR_TIMEOUT 4   /* a bounded wait inside a kernel gave up; that call's
+                                  results are incomplete */
 
 /*
  * ccu_conv1d_update -- one decode step, in place on conv_state.
@@ -196,6 +199,18 @@ CCU_API ccu_status_t ccu_conv1d_check_indices(const int32_t *indices, int64_t N,
 /* Bytes of scratch ccu_conv1d_check_indices needs for S slots (one bit per slot, rounded
  * up to whole 32-bit words); 0 for S <= 0. */
 CCU_API int64_t ccu_conv1d_check_indices_scratch_bytes(int64_t S);
+
+/*
+ * ccu_conv1d_take_device_error -- read and clear the library's own device error word.
+ *
+ * Kernels that wait on their own asynchronous copies (the bulk family) never wait without
+ * limit; if a wait gives up they OR CCU_DEVERR_TIMEOUT into the caller's status word when
+ * there is one (checked entry points), and otherwise into this per-process, per-device
+ * word. This call SYNCHRONIZES the current device (it copies the word to the host).
+ *
+ *   bits  host int32 out-parameter: the CCU_DEVERR_* bits raised since the last call.
+ */
+CCU_API ccu_status_t ccu_conv1d_take_device_error(int32_t *bits);
 
 /* Static English text for a status code. Never NULL. */
 CCU_API const char *ccu_status_string(ccu_status_t status);

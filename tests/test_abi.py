@@ -66,6 +66,7 @@ def test_status_strings(ccu):
     assert "not implemented" in ccu.ccu_status_string(2)
     assert ccu.ccu_status_string(99) == "unknown status"
     assert [ccu.ccu_route_name(r) for r in range(5)] == ["auto", "scalar", "vector", "staged", "bulk"]
+    assert ccu.ccu_route_name(5) == "unknown"
     assert ccu.ccu_conv1d_abi_version() == 1
     assert ccu.ccu_conv1d_check_indices_scratch_bytes(0) == 0
     assert ccu.ccu_conv1d_check_indices_scratch_bytes(1) == 4
@@ -160,6 +161,10 @@ ROUTE_CASES = [
     ("channel-last L3", dict(stride_s=192, stride_d=1, stride_l=64), "vector"),
     ("channel-last L12", dict(L=12, stride_s=768, stride_d=1, stride_l=64), "staged"),
     ("padded ld", dict(ld=72), "vector"),
+    ("large batch compact", dict(N=4096, D=16384, S=4096), "bulk"),
+    ("large batch channel-last", dict(N=4096, D=16384, S=4096, stride_s=3 * 16384, stride_d=1,
+                                      stride_l=16384), "vector"),
+    ("large batch L9", dict(N=4096, D=16384, S=4096, L=9), "staged"),
 ]
 
 
@@ -174,6 +179,8 @@ def test_forced_routes(ccu):
     assert select(ccu, route=1) == (0, 1)
     assert select(ccu, route=2) == (0, 2)
     assert select(ccu, route=3) == (0, 3)
+    assert select(ccu, route=4) == (0, 4)
+    assert select(ccu, route=4, stride_s=192, stride_d=1, stride_l=64)[0] == 2  # bulk: compact only
     assert select(ccu, route=2, D=63)[0] == 2  # vector needs D % 8 == 0
     assert select(ccu, route=2, L=9)[0] == 2   # vector is compiled for L <= 8
     assert select(ccu, route=7)[0] == 1        # unknown route

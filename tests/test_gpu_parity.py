@@ -78,13 +78,15 @@ def _small(i, **over):
     return synthetic.variant(base, name=f"small{i}", **kw)
 
 
-@pytest.mark.parametrize("route", ["scalar", "vector", "staged"])
+@pytest.mark.parametrize("route", ["scalar", "vector", "staged", "bulk"])
 @pytest.mark.parametrize("layout", ["compact", "channel_last"])
 @pytest.mark.parametrize("i", range(len(SMALL)))
 def test_routes(route, layout, i):
     wl = _small(i)
-    if route == "vector" and wl.L > 8:
-        pytest.skip("vector kernels are compiled for L <= 8")
+    if route in ("vector", "bulk") and wl.L > 8:
+        pytest.skip("vector and bulk kernels are compiled for L <= 8")
+    if route == "bulk" and layout != "compact":
+        pytest.skip("the bulk kernel serves the compact layout")
     inp = synthetic.generate(wl, seed=100 + i)
     _check(inp, layout=layout, route=route, what=f"{wl} {route} {layout}")
 
@@ -284,7 +286,7 @@ def test_cuda_graph_replay_matches_eager():
 
 # ----------------------------------------------------------------------------- checked path
 
-@pytest.mark.parametrize("route", ["scalar", "vector", "staged"])
+@pytest.mark.parametrize("route", ["scalar", "vector", "staged", "bulk"])
 def test_checked_path_flags_bad_slots_without_trapping(route):
     wl = synthetic.variant(synthetic.WORKLOADS["paged_n256_d8192_l3_s1024_pad10_silu"], name="chk",
                            N=12, D=1024, S=16, indices="distinct_pad", pad_frac=0.2)
@@ -314,6 +316,25 @@ def test_checked_path_clean_inputs_report_nothing():
     got_out, got_state, status, ok = run_gpu(inp, checked=True)
     assert ok and status == 0
     assert_parity(inp, got_out, got_state, want_out, want_state, "checked clean")
+
+
+@pytest.mark.parametrize("route", ["vector", "bulk"])
+def test_large_batch_routes_agree_bitwise(route):
+    """The two large-batch kernel families give bit-identical results on a multi-tile case
+    with a ragged last chunk (D = 3*2048 + 264) and padding rows."""
+    wl = synthetic.variant(synthetic.WORKLOADS[synthetic.BENCH_WORKLOAD], name="ragged", N=300, S=300,
+                           D=6408, ld=6408)
+    inp = synthetic.generate(wl, seed=21)
+    _check(inp, route=route, what=f"ragged {route}")
+
+
+def test_no_device_error_raised():
+    import depthwise_causal_conv1d_gb300 as ccu
+
+    inp = synthetic.generate(synthetic.WORKLOADS[synthetic.BENCH_WORKLOAD])
+    run_gpu(inp, route="bulk", guards=False)
+    st, bits = ccu.ccu_conv1d_take_device_error()
+    assert st == 0 and bits == 0
 
 
 @pytest.mark.parametrize("case", ["valid", "padding", "range_low", "range_high", "duplicate", "both"])
