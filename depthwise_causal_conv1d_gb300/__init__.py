@@ -63,6 +63,8 @@ def _load() -> ctypes.CDLL:
               "ccu_conv1d_select_route", "ccu_conv1d_check_indices"):
         getattr(lib, f).restype = ctypes.c_int
     lib.ccu_conv1d_check_indices.argtypes = [vp, i64, i64, vp, vp, vp]
+    lib.ccu_conv1d_check_indices_noalloc.argtypes = [vp, i64, i64, vp, vp]
+    lib.ccu_conv1d_check_indices_noalloc.restype = ctypes.c_int
     lib.ccu_conv1d_check_indices_scratch_bytes.argtypes = [i64]
     lib.ccu_conv1d_check_indices_scratch_bytes.restype = i64
     lib.ccu_status_string.argtypes = [ctypes.c_int]
@@ -115,6 +117,19 @@ def ccu_conv1d_select_route(x, ld, conv_state, stride_s, stride_d, stride_l, wei
 
 def ccu_conv1d_check_indices(indices, N, S, bitmap_scratch, status_dev, stream) -> int:
     return lib.ccu_conv1d_check_indices(indices, N, S, bitmap_scratch, status_dev, stream)
+
+
+def ccu_conv1d_check_indices_noalloc(indices, N, S, status_dev, stream) -> int:
+    """The index check with the library's built-in bitmap (no scratch from the caller).
+
+    For callers that cannot allocate device memory. S is limited to
+    CCU_CHECK_INDICES_NOALLOC_MAX_SLOTS; calls that overlap on the GPU race on the shared
+    bitmap. The first call on a device sets up the bitmap's address.
+    """
+    return lib.ccu_conv1d_check_indices_noalloc(indices, N, S, status_dev, stream)
+
+
+CCU_CHECK_INDICES_NOALLOC_MAX_SLOTS = 1 << 20
 
 
 def ccu_conv1d_check_indices_scratch_bytes(S) -> int:

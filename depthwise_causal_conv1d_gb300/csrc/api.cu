@@ -189,6 +189,8 @@ ccu_status_t run(const Args &a, int route, cudaStream_t stream) {
 
 }  // namespace
 
+void record_error(const char *msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
+
 int current_device() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return -1;

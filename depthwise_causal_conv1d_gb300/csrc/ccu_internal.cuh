@@ -145,6 +145,8 @@ cudaError_t launch_scalar(const UpdateParams &p, int act, cudaStream_t stream);
 cudaError_t launch_vector(const UpdateParams &p, int act, cudaStream_t stream);
 cudaError_t launch_staged(const UpdateParams &p, int act, cudaStream_t stream);
 cudaError_t launch_bulk(const UpdateParams &p, int act, cudaStream_t stream);
+// Sets the calling thread's message returned by ccu_conv1d_last_error.
+void record_error(const char *msg);
 // Reads and clears the device error word that kernels without a status word report into.
 cudaError_t take_async_error(int32_t *bits);
 cudaError_t launch_check_indices(const int32_t *idx, int64_t N, int64_t S, uint32_t *bitmap,

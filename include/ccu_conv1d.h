@@ -196,6 +196,41 @@ CCU_API ccu_status_t ccu_conv1d_check_indices(const int32_t *indices, int64_t N,
                                       uint32_t *bitmap_scratch, int32_t *status_dev,
                                       ccu_stream_t stream);
 
+/*
+ * ccu_conv1d_check_indices_noalloc -- ccu_conv1d_check_indices without caller scratch.
+ *
+ * The cuDNN pages have no counterpart to this entry point; it exists for callers that
+ * cannot hand the library a scratch buffer because they cannot allocate device memory:
+ * a plugin that reaches this library through a C function table without access to the
+ * host application's allocator, or a serving loop whose owner forbids cudaMalloc between
+ * steps because it can synchronize the whole device and stall every other stream.
+ *
+ * The one-bit-per-slot bitmap lives in a fixed 128 KB array compiled into the library
+ * (CCU_CHECK_INDICES_NOALLOC_MAX_SLOTS slots); every GPU on which the library's device
+ * code is loaded keeps that array until the process exits. The call allocates nothing
+ * and calls no allocating routine: it clears the bitmap words it needs with a
+ * cudaMemsetAsync on `stream`, then runs the same check kernel on `stream`.
+ *
+ *   indices     device int32 [N], 4-byte aligned.
+ *   N, S        rows and cache slots; N == 0 is a no-op. S greater than
+ *               CCU_CHECK_INDICES_NOALLOC_MAX_SLOTS is declined with
+ *               CCU_ERR_NOT_IMPLEMENTED (use ccu_conv1d_check_indices with your own
+ *               bitmap instead).
+ *   status_dev  device int32 word; CCU_DEVERR_RANGE / CCU_DEVERR_DUPLICATE are ORed in,
+ *               never cleared.
+ *
+ * The first call on each device looks up the array's device address (a runtime symbol
+ * lookup, which can load the library's device code onto that device) and caches it; make
+ * that first call on a device before any stream capture on it. All calls in the process
+ * share the one array per device, and it keeps the previous call's contents until the
+ * next call clears it: calls that overlap on the GPU (on different streams, or from
+ * different threads without ordering) race on it and can report false duplicates or miss
+ * real ones. Order such calls, or use ccu_conv1d_check_indices with separate buffers.
+ */
+#define CCU_CHECK_INDICES_NOALLOC_MAX_SLOTS (1 << 20)
+CCU_API ccu_status_t ccu_conv1d_check_indices_noalloc(const int32_t *indices, int64_t N, int64_t S,
+                                                      int32_t *status_dev, ccu_stream_t stream);
+
 /* Bytes of scratch ccu_conv1d_check_indices needs for S slots (one bit per slot, rounded
  * up to whole 32-bit words); 0 for S <= 0. */
 CCU_API int64_t ccu_conv1d_check_indices_scratch_bytes(int64_t S);
