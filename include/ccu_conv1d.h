@@ -22,10 +22,11 @@
  *
  * Conventions shared by every entry point below:
  *  - All tensor pointers are DEVICE memory owned by the caller. The library never
- *    allocates, frees, copies between host and device or synchronizes; every call only
- *    enqueues kernels (and, for ccu_conv1d_check_indices, one memset) on `stream`, so a
- *    call can be captured in a CUDA graph. Launch errors are reported as CCU_ERR_CUDA;
- *    errors of the asynchronous execution surface at the caller's next synchronization.
+ *    allocates, frees or copies between host and device, and only
+ *    ccu_conv1d_take_device_error synchronizes. The update entry points only enqueue
+ *    kernels on `stream`, so an update call can be captured in a CUDA graph. Launch
+ *    errors are reported as CCU_ERR_CUDA; errors of the asynchronous execution surface
+ *    at the caller's next synchronization.
  *  - `stream` is a cudaStream_t; NULL is the legacy default stream.
  *  - BF16 tensors are passed as `const void*` / `void*` to 16-bit storage.
  *  - Every argument check happens before any launch; a declined call changes nothing.
