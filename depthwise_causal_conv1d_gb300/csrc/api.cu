@@ -145,6 +145,16 @@ ccu_status_t choose(int requested, const Args &a, Layout layout, int *chosen) {
   return CCU_OK;
 }
 
+// True when p is host memory (pinned or pageable) rather than device or managed memory.
+bool is_host_memory(const void *p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeHost || at.type == cudaMemoryTypeUnregistered;
+}
+
 ccu_status_t run(const Args &a, int route, cudaStream_t stream) {
   bool noop = false;
   Layout layout = Layout::Compact;
@@ -153,6 +163,15 @@ ccu_status_t run(const Args &a, int route, cudaStream_t stream) {
   int chosen = CCU_ROUTE_AUTO;
   st = choose(route, a, layout, &chosen);
   if (st != CCU_OK) return st;
+  // The bulk kernel's copies run between device memory and shared memory. x and out may
+  // also be host memory the device can address (for example pinned with cudaHostAlloc):
+  // the vector kernel reads and writes those with ordinary loads and stores.
+  if (chosen == CCU_ROUTE_BULK && (is_host_memory(a.x) || is_host_memory(a.out))) {
+    if (route == CCU_ROUTE_BULK)
+      return fail(CCU_ERR_NOT_IMPLEMENTED,
+                  "route 'bulk' needs x and out in device memory; x or out is host memory");
+    chosen = CCU_ROUTE_VECTOR;  // serves every call the bulk family serves
+  }
 
   UpdateParams p;
   p.x = static_cast<const uint16_t *>(a.x);

@@ -21,7 +21,13 @@
  * FP32, output rounded to BF16 to nearest-even. The state update is a bit copy.
  *
  * Conventions shared by every entry point below:
- *  - All tensor pointers are DEVICE memory owned by the caller. The library never
+ *  - All tensor pointers are device-accessible memory owned by the caller: device memory,
+ *    and for x and out of the update also host memory the device can address directly
+ *    (pinned with cudaHostAlloc / cudaMallocHost, or registered with cudaHostRegister's
+ *    mapped flag, under unified addressing). Host-resident x or out are read and written
+ *    in place by the kernel (no staging copy); a call the library would give to the bulk
+ *    family then runs on the vector family, which is found with cudaPointerGetAttributes
+ *    on those two pointers (launching entry points only, large calls only). The library never
  *    allocates, frees or copies between host and device, and only
  *    ccu_conv1d_take_device_error synchronizes. The update entry points only enqueue
  *    kernels on `stream`, so an update call can be captured in a CUDA graph. Launch
@@ -166,8 +172,9 @@ CCU_API ccu_status_t ccu_conv1d_update_ex(const void *x, int64_t ld, void *conv_
 
 /*
  * ccu_conv1d_select_route -- run every argument check of ccu_conv1d_update_ex and report,
- * in *chosen_route, the kernel family a call with these arguments would launch. Touches no
- * memory behind the pointers and makes no CUDA call, so it also works without a GPU.
+ * in *chosen_route, the kernel family a call with these arguments would launch when x and
+ * out are device memory. Touches no memory behind the pointers and makes no CUDA call, so
+ * it also works without a GPU.
  *
  *   chosen_route  host int32 out-parameter; set only when CCU_OK is returned (to
  *                 CCU_ROUTE_AUTO for a no-op call with N == 0 or D == 0).

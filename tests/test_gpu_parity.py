@@ -398,3 +398,30 @@ def test_typed_declines_through_binding():
         ccu.causal_conv1d_update(x, st[:3].contiguous(), w)
     # nothing was launched by any decline
     torch.cuda.synchronize()
+
+
+# ----------------------------------------------------------------------------- host buffers
+
+def test_host_resident_x_and_out():
+    """x and out in pinned host memory, read and written by the kernel in place."""
+    import depthwise_causal_conv1d_gb300 as ccu
+
+    wl = synthetic.variant(synthetic.WORKLOADS[synthetic.BENCH_WORKLOAD], name="hostio", N=520, S=520)
+    assert wl.N * wl.D >= 1 << 22  # large enough that device operands would take the bulk route
+    inp = synthetic.generate(wl, seed=33)
+    want_out, want_state = oracle_ref(inp)
+    h_x = torch.from_numpy(inp.x.view(np.int16)).pin_memory()
+    h_out = torch.full((wl.N, wl.D), -1, dtype=torch.int16).pin_memory()
+    st = to_dev_u16(inp.conv_state, DEV)
+    w, b = to_dev_u16(inp.weight, DEV), to_dev_u16(inp.bias, DEV)
+    idx = torch.from_numpy(inp.indices).to(DEV)
+    stream = torch.cuda.current_stream().cuda_stream
+    args = (h_x.data_ptr(), wl.ld, st.data_ptr(), wl.D * wl.L, wl.L, 1, w.data_ptr(), b.data_ptr(),
+            ccu.CCU_ACT_SILU, idx.data_ptr(), None, wl.N, wl.D, wl.S, wl.L, wl.W, h_out.data_ptr())
+    # a forced bulk route declines host operands; nothing is launched
+    assert ccu.ccu_conv1d_update_ex(*args, None, ccu.ROUTES["bulk"], stream) == ccu.CCU_ERR_NOT_IMPLEMENTED
+    assert ccu.ccu_conv1d_update(*args, stream) == 0, ccu.ccu_conv1d_last_error()
+    torch.cuda.synchronize()
+    got_out = h_out.numpy().view(np.uint16)
+    got_state = from_dev_u16(st)
+    assert_parity(inp, got_out, got_state, want_out, want_state, "host x/out")
