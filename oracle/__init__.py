@@ -56,6 +56,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.ccu_oracle_conv1d_update.argtypes = [
         _u16p, _i64, _u16p, _i64, _i64, _i64, _u16p, _u16p, ctypes.c_int, _i32p,
         _i64, _i64, _i64, _i64, _i64, _u16p, _f32p]
+    lib.ccu_oracle_conv1d_update_circular.restype = ctypes.c_int
+    lib.ccu_oracle_conv1d_update_circular.argtypes = [
+        _u16p, _i64, _u16p, _i64, _i64, _i64, _u16p, _u16p, ctypes.c_int, _i32p, _i32p,
+        _i64, _i64, _i64, _i64, _i64, _u16p, _f32p]
     lib.ccu_oracle_full_causal_conv.restype = ctypes.c_int
     lib.ccu_oracle_full_causal_conv.argtypes = [
         _u16p, _i64, _i64, _u16p, _u16p, ctypes.c_int, _i64, _u16p, _i64, _u16p, _u16p, _f32p]
@@ -120,6 +124,30 @@ def conv1d_update(x: np.ndarray, ld: int, conv_state: np.ndarray, strides, weigh
     return (out, acc) if with_acc else out
 
 
+def conv1d_update_circular(x: np.ndarray, ld: int, conv_state: np.ndarray, strides, weight: np.ndarray,
+                           bias: Optional[np.ndarray], act: str, indices: Optional[np.ndarray],
+                           cache_seqlens: np.ndarray, N: int, D: int, S: int, L: int, W: int, *,
+                           with_acc: bool = False, lib: Optional[ctypes.CDLL] = None):
+    """One ring-buffer decode update in place on ``conv_state``; returns out (and acc)."""
+    lib = lib or load()
+    for a in (x, conv_state, weight):
+        assert a.dtype == np.uint16 and a.flags["C_CONTIGUOUS"]
+    if indices is not None:
+        indices = np.ascontiguousarray(indices, dtype=np.int32)
+    cache_seqlens = np.ascontiguousarray(cache_seqlens, dtype=np.int32)
+    out = np.empty((N, D), dtype=np.uint16)
+    acc = np.empty((N, D), dtype=np.float32) if with_acc else None
+    rc = lib.ccu_oracle_conv1d_update_circular(
+        _ptr(x, ctypes.c_uint16), ld, _ptr(conv_state, ctypes.c_uint16),
+        strides[0], strides[1], strides[2], _ptr(weight, ctypes.c_uint16),
+        _ptr(bias, ctypes.c_uint16), ACT[act], _ptr(indices, ctypes.c_int32),
+        _ptr(cache_seqlens, ctypes.c_int32), N, D, S, L, W, _ptr(out, ctypes.c_uint16),
+        _ptr(acc, ctypes.c_float))
+    if rc != OK:
+        raise ValueError(f"oracle refused the inputs (code {rc})")
+    return (out, acc) if with_acc else out
+
+
 def full_causal_conv(x_seq: np.ndarray, weight: np.ndarray, bias: Optional[np.ndarray], act: str,
                      init_state: Optional[np.ndarray], L: int, *, with_acc: bool = False,
                      lib: Optional[ctypes.CDLL] = None):
@@ -149,7 +177,8 @@ def check_indices(indices: np.ndarray, N: int, S: int, lib: Optional[ctypes.CDLL
     return lib.ccu_oracle_check_indices(_ptr(indices, ctypes.c_int32), N, S)
 
 
-def run_workload(inp, layout: str = "compact", *, with_acc: bool = False, lib=None):
+def run_workload(inp, layout: str = "compact", *, with_acc: bool = False, lib=None,
+                 cache_seqlens: Optional[np.ndarray] = None):
     """Apply one update to a copy of a ``synthetic.Inputs``; returns (out, new_state[, acc]).
 
     ``new_state`` is returned as a logical [S, D, L] array whatever the layout.
@@ -166,8 +195,13 @@ def run_workload(inp, layout: str = "compact", *, with_acc: bool = False, lib=No
         strides = (L * D, 1, D)
     else:
         raise ValueError(layout)
-    res = conv1d_update(inp.x, wl.ld, state, strides, inp.weight, inp.bias, wl.act, inp.indices,
-                        wl.N, D, S, L, wl.W, with_acc=with_acc, lib=lib)
+    if cache_seqlens is None:
+        res = conv1d_update(inp.x, wl.ld, state, strides, inp.weight, inp.bias, wl.act, inp.indices,
+                            wl.N, D, S, L, wl.W, with_acc=with_acc, lib=lib)
+    else:
+        res = conv1d_update_circular(inp.x, wl.ld, state, strides, inp.weight, inp.bias, wl.act,
+                                     inp.indices, cache_seqlens, wl.N, D, S, L, wl.W,
+                                     with_acc=with_acc, lib=lib)
     if layout == "channel_last":
         state = np.array(np.transpose(state, (0, 2, 1)), order="C", copy=True)
     if with_acc:

@@ -25,7 +25,12 @@
  *   - SiLU is a / (1 + exp(-a)), evaluated in double from the FP32 accumulator and
  *     rounded to float;
  *   - the output is the float result rounded to BF16, nearest-even;
- *   - a padding row's output is +0.
+ *   - a padding row's output is +0;
+ *   - the circular-buffer state the page reserves cache_seqlens for (its section on the
+ *     keyword says only that a future version may use it so): the slot is a ring of L
+ *     entries, p = cache_seqlens[n] mod L indexes its oldest entry, the history is the
+ *     ring read from p onward followed by x, and the step overwrites only that oldest
+ *     entry with x. Read this way, a ring read from p is exactly the linear state.
  *
  * Build: gcc -O2 -ffp-contract=off -fPIC -shared (no fast-math, no FMA contraction).
  */
@@ -143,6 +148,68 @@ int ccu_oracle_conv1d_update(const uint16_t *x, int64_t ld, uint16_t *conv_state
 
       /* conv_state[s, d, :] = history[-L:], i.e. history[1..L]: raw bit copies */
       for (int64_t l = 0; l < L; ++l) st[l * stride_l] = history[l + 1];
+    }
+  }
+  free(history);
+  return CCU_ORACLE_OK;
+}
+
+int ccu_oracle_conv1d_update_circular(const uint16_t *x, int64_t ld, uint16_t *conv_state,
+                                      int64_t stride_s, int64_t stride_d, int64_t stride_l,
+                                      const uint16_t *weight, const uint16_t *bias, int act,
+                                      const int32_t *indices, const int32_t *cache_seqlens,
+                                      int64_t N, int64_t D, int64_t S, int64_t L, int64_t W,
+                                      uint16_t *out, float *acc_out) {
+  if (N < 0 || D < 0 || S < 0 || W < 1 || L < W - 1 || L < 1 || ld < D) return CCU_ORACLE_BAD_ARGS;
+  if (act != CCU_ORACLE_ACT_IDENTITY && act != CCU_ORACLE_ACT_SILU) return CCU_ORACLE_BAD_ARGS;
+  if (N == 0 || D == 0) return CCU_ORACLE_OK;
+  if (x == NULL || conv_state == NULL || weight == NULL || out == NULL || cache_seqlens == NULL)
+    return CCU_ORACLE_BAD_ARGS;
+  if (indices == NULL && S < N) return CCU_ORACLE_BAD_ARGS;
+  if (indices != NULL) {
+    int flags = ccu_oracle_check_indices(indices, N, S);
+    if (flags < 0) return flags;
+    if (flags != 0) return CCU_ORACLE_BAD_INDICES;
+  }
+  for (int64_t n = 0; n < N; ++n) {
+    int64_t s = indices ? (int64_t)indices[n] : n;
+    if (s != -1 && cache_seqlens[n] < 0) return CCU_ORACLE_BAD_ARGS;
+  }
+
+  uint16_t *history = (uint16_t *)malloc((size_t)(L + 1) * sizeof(uint16_t));
+  if (history == NULL) return CCU_ORACLE_NO_MEMORY;
+
+  for (int64_t n = 0; n < N; ++n) {
+    int64_t s = indices ? (int64_t)indices[n] : n;
+    if (s == -1) {
+      for (int64_t d = 0; d < D; ++d) {
+        out[n * D + d] = 0x0000u;
+        if (acc_out) acc_out[n * D + d] = 0.0f;
+      }
+      continue;
+    }
+    const int64_t p = (int64_t)cache_seqlens[n] % L; /* position of the oldest entry */
+    for (int64_t d = 0; d < D; ++d) {
+      uint16_t *ring = conv_state + s * stride_s + d * stride_d;
+
+      /* history, oldest first: the ring read from position p, then x */
+      for (int64_t i = 0; i < L; ++i) history[i] = ring[((p + i) % L) * stride_l];
+      history[L] = x[n * ld + d];
+
+      float acc = 0.0f;
+      for (int64_t j = 0; j < W; ++j) {
+        float h = ccu_oracle_bf16_to_f32(history[(L + 1) - W + j]);
+        float w = ccu_oracle_bf16_to_f32(weight[d * W + j]);
+        float term = h * w;
+        acc = acc + term;
+      }
+      if (bias != NULL) acc = acc + ccu_oracle_bf16_to_f32(bias[d]);
+
+      out[n * D + d] = ccu_oracle_f32_to_bf16(activation(acc, act));
+      if (acc_out) acc_out[n * D + d] = acc;
+
+      /* the new input replaces the oldest entry; the others stay where they are */
+      ring[p * stride_l] = history[L];
     }
   }
   free(history);

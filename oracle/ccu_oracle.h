@@ -51,6 +51,21 @@ int ccu_oracle_conv1d_update(const uint16_t *x, int64_t ld, uint16_t *conv_state
                              const int32_t *indices, int64_t N, int64_t D, int64_t S,
                              int64_t L, int64_t W, uint16_t *out, float *acc_out);
 
+/* One decode step with conv_state[s, d, :] used as a ring of L entries (the
+ * circular-buffer state the page reserves the cache_seqlens keyword for). With
+ * p = cache_seqlens[n] mod L, the slot's history, oldest first, is
+ * ring[p], ring[p+1], ..., ring[p+L-1] (indices mod L), followed by x[n, d]; the sum
+ * takes its last W entries as in ccu_oracle_conv1d_update, and the step writes only
+ * ring[p] = x[n, d] (the oldest entry). cache_seqlens [N] holds the number of inputs each
+ * row's slot has already received; it must be >= 0 for non-padding rows and is not
+ * modified. Other arguments as ccu_oracle_conv1d_update. */
+int ccu_oracle_conv1d_update_circular(const uint16_t *x, int64_t ld, uint16_t *conv_state,
+                                      int64_t stride_s, int64_t stride_d, int64_t stride_l,
+                                      const uint16_t *weight, const uint16_t *bias, int act,
+                                      const int32_t *indices, const int32_t *cache_seqlens,
+                                      int64_t N, int64_t D, int64_t S, int64_t L, int64_t W,
+                                      uint16_t *out, float *acc_out);
+
 /* Full-sequence causal depthwise convolution over T steps, written directly
  * from the convolution sum (no state shifting):
  *   y[t, d] = act( sum_{j=0}^{W-1} w[d, j] * xx(t - (W-1) + j, d) + b[d] )

@@ -297,6 +297,79 @@ def pin_check_indices(lib):
         oracle.IDX_RANGE | oracle.IDX_DUPLICATE)
 
 
+def _rotate(ring, p):
+    """The linear state a ring represents when its oldest entry sits at position p."""
+    L = ring.shape[-1]
+    return np.ascontiguousarray(ring[..., [(p + i) % L for i in range(L)]])
+
+
+def pin_circular_equals_linear_through_rotation(lib):
+    # Reading the ring from p gives the linear state: the ring update must produce the
+    # linear update's output, and its new ring read from p + 1 must be the linear new state.
+    rng = np.random.default_rng(10)
+    for L in (3, 4, 7):
+        N, D, W = 5, 9, 4
+        x = rand_bf16(rng, (N, D))
+        weight = rand_bf16(rng, (D, W))
+        bias = rand_bf16(rng, (D,), 0.1)
+        ring = rand_bf16(rng, (N, D, L))
+        seqlens = np.array([0, 1, L - 1, L + 2, 1000 * L + 5], np.int32)
+        ring_after = ring.copy()
+        out_c = oracle.conv1d_update_circular(x, D, ring_after, (D * L, L, 1), weight, bias, "silu",
+                                              None, seqlens, N, D, N, L, W, lib=lib)
+        lin = np.ascontiguousarray(np.stack([_rotate(ring[n], int(seqlens[n]) % L) for n in range(N)]))
+        out_l = oracle.conv1d_update(x, D, lin, (D * L, L, 1), weight, bias, "silu", None,
+                                     N, D, N, L, W, lib=lib)
+        assert np.array_equal(out_c, out_l), f"ring output differs from the linear one (L={L})"
+        for n in range(N):
+            p1 = (int(seqlens[n]) + 1) % L
+            assert np.array_equal(_rotate(ring_after[n], p1), lin[n]), f"ring state (L={L}, n={n})"
+
+
+def pin_circular_writes_one_entry(lib):
+    rng = np.random.default_rng(11)
+    N, D, L, W, S = 4, 6, 5, 4, 7
+    x = rand_bf16(rng, (N, D))
+    weight = rand_bf16(rng, (D, W))
+    ring = rand_bf16(rng, (S, D, L))
+    idx = np.array([6, -1, 0, 3], np.int32)
+    seqlens = np.array([2, -7, 9, 0], np.int32)  # a padding row's value is never used
+    after = ring.copy()
+    out = oracle.conv1d_update_circular(x, D, after, (D * L, L, 1), weight, None, "identity", idx,
+                                        seqlens, N, D, S, L, W, lib=lib)
+    assert np.all(out[1] == 0)
+    for n, s in enumerate(idx):
+        if s < 0:
+            continue
+        p = int(seqlens[n]) % L
+        changed = np.argwhere(after[s] != ring[s])
+        assert set(changed[:, 1].tolist()) <= {p}, "an entry other than the oldest changed"
+        assert np.array_equal(after[s][:, p], x[n])
+    untouched = [1, 2, 4, 5]
+    assert np.array_equal(after[untouched], ring[untouched])
+
+
+def pin_circular_chain_vs_full(lib):
+    # A ring fed T inputs with cache_seqlens 0, 1, 2, ... equals the direct convolution.
+    rng = np.random.default_rng(12)
+    for L in (3, 6):
+        W, D, T = 4, 11, 14
+        x_seq = rand_bf16(rng, (T, D))
+        weight = rand_bf16(rng, (D, W), 0.5)
+        bias = rand_bf16(rng, (D,), 0.1)
+        ring = np.zeros((1, D, L), np.uint16)
+        ys = []
+        for t in range(T):
+            ys.append(oracle.conv1d_update_circular(x_seq[t:t + 1].copy(), D, ring, (D * L, L, 1), weight,
+                                                    bias, "identity", None, np.array([t], np.int32),
+                                                    1, D, 1, L, W, lib=lib)[0])
+        y_full, fin = oracle.full_causal_conv(x_seq, weight, bias, "identity", None, L, lib=lib)
+        assert np.array_equal(np.stack(ys), y_full), f"ring chain vs full conv (L={L})"
+        assert np.array_equal(_rotate(ring[0], T % L), fin), f"ring after T steps (L={L})"
+
+
 ALL_PINS = [pin_golden, pin_bf16_conversion, pin_silu, pin_one_hot, pin_chain_vs_full,
             pin_full_vs_convolve, pin_closed_form, pin_padding_and_untouched, pin_routing,
-            pin_layouts, pin_padded_ld, pin_check_indices]
+            pin_layouts, pin_padded_ld, pin_check_indices,
+            pin_circular_equals_linear_through_rotation, pin_circular_writes_one_entry,
+            pin_circular_chain_vs_full]

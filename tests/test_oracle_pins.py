@@ -65,6 +65,12 @@ MUTATIONS = [
      "float term = ccu_oracle_bf16_to_f32(v) * ccu_oracle_bf16_to_f32(weight[d * W + j]);",
      "float term = ccu_oracle_bf16_to_f32(v) * ccu_oracle_bf16_to_f32(weight[d * W + W - 1 - j]);"),
     ("duplicate slots accepted", "if (seen[s]) flags |= CCU_ORACLE_IDX_DUPLICATE;", ""),
+    ("ring read backwards", "history[i] = ring[((p + i) % L) * stride_l];",
+     "history[i] = ring[((p + L - i) % L) * stride_l];"),
+    ("ring writes the newest slot", "ring[p * stride_l] = history[L];",
+     "ring[((p + L - 1) % L) * stride_l] = history[L];"),
+    ("ring ignores seqlens", "const int64_t p = (int64_t)cache_seqlens[n] % L;",
+     "const int64_t p = 0;"),
 ]
 
 
@@ -78,13 +84,33 @@ def _pins_fail(lib):
     return failed
 
 
-@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
-def test_planted_mistake_is_caught(name, old, new, tmp_path):
+# The same mistakes planted in the ring-buffer update (second occurrence of the line).
+MUTATIONS += [
+    ("ring update taps reversed", "float w = ccu_oracle_bf16_to_f32(weight[d * W + j]);",
+     "float w = ccu_oracle_bf16_to_f32(weight[d * W + (W - 1 - j)]);", 2),
+    ("ring update bias dropped", "if (bias != NULL) acc = acc + ccu_oracle_bf16_to_f32(bias[d]);\n\n      out[n * D + d]",
+     "\n\n      out[n * D + d]", 2),
+    ("ring update window off by one", "float h = ccu_oracle_bf16_to_f32(history[(L + 1) - W + j]);",
+     "float h = ccu_oracle_bf16_to_f32(history[L - W + j]);", 2),
+]
+
+
+def _replace_nth(src, old, new, nth):
+    at = -1
+    for _ in range(nth):
+        at = src.index(old, at + 1)
+    return src[:at] + new + src[at + len(old):]
+
+
+@pytest.mark.parametrize("mutation", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(mutation, tmp_path):
+    name, old, new = mutation[:3]
+    nth = mutation[3] if len(mutation) > 3 else 1
     src_dir = os.path.dirname(oracle.__file__)
     src = open(os.path.join(src_dir, "ccu_oracle.c")).read()
-    assert src.count(old) == 1, f"mutation anchor for {name!r} not unique"
+    assert src.count(old) >= nth, f"mutation anchor for {name!r} not found"
     shutil.copy(os.path.join(src_dir, "ccu_oracle.h"), tmp_path / "ccu_oracle.h")
-    (tmp_path / "ccu_oracle.c").write_text(src.replace(old, new))
+    (tmp_path / "ccu_oracle.c").write_text(_replace_nth(src, old, new, nth))
     lib_path = str(tmp_path / "libmutant.so")
     oracle.build(src=str(tmp_path / "ccu_oracle.c"), out=lib_path)
     failed = _pins_fail(oracle.load(lib_path))
