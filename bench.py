@@ -43,6 +43,10 @@ import numpy as np  # noqa: E402
 import synthetic  # noqa: E402
 
 METRIC = "conv1d_update HBM GB/s (% of GB300 peak) and µs/call vs N·D, 1 GPU"
+try:
+    PEAK_GBPS = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["hbm_gbs"])
+except (OSError, KeyError, ValueError):
+    PEAK_GBPS = 6800.0  # fallback figure when the measured peaks are absent
 UNIT = "GB/s"
 L2_BYTES = 129 * 1024 * 1024
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "update_bulk_large_n4096_d16384.txt")
@@ -263,6 +267,8 @@ class Resident:
         self.w = to_dev(inp.weight, dev)
         self.b = to_dev(inp.bias, dev) if inp.bias is not None else None
         self.idx = torch.from_numpy(inp.indices).to(dev) if inp.indices is not None else None
+        self.seq = (torch.from_numpy(inp.cache_seqlens).to(dev) if inp.cache_seqlens is not None
+                    else None)
         self.out = torch.empty((wl.N, wl.D), dtype=torch.bfloat16, device=dev)
         self.stream = stream
         self.route = ccu.ROUTES[route]
@@ -270,7 +276,8 @@ class Resident:
         self.args = (self.x.data_ptr(), wl.ld, self.state.data_ptr(), ss, sd, sl, self.w.data_ptr(),
                      None if self.b is None else self.b.data_ptr(),
                      ccu.CCU_ACT_SILU if wl.act == "silu" else ccu.CCU_ACT_IDENTITY,
-                     None if self.idx is None else self.idx.data_ptr(), None,
+                     None if self.idx is None else self.idx.data_ptr(),
+                     None if self.seq is None else self.seq.data_ptr(),
                      wl.N, wl.D, wl.S, wl.L, wl.W, self.out.data_ptr(), None, self.route,
                      stream.cuda_stream)
         st, chosen = ccu.ccu_conv1d_select_route(*self.args[:17], self.route)
@@ -457,9 +464,9 @@ def per_workload_table(dev, stream, reps=50):
 
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
     rows = {}
-    for name, wl in synthetic.WORKLOADS.items():
+    for name, wl in {**synthetic.WORKLOADS, **synthetic.RING_WORKLOADS}.items():
         inp = synthetic.generate(wl)
-        res = Resident(inp, dev, stream)
+        res = Resident(inp, dev, stream, layout=wl.layout)
         nbytes = synthetic.algorithmic_bytes(wl, inp.indices)
         for _ in range(5):
             res.call()
@@ -500,9 +507,11 @@ def per_workload_table(dev, stream, reps=50):
         torch.cuda.synchronize()
         graph_us = g0.elapsed_time(g1) * 1e3 / 2000
         rows[name] = {"N_x_D": wl.N * wl.D, "bytes": nbytes, "route": res.route_name,
+                      "state": f"{'ring' if wl.ring else 'linear'} {wl.layout}",
                       "eager_us": round(eager_us, 3), "graph_us": round(graph_us, 3),
                       "cold_us": round(cold_us, 3),
-                      "cold_GBps": round(nbytes / (cold_us * 1e-6) / 1e9, 1)}
+                      "cold_GBps": round(nbytes / (cold_us * 1e-6) / 1e9, 1),
+                      "warm_frac": round(nbytes / (eager_us * 1e-6) / 1e9 / PEAK_GBPS, 4)}
         del g, res
     del flush
     return rows

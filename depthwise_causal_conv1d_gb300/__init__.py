@@ -197,14 +197,13 @@ def causal_conv1d_update(x, conv_state, weight, bias=None, activation=None, *, c
     ``[S, D, L]``, compact or channel-last ``(L*D, 1, D)``; ``weight`` BF16 ``[D, 4]``;
     ``bias`` BF16 ``[D]`` or None; ``activation`` None/"identity" or "silu"/"swish";
     ``conv_state_indices`` int32 ``[N]`` (``-1`` = padding row) or None; ``cache_seqlens``
-    must be None. ``out`` (optional, preallocated ``[N, D]`` BF16), ``route`` (kernel
+    None (linear state) or int32 ``[N]``: the state is then a ring buffer whose oldest entry
+    is at ``cache_seqlens[n] % L`` and only that entry is overwritten. ``out`` (optional, preallocated ``[N, D]`` BF16), ``route`` (kernel
     family) and ``status`` (int32 device word: turns on the device range check) are
     extensions of this binding. Runs on the current CUDA stream.
     """
     import torch
 
-    if cache_seqlens is not None:
-        raise NotImplementedError("cache_seqlens must be None: circular-buffer state is not served")
     if activation not in _ACTIVATIONS:
         raise ValueError(f"activation must be one of None, 'identity', 'silu', 'swish'; got {activation!r}")
     _check_tensor("x", x, torch.bfloat16, torch)
@@ -233,6 +232,10 @@ def causal_conv1d_update(x, conv_state, weight, bias=None, activation=None, *, c
         _check_tensor("conv_state_indices", conv_state_indices, torch.int32, torch)
         if conv_state_indices.shape != (N,) or not conv_state_indices.is_contiguous():
             raise ValueError("conv_state_indices must be a contiguous int32 [N] tensor")
+    if cache_seqlens is not None:
+        _check_tensor("cache_seqlens", cache_seqlens, torch.int32, torch)
+        if cache_seqlens.shape != (N,) or not cache_seqlens.is_contiguous():
+            raise ValueError("cache_seqlens must be a contiguous int32 [N] tensor")
     if out is None:
         out = torch.empty((N, D), dtype=torch.bfloat16, device=x.device)
     else:
@@ -248,7 +251,7 @@ def causal_conv1d_update(x, conv_state, weight, bias=None, activation=None, *, c
     stream = torch.cuda.current_stream(x.device).cuda_stream
     st = lib.ccu_conv1d_update_ex(
         _ptr(x), ld, _ptr(conv_state), ss, sd, sl, _ptr(weight), _ptr(bias),
-        _ACTIVATIONS[activation], _ptr(conv_state_indices), None, N, D, S, L, W, _ptr(out),
+        _ACTIVATIONS[activation], _ptr(conv_state_indices), _ptr(cache_seqlens), N, D, S, L, W, _ptr(out),
         _ptr(status), ROUTES[route], stream)
     raise_for_status(st)
     return out

@@ -23,6 +23,7 @@ struct UpdateParams {
   const uint16_t *w;      // [D, 4]
   const uint16_t *bias;   // [D] or nullptr
   const int32_t *idx;     // [N] or nullptr
+  const int32_t *seqlens; // [N] cache_seqlens (ring-buffer state) or nullptr (linear state)
   uint16_t *out;          // [N, D]
   int32_t *status;        // nullptr: unchecked; else device error word (range check on)
   int64_t N, D, S, L;
@@ -138,6 +139,113 @@ __device__ __forceinline__ uint4 update8_compact(const uint32_t (&xw)[4], const 
                     pack_bf16x2(y[6], y[7]));
 }
 
+// Slot of row n and, for a ring-buffer state, the ring position of its oldest entry:
+// q = cache_seqlens[n] mod L (taken non-negative, so every access stays inside the slot
+// whatever the value). In checked mode a negative cache_seqlens of a non-padding row
+// raises CCU_DEVERR_RANGE and the row is treated as padding.
+struct RowSlot {
+  int64_t s;
+  int q;
+};
+
+__device__ __forceinline__ RowSlot resolve_row(const UpdateParams &p, int64_t n) {
+  RowSlot r;
+  r.s = resolve_slot(p, n);
+  r.q = 0;
+  if (r.s >= 0 && p.seqlens != nullptr) {
+    const int64_t v = __ldg(p.seqlens + n);
+    if (v < 0 && p.status != nullptr) {
+      atomicOr(p.status, 1);  // CCU_DEVERR_RANGE
+      r.s = -1;
+    } else {
+      int64_t m = v % p.L;
+      r.q = (int)(m < 0 ? m + p.L : m);
+    }
+  }
+  return r;
+}
+
+// The ring-buffer form of update8_compact for a ring position Q known at compile time:
+// the 8 channels' rings sit in `ow` (flat position c*L + l) and Q is the ring position of
+// the oldest entry. The history, oldest first, is ring[Q], ring[Q+1], ..., ring[Q+L-1]
+// (mod L) followed by x, so the width-4 window is ring[(Q+L-3) % L], ring[(Q+L-2) % L],
+// ring[(Q+L-1) % L], x. The new rings in `nw` equal the old ones with entry Q replaced by x.
+template <int L, int ACT, int Q>
+__device__ __forceinline__ uint4 update8_ring_q(const uint32_t (&xw)[4], const uint32_t (&ow)[4 * L],
+                                                const uint32_t (&wv)[16], const uint32_t (&bv)[4],
+                                                bool has_bias, uint32_t (&nw)[4 * L]) {
+  float y[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    float acc = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kW - 1; ++k) {
+      const uint32_t h = get16(ow, c * L + (Q + L - (kW - 1) + k) % L);
+      acc = __fmaf_rn(bf16_bits(h), bf16_bits(get16(wv, c * kW + k)), acc);
+    }
+    acc = __fmaf_rn(bf16_bits(get16(xw, c)), bf16_bits(get16(wv, c * kW + kW - 1)), acc);
+    if (has_bias) acc = acc + bf16_bits(get16(bv, c));
+    y[c] = activate<ACT>(acc);
+  }
+#pragma unroll
+  for (int i = 0; i < 4 * L; ++i) {
+    const int e0 = 2 * i, e1 = 2 * i + 1;
+    const uint32_t v0 = (e0 % L == Q) ? get16(xw, e0 / L) : get16(ow, e0);
+    const uint32_t v1 = (e1 % L == Q) ? get16(xw, e1 / L) : get16(ow, e1);
+    nw[i] = v0 | (v1 << 16);
+  }
+  return make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                    pack_bf16x2(y[6], y[7]));
+}
+
+// Runtime ring position q in [0, L): one branch to the matching compile-time form (q is
+// the same for every lane of a row, so the branch does not diverge within a row).
+template <int L, int ACT>
+__device__ __forceinline__ uint4 update8_compact_ring(const uint32_t (&xw)[4], const uint32_t (&ow)[4 * L],
+                                                      const uint32_t (&wv)[16], const uint32_t (&bv)[4],
+                                                      bool has_bias, int q, uint32_t (&nw)[4 * L]) {
+  switch (q) {
+    case 0: return update8_ring_q<L, ACT, 0>(xw, ow, wv, bv, has_bias, nw);
+    case 1: return update8_ring_q<L, ACT, 1 % L>(xw, ow, wv, bv, has_bias, nw);
+    case 2: return update8_ring_q<L, ACT, 2 % L>(xw, ow, wv, bv, has_bias, nw);
+    case 3: return update8_ring_q<L, ACT, 3 % L>(xw, ow, wv, bv, has_bias, nw);
+    case 4: return update8_ring_q<L, ACT, 4 % L>(xw, ow, wv, bv, has_bias, nw);
+    case 5: return update8_ring_q<L, ACT, 5 % L>(xw, ow, wv, bv, has_bias, nw);
+    case 6: return update8_ring_q<L, ACT, 6 % L>(xw, ow, wv, bv, has_bias, nw);
+    default: return update8_ring_q<L, ACT, 7 % L>(xw, ow, wv, bv, has_bias, nw);
+  }
+}
+
+// Outputs of 8 channels from the three window entries (h[k][c]) and x (xs[c]).
+template <int ACT>
+__device__ __forceinline__ uint4 outputs8_window(const uint32_t (&h)[3][8], const uint32_t (&xs)[8],
+                                                 const uint32_t (&wv)[16], const uint32_t (&bv)[4],
+                                                 bool has_bias) {
+  float y[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    float acc = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kW - 1; ++k)
+      acc = __fmaf_rn(bf16_bits(h[k][c]), bf16_bits(get16(wv, c * kW + k)), acc);
+    acc = __fmaf_rn(bf16_bits(xs[c]), bf16_bits(get16(wv, c * kW + kW - 1)), acc);
+    if (has_bias) acc = acc + bf16_bits(get16(bv, c));
+    y[c] = activate<ACT>(acc);
+  }
+  return make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                    pack_bf16x2(y[6], y[7]));
+}
+
+// Unpack a 16-byte vector of 8 BF16 into 8 raw 16-bit values.
+__device__ __forceinline__ void unpack8(const uint4 v, uint32_t (&e)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    e[2 * i] = w[i] & 0xffffu;
+    e[2 * i + 1] = w[i] >> 16;
+  }
+}
+
 // ---------------------------------------------------------------------------------------
 // Kernel launchers (one per family). Each returns the cudaError_t of its launch.
 
@@ -145,6 +253,8 @@ cudaError_t launch_scalar(const UpdateParams &p, int act, cudaStream_t stream);
 cudaError_t launch_vector(const UpdateParams &p, int act, cudaStream_t stream);
 cudaError_t launch_staged(const UpdateParams &p, int act, cudaStream_t stream);
 cudaError_t launch_bulk(const UpdateParams &p, int act, cudaStream_t stream);
+cudaError_t launch_bulk_planes(const UpdateParams &p, int act, cudaStream_t stream);
+cudaError_t take_planes_error(int32_t *bits);
 // Sets the calling thread's message returned by ccu_conv1d_last_error.
 void record_error(const char *msg);
 // Reads and clears the device error word that kernels without a status word report into.

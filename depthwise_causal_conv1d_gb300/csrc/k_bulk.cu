@@ -1,4 +1,5 @@
-// Bulk-copy kernel for large batches (compact state layout, L = 3..8, D % 8 == 0).
+// Bulk-copy kernel for large batches (compact state layout, L = 3..8, D % 8 == 0; the
+// channel-last layout has its own bulk kernel in k_bulk_planes.cu).
 //
 // Every warp is an independent pipeline. Its work items are slices (row n, 256*G
 // consecutive channels); lane 0 moves whole slices between global and shared memory with
@@ -18,7 +19,7 @@
 // tensor contract".
 #include <atomic>
 
-#include "ccu_internal.cuh"
+#include "ccu_bulk.cuh"
 
 namespace ccu {
 
@@ -29,113 +30,11 @@ __device__ int32_t g_async_error = 0;  // CCU_DEVERR_* bits raised by a kernel w
 
 namespace {
 
-constexpr int kThreads = 256;              // 8 warps per CTA
-constexpr int kWarps = kThreads / 32;
-constexpr int kMaxStages = 8;
-constexpr int kBarrierBytes = 64;           // a warp's P mbarriers, padded
-constexpr uint32_t kMaxSpins = 1u << 22;    // try_wait rounds before a wait is declared failed
-constexpr unsigned kFull = 0xffffffffu;
-
-__device__ __forceinline__ uint32_t smem_addr(const void *p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void fence_mbar_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
-               "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
-// Bounded wait for the phase with the given parity to complete.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kMaxSpins; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
-}
-
-// global -> shared bulk copy; completes `bytes` of transaction count on `bar`.
-__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
-}
-
-// shared -> global bulk copy, tracked by bulk async-groups.
-__device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
-               "r"(smem_addr(src)), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-
-// All but the newest N committed store groups have finished reading shared memory.
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
-// Generic-proxy writes to shared memory become visible to the bulk-copy (async) proxy.
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-struct Slice {
-  int64_t n, c_base, cn, s;
-};
-
-template <int G>
-__device__ __forceinline__ Slice slice_of(const UpdateParams &p, int64_t t, int64_t slices, bool report) {
-  constexpr int64_t kSlice = 256 * G;
-  Slice sl;
-  sl.n = t / slices;
-  sl.c_base = (t - sl.n * slices) * kSlice;
-  const int64_t rem = p.D - sl.c_base;
-  sl.cn = rem < kSlice ? rem : kSlice;
-  if (p.idx == nullptr) {
-    sl.s = sl.n;
-  } else {
-    sl.s = __ldg(p.idx + sl.n);
-    if (p.status != nullptr && (sl.s < -1 || sl.s >= p.S)) {
-      if (report) atomicOr(p.status, 1);  // CCU_DEVERR_RANGE
-      sl.s = -1;
-    }
-  }
-  return sl;
-}
+using namespace bulk;
 
 // Shared memory per warp: kBarrierBytes of mbarriers, then P stages of stage_bytes.
-template <int L, int ACT, int G>
+// RING: conv_state is a ring buffer indexed by cache_seqlens (entry q replaced by x).
+template <int L, int ACT, int G, bool RING>
 __global__ void __launch_bounds__(kThreads) k_update_bulk(UpdateParams p, int stages, int64_t stage_bytes) {
   constexpr int64_t kSlice = 256 * G;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -235,7 +134,12 @@ __global__ void __launch_bounds__(kThreads) k_update_bulk(UpdateParams p, int st
         const uint4 t = ss[q];
         ow[4 * q] = t.x; ow[4 * q + 1] = t.y; ow[4 * q + 2] = t.z; ow[4 * q + 3] = t.w;
       }
-      const uint4 outv = update8_compact<L, ACT>(xw, ow, wv[g], bv[g], has_bias, nw);
+      uint4 outv;
+      if constexpr (RING) {
+        outv = update8_compact_ring<L, ACT>(xw, ow, wv[g], bv[g], has_bias, sl.q, nw);
+      } else {
+        outv = update8_compact<L, ACT>(xw, ow, wv[g], bv[g], has_bias, nw);
+      }
 #pragma unroll
       for (int q = 0; q < L; ++q) ss[q] = make_uint4(nw[4 * q], nw[4 * q + 1], nw[4 * q + 2], nw[4 * q + 3]);
       *sx = outv;
@@ -269,7 +173,7 @@ __global__ void __launch_bounds__(kThreads) k_update_bulk(UpdateParams p, int st
 }
 
 constexpr int kMaxDevices = 64;
-std::atomic<bool> g_opted_in[kMaxDevices][kVectorMaxL + 1][2];
+std::atomic<bool> g_opted_in[kMaxDevices][kVectorMaxL + 1][2][2];
 
 constexpr int kGroups = 2;  // 8-channel groups per lane: slices of 512 channels
 
@@ -278,8 +182,8 @@ int64_t stage_bytes_for(int64_t L) {
   return (b + 127) / 128 * 128;
 }
 
-template <int L, int ACT>
-cudaError_t launch_LA(const UpdateParams &p, cudaStream_t stream) {
+template <int L, int ACT, bool RING>
+cudaError_t launch_LAR(const UpdateParams &p, cudaStream_t stream) {
   const int64_t sb = stage_bytes_for(L);
   // About 8 KB of stages per warp (two 4 KB stages at L = 3): 3 CTAs of 8 warps fit an SM.
   // Measured on the large batch: slices of 512 channels with two stages beat 256-channel
@@ -289,15 +193,15 @@ cudaError_t launch_LA(const UpdateParams &p, cudaStream_t stream) {
   const size_t smem = (size_t)kWarps * (kBarrierBytes + (size_t)P * sb);
   const int dev = current_device();
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!g_opted_in[dev][L][ACT].load(std::memory_order_acquire)) {
-    cudaError_t e = cudaFuncSetAttribute(k_update_bulk<L, ACT, kGroups>,
+  if (!g_opted_in[dev][L][ACT][RING].load(std::memory_order_acquire)) {
+    cudaError_t e = cudaFuncSetAttribute(k_update_bulk<L, ACT, kGroups, RING>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    g_opted_in[dev][L][ACT].store(true, std::memory_order_release);
+    g_opted_in[dev][L][ACT][RING].store(true, std::memory_order_release);
   }
   int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_update_bulk<L, ACT, kGroups>,
-                                                                kThreads, smem);
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &per_sm, k_update_bulk<L, ACT, kGroups, RING>, kThreads, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   const int64_t slices = (p.D + 256 * kGroups - 1) / (256 * kGroups);
@@ -309,8 +213,13 @@ cudaError_t launch_LA(const UpdateParams &p, cudaStream_t stream) {
   if (warps > items) warps = items;
   int64_t grid = (warps + kWarps - 1) / kWarps;
   if (grid < 1) grid = 1;
-  k_update_bulk<L, ACT, kGroups><<<(unsigned)grid, kThreads, smem, stream>>>(p, P, sb);
+  k_update_bulk<L, ACT, kGroups, RING><<<(unsigned)grid, kThreads, smem, stream>>>(p, P, sb);
   return cudaGetLastError();
+}
+
+template <int L, int ACT>
+cudaError_t launch_LA(const UpdateParams &p, cudaStream_t stream) {
+  return p.seqlens != nullptr ? launch_LAR<L, ACT, true>(p, stream) : launch_LAR<L, ACT, false>(p, stream);
 }
 
 template <int ACT>
@@ -329,14 +238,16 @@ cudaError_t launch_A(const UpdateParams &p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t take_async_error(int32_t *bits) {
-  int32_t zero = 0;
+  int32_t zero = 0, planes = 0;
   cudaError_t e = cudaMemcpyFromSymbol(bits, g_async_error, sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_async_error, &zero, sizeof(int32_t));
+  if (e == cudaSuccess) e = take_planes_error(&planes);
+  if (e == cudaSuccess) *bits |= planes;
   return e;
 }
 
 cudaError_t launch_bulk(const UpdateParams &p, int act, cudaStream_t stream) {
-  if (p.layout != (int)Layout::Compact) return cudaErrorInvalidValue;
+  if (p.layout == (int)Layout::ChannelLast) return launch_bulk_planes(p, act, stream);
   return act == 1 ? launch_A<1>(p, stream) : launch_A<0>(p, stream);
 }
 

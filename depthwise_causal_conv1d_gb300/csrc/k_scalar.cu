@@ -20,18 +20,20 @@ __global__ void __launch_bounds__(256) k_update_scalar(UpdateParams p) {
        i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t n = i / p.D;
     const int64_t d = i - n * p.D;
-    const int64_t s = resolve_slot(p, n);
-    if (s < 0) {
+    const RowSlot r = resolve_row(p, n);
+    if (r.s < 0) {
       p.out[n * p.D + d] = 0;  // padding row: +0, no state access
       continue;
     }
-    uint16_t *st = p.state + s * p.ss + d * p.sd;
+    uint16_t *st = p.state + r.s * p.ss + d * p.sd;
     const int64_t L = p.L;
     const uint16_t xv = p.x[n * p.ld + d];
-    // history = [st[0], ..., st[L-1], x]; the width-4 window is its last four entries.
-    const uint16_t h0 = st[(L - 3) * p.sl];
-    const uint16_t h1 = st[(L - 2) * p.sl];
-    const uint16_t h2 = st[(L - 1) * p.sl];
+    // history = [st[0], ..., st[L-1], x] (linear), or the ring read from its oldest entry
+    // q followed by x; the width-4 window is the last four entries of the history.
+    const int64_t q = p.seqlens != nullptr ? r.q : 0;
+    const uint16_t h0 = st[((q + L - 3) % L) * p.sl];
+    const uint16_t h1 = st[((q + L - 2) % L) * p.sl];
+    const uint16_t h2 = st[((q + L - 1) % L) * p.sl];
     const uint16_t *w = p.w + d * kW;
     float acc = 0.0f;
     acc = __fmaf_rn(bf16_bits(h0), bf16_bits(w[0]), acc);
@@ -40,9 +42,13 @@ __global__ void __launch_bounds__(256) k_update_scalar(UpdateParams p) {
     acc = __fmaf_rn(bf16_bits(xv), bf16_bits(w[3]), acc);
     if (p.bias != nullptr) acc = acc + bf16_bits(p.bias[d]);
     p.out[n * p.D + d] = round_bf16(activate<ACT>(acc));
-    // conv_state[s, d, :] = history[1:], ascending so every entry is read before overwritten
-    for (int64_t l = 0; l + 1 < L; ++l) st[l * p.sl] = st[(l + 1) * p.sl];
-    st[(L - 1) * p.sl] = xv;
+    if (p.seqlens != nullptr) {
+      st[q * p.sl] = xv;  // ring: the new input replaces the oldest entry
+    } else {
+      // conv_state[s, d, :] = history[1:], ascending so each entry is read before overwritten
+      for (int64_t l = 0; l + 1 < L; ++l) st[l * p.sl] = st[(l + 1) * p.sl];
+      st[(L - 1) * p.sl] = xv;
+    }
   }
 }
 

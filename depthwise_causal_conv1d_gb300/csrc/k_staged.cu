@@ -90,8 +90,11 @@ __global__ void __launch_bounds__(256) k_update_staged_compact(UpdateParams p) {
   float wf[8][kW], bf[8];
   if (mine) load_weights8(p, c_base + 8 * tid, wf, bf);
 
+  const bool ring = p.seqlens != nullptr;
   for (int64_t n = blockIdx.y; n < p.N; n += gridDim.y) {
-    const int64_t s = resolve_slot(p, n);  // same for the whole CTA
+    const RowSlot row = resolve_row(p, n);  // same for the whole CTA
+    const int64_t s = row.s;
+    const int64_t q = row.q;                // ring position of the oldest entry
     uint16_t *outp = p.out + n * p.D + c_base + 8 * tid;
     if (s < 0) {
       if (mine) st_stream(outp, make_uint4(0u, 0u, 0u, 0u));
@@ -109,9 +112,15 @@ __global__ void __launch_bounds__(256) k_update_staged_compact(UpdateParams p) {
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         const int64_t base = (int64_t)(8 * tid + c) * L;
-        h[0][c] = s_state[base + L - 3];
-        h[1][c] = s_state[base + L - 2];
-        h[2][c] = s_state[base + L - 1];
+        if (ring) {  // the window is the ring read from q: positions q+L-3 .. q+L-1 mod L
+          h[0][c] = s_state[base + (q + L - 3) % L];
+          h[1][c] = s_state[base + (q + L - 2) % L];
+          h[2][c] = s_state[base + (q + L - 1) % L];
+        } else {
+          h[0][c] = s_state[base + L - 3];
+          h[1][c] = s_state[base + L - 2];
+          h[2][c] = s_state[base + L - 1];
+        }
         xs[c] = s_x[8 * tid + c];
       }
       st_stream(outp, outputs8<ACT>(h, xs, wf, bf, has_bias));
@@ -125,7 +134,13 @@ __global__ void __launch_bounds__(256) k_update_staged_compact(UpdateParams p) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         uint32_t val;
-        if (l == L - 1) {
+        if (ring) {  // ring: only the oldest entry q of each channel takes x
+          val = (l == q) ? (uint32_t)s_x[c] : (uint32_t)s_state[e0 + i];
+          if (++l == L) {
+            l = 0;
+            ++c;
+          }
+        } else if (l == L - 1) {
           val = s_x[c];
           l = 0;
           ++c;
@@ -159,7 +174,8 @@ __global__ void __launch_bounds__(256) k_update_staged_chlast(UpdateParams p) {
   load_weights8(p, c0, wf, bf);
 
   for (int64_t n = blockIdx.y; n < p.N; n += gridDim.y) {
-    const int64_t s = resolve_slot(p, n);
+    const RowSlot row = resolve_row(p, n);
+    const int64_t s = row.s;
     uint16_t *outp = p.out + n * p.D + c0;
     if (s < 0) {
       st_stream(outp, make_uint4(0u, 0u, 0u, 0u));
@@ -167,6 +183,17 @@ __global__ void __launch_bounds__(256) k_update_staged_chlast(UpdateParams p) {
     }
     const uint4 xv = ld_stream(p.x + n * p.ld + c0);
     uint16_t *sp = p.state + s * (L * p.D) + c0;
+    if (p.seqlens != nullptr) {
+      // Ring in planes: read the three window planes, write x over the oldest plane.
+      const int64_t q = row.q;
+      uint32_t h[3][8], xs[8];
+#pragma unroll
+      for (int k = 0; k < 3; ++k) unpack8(ld_stream(sp + ((q + L - 3 + k) % L) * p.D), h[k]);
+      unpack8(xv, xs);
+      st_stream(sp + q * p.D, xv);
+      st_stream(outp, outputs8<ACT>(h, xs, wf, bf, has_bias));
+      continue;
+    }
     // window planes L-3..L-1 (plane 0 is read only when L == 3: it is then in the window)
     uint4 win[3];
     if (L == kW - 1) win[0] = ld_stream(sp);

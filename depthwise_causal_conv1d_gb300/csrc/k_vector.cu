@@ -23,7 +23,8 @@ __device__ __forceinline__ constexpr int elem_pos(int c, int l) {
   return LAYOUT == (int)Layout::Compact ? c * L + l : l * 8 + c;
 }
 
-template <int L, int ACT, int LAYOUT>
+// RING: conv_state is a ring buffer indexed by cache_seqlens (see resolve_row).
+template <int L, int ACT, int LAYOUT, bool RING>
 __global__ void __launch_bounds__(256) k_update_vector(UpdateParams p) {
   const int64_t groups = p.D >> 3;  // 8-channel groups per row (D % 8 == 0)
   const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -48,95 +49,129 @@ __global__ void __launch_bounds__(256) k_update_vector(UpdateParams p) {
     bv[0] = t.x; bv[1] = t.y; bv[2] = t.z; bv[3] = t.w;
   }
 
+  // A thread walks R rows two at a time: the loads of both rows (slot, x and state) are
+  // issued before either is computed and stored, so two rows' loads are in flight per
+  // thread whatever the compiler's schedule (left to itself, the schedule of the compact
+  // single-row loop varied between builds from 168 to 303 us on the large batch). Slots
+  // are unique within a call, so one row's stores never touch the other row's state.
+  constexpr bool kPlanes = (LAYOUT == (int)Layout::ChannelLast);
+  // State words held per row: compact 4L; channel-last linear 4L (plane 0 unused when
+  // L > 3); channel-last ring: the three window planes.
+  constexpr int kWords = (kPlanes && RING) ? 4 * (kW - 1) : 4 * L;
+  struct Row {
+    RowSlot slot;
+    uint32_t xw[4];
+    uint32_t ow[kWords];
+  };
+
+  auto load_row = [&](int64_t n, Row &r) {
+    r.slot = resolve_row(p, n);
+    if (r.slot.s < 0) return;
+    const uint4 t = ld_stream(p.x + n * p.ld + c0);
+    r.xw[0] = t.x; r.xw[1] = t.y; r.xw[2] = t.z; r.xw[3] = t.w;
+    if constexpr (!kPlanes) {
+      const uint16_t *sp = p.state + r.slot.s * (p.D * L) + c0 * L;
+#pragma unroll
+      for (int k = 0; k < L; ++k) {
+        const uint4 u = ld_stream(sp + 8 * k);
+        r.ow[4 * k] = u.x; r.ow[4 * k + 1] = u.y; r.ow[4 * k + 2] = u.z; r.ow[4 * k + 3] = u.w;
+      }
+    } else if constexpr (RING) {
+      const uint16_t *sp = p.state + r.slot.s * (L * p.D) + c0;
+#pragma unroll
+      for (int k = 0; k < kW - 1; ++k) {
+        const uint4 u = ld_stream(sp + (int64_t)((r.slot.q + L - (kW - 1) + k) % L) * p.D);
+        r.ow[4 * k] = u.x; r.ow[4 * k + 1] = u.y; r.ow[4 * k + 2] = u.z; r.ow[4 * k + 3] = u.w;
+      }
+    } else {
+      // Plane 0 is read only when L == 3: it is then inside the width-4 window; otherwise
+      // it is outside the window and is overwritten by plane 1.
+      const uint16_t *sp = p.state + r.slot.s * (L * p.D) + c0;
+      constexpr int first = (L == kW - 1) ? 0 : 1;
+#pragma unroll
+      for (int l = 0; l < L; ++l) {
+        if (l < first) {
+          r.ow[4 * l] = r.ow[4 * l + 1] = r.ow[4 * l + 2] = r.ow[4 * l + 3] = 0u;
+          continue;
+        }
+        const uint4 u = ld_stream(sp + (int64_t)l * p.D);
+        r.ow[4 * l] = u.x; r.ow[4 * l + 1] = u.y; r.ow[4 * l + 2] = u.z; r.ow[4 * l + 3] = u.w;
+      }
+    }
+  };
+
+  auto store_row = [&](int64_t n, const Row &r) {
+    uint16_t *outp = p.out + n * p.D + c0;
+    if (r.slot.s < 0) {  // padding row: zero output, state untouched
+      st_stream(outp, make_uint4(0u, 0u, 0u, 0u));
+      return;
+    }
+    uint4 outv;
+    if constexpr (!kPlanes) {
+      uint32_t nw[4 * L];
+      if constexpr (RING) {
+        outv = update8_compact_ring<L, ACT>(r.xw, r.ow, wv, bv, has_bias, r.slot.q, nw);
+      } else {
+        outv = update8_compact<L, ACT>(r.xw, r.ow, wv, bv, has_bias, nw);
+      }
+      uint16_t *sp = p.state + r.slot.s * (p.D * L) + c0 * L;
+#pragma unroll
+      for (int k = 0; k < L; ++k)
+        st_stream(sp + 8 * k, make_uint4(nw[4 * k], nw[4 * k + 1], nw[4 * k + 2], nw[4 * k + 3]));
+    } else {
+      uint16_t *sp = p.state + r.slot.s * (L * p.D) + c0;
+      // window planes: the ring's three, or the linear state's last three
+      constexpr int wp0 = RING ? 0 : L - (kW - 1);
+      uint32_t h[kW - 1][8], xs[8];
+#pragma unroll
+      for (int k = 0; k < kW - 1; ++k)
+        unpack8(make_uint4(r.ow[4 * (wp0 + k)], r.ow[4 * (wp0 + k) + 1], r.ow[4 * (wp0 + k) + 2],
+                           r.ow[4 * (wp0 + k) + 3]),
+                h[k]);
+      unpack8(make_uint4(r.xw[0], r.xw[1], r.xw[2], r.xw[3]), xs);
+      outv = outputs8_window<ACT>(h, xs, wv, bv, has_bias);
+      if constexpr (RING) {
+        st_stream(sp + (int64_t)r.slot.q * p.D, make_uint4(r.xw[0], r.xw[1], r.xw[2], r.xw[3]));
+      } else {
+        // plane l takes old plane l+1; the newest plane takes x
+#pragma unroll
+        for (int l = 0; l + 1 < L; ++l)
+          st_stream(sp + (int64_t)l * p.D, make_uint4(r.ow[4 * (l + 1)], r.ow[4 * (l + 1) + 1],
+                                                      r.ow[4 * (l + 1) + 2], r.ow[4 * (l + 1) + 3]));
+        st_stream(sp + (int64_t)(L - 1) * p.D, make_uint4(r.xw[0], r.xw[1], r.xw[2], r.xw[3]));
+      }
+    }
+    st_stream(outp, outv);
+  };
+
   const int64_t R = p.rows_per_cta;
   for (int64_t r0 = (int64_t)blockIdx.y * R; r0 < p.N; r0 += (int64_t)gridDim.y * R) {
     const int64_t r1 = r0 + R < p.N ? r0 + R : p.N;
-    for (int64_t n = r0; n < r1; ++n) {
-      const int64_t s = resolve_slot(p, n);
-      uint16_t *outp = p.out + n * p.D + c0;
-      if (s < 0) {  // padding row: zero output, state untouched
-        st_stream(outp, make_uint4(0u, 0u, 0u, 0u));
-        continue;
-      }
-
-      uint32_t xw[4];
-      {
-        const uint4 t = ld_stream(p.x + n * p.ld + c0);
-        xw[0] = t.x; xw[1] = t.y; xw[2] = t.z; xw[3] = t.w;
-      }
-
-      // Old state of the 8 channels. Channel-last with L > 3 never reads plane 0: it
-      // is outside the width-4 window and is overwritten by plane 1.
-      uint32_t ow[4 * L];
-      uint16_t *sp;
-      if constexpr (LAYOUT == (int)Layout::Compact) {
-        sp = p.state + s * (p.D * L) + c0 * L;
-#pragma unroll
-        for (int k = 0; k < L; ++k) {
-          const uint4 t = ld_stream(sp + 8 * k);
-          ow[4 * k] = t.x; ow[4 * k + 1] = t.y; ow[4 * k + 2] = t.z; ow[4 * k + 3] = t.w;
-        }
-      } else {
-        sp = p.state + s * (L * p.D) + c0;
-        constexpr int first = (L == kW - 1) ? 0 : 1;
-#pragma unroll
-        for (int l = 0; l < L; ++l) {
-          if (l < first) {
-            ow[4 * l] = ow[4 * l + 1] = ow[4 * l + 2] = ow[4 * l + 3] = 0u;
-            continue;
-          }
-          const uint4 t = ld_stream(sp + (int64_t)l * p.D);
-          ow[4 * l] = t.x; ow[4 * l + 1] = t.y; ow[4 * l + 2] = t.z; ow[4 * l + 3] = t.w;
-        }
-      }
-
-      uint32_t nw[4 * L];
-      uint4 outv;
-      if constexpr (LAYOUT == (int)Layout::Compact) {
-        outv = update8_compact<L, ACT>(xw, ow, wv, bv, has_bias, nw);
-#pragma unroll
-        for (int k = 0; k < L; ++k)
-          st_stream(sp + 8 * k, make_uint4(nw[4 * k], nw[4 * k + 1], nw[4 * k + 2], nw[4 * k + 3]));
-      } else {
-        // acc = sum_j history[L-3+j] * w[j] (j = 0..3, history[L] = x), then bias.
-        float y[8];
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          float acc = 0.0f;
-#pragma unroll
-          for (int j = 0; j < kW; ++j) {
-            const int hidx = L - (kW - 1) + j;
-            const uint32_t h = (hidx == L) ? get16(xw, c) : get16(ow, elem_pos<L, LAYOUT>(c, hidx));
-            acc = __fmaf_rn(bf16_bits(h), bf16_bits(get16(wv, c * kW + j)), acc);
-          }
-          if (has_bias) acc = acc + bf16_bits(get16(bv, c));
-          y[c] = activate<ACT>(acc);
-        }
-        outv = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
-                          pack_bf16x2(y[6], y[7]));
-        // New state: plane l takes old plane l+1; the newest plane takes x.
-#pragma unroll
-        for (int l = 0; l + 1 < L; ++l)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) nw[4 * l + i] = ow[4 * (l + 1) + i];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) nw[4 * (L - 1) + i] = xw[i];
-#pragma unroll
-        for (int l = 0; l < L; ++l)
-          st_stream(sp + (int64_t)l * p.D,
-                    make_uint4(nw[4 * l], nw[4 * l + 1], nw[4 * l + 2], nw[4 * l + 3]));
-      }
-      st_stream(outp, outv);
+    for (int64_t n = r0; n < r1; n += 2) {
+      Row a, b;
+      load_row(n, a);
+      if (n + 1 < r1) load_row(n + 1, b);
+      store_row(n, a);
+      if (n + 1 < r1) store_row(n + 1, b);
     }
   }
 }
 
 template <int L, int ACT>
 cudaError_t launch_L(const UpdateParams &p, dim3 grid, dim3 block, cudaStream_t stream) {
+  const bool ring = p.seqlens != nullptr;
   if (p.layout == (int)Layout::Compact) {
-    k_update_vector<L, ACT, (int)Layout::Compact><<<grid, block, 0, stream>>>(p);
+    if (ring) {
+      k_update_vector<L, ACT, (int)Layout::Compact, true><<<grid, block, 0, stream>>>(p);
+    } else {
+      k_update_vector<L, ACT, (int)Layout::Compact, false><<<grid, block, 0, stream>>>(p);
+    }
   } else {
-    k_update_vector<L, ACT, (int)Layout::ChannelLast><<<grid, block, 0, stream>>>(p);
+    if (ring) {
+      k_update_vector<L, ACT, (int)Layout::ChannelLast, true><<<grid, block, 0, stream>>>(p);
+    } else {
+      k_update_vector<L, ACT, (int)Layout::ChannelLast, false><<<grid, block, 0, stream>>>(p);
+    }
   }
   return cudaGetLastError();
 }

@@ -66,7 +66,7 @@ typedef struct CUstream_st *ccu_stream_t;
 typedef enum ccu_status {
   CCU_OK = 0,
   CCU_ERR_INVALID_ARGUMENT = 1, /* the arguments break the tensor contract */
-  CCU_ERR_NOT_IMPLEMENTED = 2,  /* valid, but not served (e.g. cache_seqlens != NULL) */
+  CCU_ERR_NOT_IMPLEMENTED = 2,  /* valid, but not served (e.g. a width W != 4) */
   CCU_ERR_CUDA = 3              /* a CUDA launch or runtime call failed */
 } ccu_status_t;
 
@@ -82,7 +82,7 @@ typedef enum ccu_route {
   CCU_ROUTE_VECTOR = 2, /* 8 channels per thread, 16-byte vectors; D % 8 == 0, L <= 8 */
   CCU_ROUTE_STAGED = 3, /* shared-memory staged tiles; D % 8 == 0, any L <= 256 */
   CCU_ROUTE_BULK = 4,   /* persistent CTAs, bulk async copies through shared memory;
-                           compact layout, D % 8 == 0, L <= 8 */
+                           D % 8 == 0, L <= 8, both layouts */
   CCU_ROUTE_COUNT = 5
 } ccu_route_t;
 
@@ -117,8 +117,16 @@ typedef enum ccu_route {
  *               ccu_conv1d_update_checked / ccu_conv1d_check_indices). A repeated slot
  *               gives an unspecified state for that slot; an out-of-range one is
  *               undefined behaviour. 4-byte aligned.
- *   cache_seqlens  reserved for a circular-buffer state; must be NULL (otherwise
- *               CCU_ERR_NOT_IMPLEMENTED, as on the page).
+ *   cache_seqlens  NULL for the linear state above, or int32 [N] (4-byte aligned) for a
+ *               ring-buffer state, the use the page reserves this keyword for (section on
+ *               cache_seqlens). Then conv_state[s, d, :] is a ring of L entries whose oldest
+ *               entry sits at q = cache_seqlens[n] mod L: the history is ring[q], ...,
+ *               ring[q+L-1] (mod L) followed by x, the output is computed from its last W
+ *               entries as above, and the call writes only ring[q] = x (one entry per
+ *               channel instead of L). cache_seqlens counts the inputs the row's slot has
+ *               received and is not modified; the caller advances it. Values must be >= 0
+ *               for non-padding rows (checked entry: a negative value is reported as
+ *               CCU_DEVERR_RANGE and the row treated as padding).
  *   N, D, S     rows, channels, cache slots. N == 0 or D == 0 is a no-op.
  *   L, W        state length and filter width, L >= W - 1. Served: W == 4, any L >= 3.
  *   out         BF16, contiguous [N, D], written for every row (+0 for padding rows).

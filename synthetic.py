@@ -47,6 +47,7 @@ class Workload:
     pad_frac: float = 0.0  # fraction of rows set to -1 (padding)
     layout: str = "compact"  # "compact" (D*L, L, 1) or "channel_last" (L*D, 1, D)
     seed: int = 0
+    ring: bool = False  # ring-buffer state: draw cache_seqlens [N]
 
     @property
     def has_bias(self) -> bool:
@@ -71,6 +72,19 @@ WORKLOADS = {
         Workload("large_n4096_d16384_l3_perm_pad5_silu", N=4096, D=16384, W=4, L=3, S=4096,
                  ld=16384, x_dist=("normal", 1.0), w_dist=("normal", 1.0), bias_std=0.1,
                  act="silu", indices="perm_pad", pad_frac=0.05),
+    ]
+}
+
+# Ring-buffer variants of the large-batch decode (conv_state used as a ring indexed by
+# cache_seqlens), in both state layouts. Measured beside the workloads above.
+RING_WORKLOADS = {
+    w.name: w
+    for w in [
+        dataclasses.replace(WORKLOADS["large_n4096_d16384_l3_perm_pad5_silu"],
+                            name="large_n4096_d16384_l3_perm_pad5_silu_ring", ring=True),
+        dataclasses.replace(WORKLOADS["large_n4096_d16384_l3_perm_pad5_silu"],
+                            name="large_n4096_d16384_l3_perm_pad5_silu_ring_chlast", ring=True,
+                            layout="channel_last"),
     ]
 }
 
@@ -159,10 +173,12 @@ class Inputs:
     conv_state: np.ndarray  # logical [S, D, L], compact
     bias: Optional[np.ndarray]  # [D] or None
     indices: Optional[np.ndarray]  # int32 [N] or None
+    cache_seqlens: Optional[np.ndarray] = None  # int32 [N] for a ring-buffer state, else None
 
 
 def generate(wl: Workload, seed: Optional[int] = None) -> Inputs:
-    """Draw one workload's inputs from its seed (x, weight, conv_state, bias, indices)."""
+    """Draw one workload's inputs from its seed (x, weight, conv_state, bias, indices, and
+    for a ring-buffer state cache_seqlens: counts uniform in [0, 2^20))."""
     rng = np.random.Generator(np.random.PCG64(wl.seed if seed is None else seed))
     N, D, W, L, S, ld = wl.N, wl.D, wl.W, wl.L, wl.S, wl.ld
     x = np.full((N, ld), BF16_NAN_BITS, dtype=np.uint16)
@@ -171,7 +187,8 @@ def generate(wl: Workload, seed: Optional[int] = None) -> Inputs:
     conv_state = _draw(rng, wl.x_dist, S * D * L).reshape(S, D, L)
     bias = _draw(rng, ("normal", wl.bias_std), D) if wl.has_bias else None
     indices = make_indices(rng, wl.indices, N, S, wl.pad_frac)
-    return Inputs(wl, x, weight, conv_state, bias, indices)
+    seqlens = rng.integers(0, 1 << 20, size=N).astype(np.int32) if wl.ring else None
+    return Inputs(wl, x, weight, conv_state, bias, indices, seqlens)
 
 
 def variant(base: Workload, **changes) -> Workload:
@@ -184,15 +201,22 @@ def algorithmic_bytes(wl: Workload, indices: Optional[np.ndarray]) -> int:
 
     Active row element: 2 B x read + 2L B state read + 2L B state write + 2 B out
     write. Padding row element: 2 B out write. Plus weight (2*D*W B), bias (2*D B)
-    and indices (4*N B), each read once.
+    and indices (4*N B), each read once. A ring-buffer state needs only the W-1 window
+    entries read and one entry written: 2 + 2(W-1) + 2 + 2 B per active element, plus
+    cache_seqlens (4*N B).
     """
     n_pad = 0 if indices is None else int(np.count_nonzero(indices == -1))
     active = wl.N - n_pad
-    per_active = 2 + 2 * wl.L + 2 * wl.L + 2
+    if wl.ring:
+        per_active = 2 + 2 * (wl.W - 1) + 2 + 2
+    else:
+        per_active = 2 + 2 * wl.L + 2 * wl.L + 2
     total = active * wl.D * per_active + n_pad * wl.D * 2
     total += 2 * wl.D * wl.W
     if wl.has_bias:
         total += 2 * wl.D
     if indices is not None:
+        total += 4 * wl.N
+    if wl.ring:
         total += 4 * wl.N
     return total

@@ -48,7 +48,7 @@ def guarded_u16(a: np.ndarray, dev):
 
 
 def run_gpu(inp: synthetic.Inputs, layout="compact", route="auto", checked=False, dev="cuda:0",
-            stream=None, guards=True):
+            stream=None, guards=True, cache_seqlens=None):
     """One update on the GPU through the torch binding (which calls the C-ABI).
 
     Returns (out, logical state [S, D, L], status or None, guards_ok).
@@ -66,13 +66,14 @@ def run_gpu(inp: synthetic.Inputs, layout="compact", route="auto", checked=False
     w = to_dev_u16(inp.weight, dev)
     b = to_dev_u16(inp.bias, dev) if inp.bias is not None else None
     idx = torch.from_numpy(inp.indices).to(dev) if inp.indices is not None else None
+    seq = torch.from_numpy(np.ascontiguousarray(cache_seqlens, np.int32)).to(dev) if cache_seqlens is not None else None
     go = Guarded(N * D * 2, dev)
     out = go.view(torch.bfloat16, (N, D))
     status = torch.zeros((1,), dtype=torch.int32, device=dev) if checked else None
     ctx = torch.cuda.stream(stream) if stream is not None else torch.cuda.stream(torch.cuda.current_stream())
     with ctx:
-        ccu.causal_conv1d_update(x, st, w, b, wl.act, conv_state_indices=idx, out=out, route=route,
-                                 status=status)
+        ccu.causal_conv1d_update(x, st, w, b, wl.act, conv_state_indices=idx, cache_seqlens=seq,
+                                 out=out, route=route, status=status)
     torch.cuda.synchronize()
     got_out = from_dev_u16(out)
     mem = from_dev_u16(gs.view(torch.int16, state_mem.shape))
@@ -97,5 +98,17 @@ def assert_parity(inp, got_out, got_state, want_out, want_state, what=""):
                              f"(n={n}, d={d}) got {got_out[n, d]:#06x} want {want_out[n, d]:#06x}")
 
 
-def oracle_ref(inp, layout="compact"):
-    return oracle.run_workload(inp, layout)
+def oracle_ref(inp, layout="compact", cache_seqlens=None):
+    return oracle.run_workload(inp, layout, cache_seqlens=cache_seqlens)
+
+
+def ring_seqlens(rng, inp):
+    """Seeded cache_seqlens for a workload: 0, small, multiples of L and large values;
+    padding rows get -1 (never read for them)."""
+    N, L = inp.wl.N, inp.wl.L
+    seq = rng.integers(0, 10 * L + 7, size=N).astype(np.int32)
+    seq[::5] = 0
+    seq[1::7] = 2_000_000_000  # large counts: only the value mod L matters
+    if inp.indices is not None:
+        seq[inp.indices == -1] = -1
+    return seq

@@ -95,7 +95,7 @@ def select(ccu, route=0, **kw):
 
 
 DECLINES = [
-    ("cache_seqlens", dict(cache_seqlens=0x700000), 2, "cache_seqlens"),
+    ("misaligned cache_seqlens", dict(cache_seqlens=0x700002), 1, "cache_seqlens must be 4-byte"),
     ("width 3", dict(W=3, L=3), 2, "W == 4"),
     ("width 2", dict(W=2, L=1), 2, "W == 4"),
     ("L < W-1", dict(L=2), 1, "L must be >= W - 1"),
@@ -146,6 +146,11 @@ def test_noop_sizes(ccu):
     assert select(ccu, D=0, x=None, weight=None) == (0, 0)
 
 
+def test_ring_buffer_state_is_served(ccu):
+    assert select(ccu, cache_seqlens=0x700000) == (0, 2)
+    assert select(ccu, cache_seqlens=0x700000, N=4096, D=16384, S=4096) == (0, 4)
+
+
 def test_indices_allow_S_below_N(ccu):
     st, r = select(ccu, S=2, indices=IDX)
     assert st == 0 and r == 2
@@ -180,7 +185,8 @@ def test_forced_routes(ccu):
     assert select(ccu, route=2) == (0, 2)
     assert select(ccu, route=3) == (0, 3)
     assert select(ccu, route=4) == (0, 4)
-    assert select(ccu, route=4, stride_s=192, stride_d=1, stride_l=64)[0] == 2  # bulk: compact only
+    assert select(ccu, route=4, stride_s=192, stride_d=1, stride_l=64) == (0, 4)  # both layouts
+    assert select(ccu, route=4, L=9)[0] == 2  # bulk kernels are compiled for L <= 8
     assert select(ccu, route=2, D=63)[0] == 2  # vector needs D % 8 == 0
     assert select(ccu, route=2, L=9)[0] == 2   # vector is compiled for L <= 8
     assert select(ccu, route=7)[0] == 1        # unknown route

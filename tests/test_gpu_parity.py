@@ -15,7 +15,8 @@ import torch
 
 import oracle
 import synthetic
-from gpu_util import Guarded, assert_parity, from_dev_u16, oracle_ref, run_gpu, to_dev_u16
+from gpu_util import (Guarded, assert_parity, from_dev_u16, oracle_ref, ring_seqlens, run_gpu,
+                      to_dev_u16)
 
 pytestmark = pytest.mark.gpu
 
@@ -85,8 +86,6 @@ def test_routes(route, layout, i):
     wl = _small(i)
     if route in ("vector", "bulk") and wl.L > 8:
         pytest.skip("vector and bulk kernels are compiled for L <= 8")
-    if route == "bulk" and layout != "compact":
-        pytest.skip("the bulk kernel serves the compact layout")
     inp = synthetic.generate(wl, seed=100 + i)
     _check(inp, layout=layout, route=route, what=f"{wl} {route} {layout}")
 
@@ -318,14 +317,15 @@ def test_checked_path_clean_inputs_report_nothing():
     assert_parity(inp, got_out, got_state, want_out, want_state, "checked clean")
 
 
+@pytest.mark.parametrize("layout", ["compact", "channel_last"])
 @pytest.mark.parametrize("route", ["vector", "bulk"])
-def test_large_batch_routes_agree_bitwise(route):
+def test_large_batch_routes_agree_bitwise(route, layout):
     """The two large-batch kernel families give bit-identical results on a multi-tile case
     with a ragged last chunk (D = 3*2048 + 264) and padding rows."""
     wl = synthetic.variant(synthetic.WORKLOADS[synthetic.BENCH_WORKLOAD], name="ragged", N=300, S=300,
                            D=6408, ld=6408)
     inp = synthetic.generate(wl, seed=21)
-    _check(inp, route=route, what=f"ragged {route}")
+    _check(inp, layout=layout, route=route, what=f"ragged {route} {layout}")
 
 
 def test_no_device_error_raised():
@@ -375,8 +375,8 @@ def test_typed_declines_through_binding():
     st = torch.randn((4, 64, 3), device=DEV).to(torch.bfloat16)
     w = torch.randn((64, 4), device=DEV).to(torch.bfloat16)
     seq = torch.zeros((4,), dtype=torch.int32, device=DEV)
-    with pytest.raises(NotImplementedError, match="cache_seqlens"):
-        ccu.causal_conv1d_update(x, st, w, cache_seqlens=seq)
+    with pytest.raises(ValueError, match="cache_seqlens"):
+        ccu.causal_conv1d_update(x, st, w, cache_seqlens=seq[:3])
     with pytest.raises(NotImplementedError, match="3D x"):
         ccu.causal_conv1d_update(x.view(4, 64, 1), st, w)
     with pytest.raises(NotImplementedError, match="W == 4"):
@@ -425,3 +425,81 @@ def test_host_resident_x_and_out():
     got_out = h_out.numpy().view(np.uint16)
     got_state = from_dev_u16(st)
     assert_parity(inp, got_out, got_state, want_out, want_state, "host x/out")
+
+
+# ----------------------------------------------------------------------------- ring-buffer state
+
+def _check_ring(inp, seq, layout="compact", route="auto", what=""):
+    want_out, want_state = oracle_ref(inp, layout, cache_seqlens=seq)
+    got_out, got_state, _, ok = run_gpu(inp, layout, route, cache_seqlens=seq)
+    assert ok, f"{what}: a guard band was overwritten"
+    assert_parity(inp, got_out, got_state, want_out, want_state, what)
+
+
+@pytest.mark.parametrize("route", ["scalar", "vector", "staged", "bulk"])
+@pytest.mark.parametrize("layout", ["compact", "channel_last"])
+@pytest.mark.parametrize("i", range(len(SMALL)))
+def test_ring_routes(route, layout, i):
+    wl = _small(i)
+    if route in ("vector", "bulk") and wl.L > 8:
+        pytest.skip("vector and bulk kernels are compiled for L <= 8")
+    inp = synthetic.generate(wl, seed=200 + i)
+    seq = ring_seqlens(np.random.default_rng(i), inp)
+    _check_ring(inp, seq, layout, route, what=f"ring {wl} {route} {layout}")
+
+
+@pytest.mark.parametrize("layout", ["compact", "channel_last"])
+def test_ring_large_batch_full_size(layout):
+    inp = synthetic.generate(synthetic.WORKLOADS[synthetic.BENCH_WORKLOAD])
+    seq = ring_seqlens(np.random.default_rng(7), inp)
+    _check_ring(inp, seq, layout, what=f"ring large {layout}")
+
+
+@pytest.mark.parametrize("L,layout,route", [(3, "compact", "bulk"), (3, "channel_last", "vector"),
+                                            (5, "compact", "vector"), (12, "channel_last", "staged"),
+                                            (9, "compact", "scalar")])
+def test_ring_chain_equals_full_convolution(L, layout, route):
+    """T GPU updates of a ring fed with cache_seqlens 0..T-1 equal one full convolution."""
+    import depthwise_causal_conv1d_gb300 as ccu
+
+    rng = np.random.default_rng(100 + L)
+    T, D = 13, 1032
+    x_seq = synthetic.f64_to_bf16_bits(rng.standard_normal((T, D)))
+    weight = synthetic.f64_to_bf16_bits(rng.standard_normal((D, 4)) * 0.5)
+    bias = synthetic.f64_to_bf16_bits(rng.standard_normal(D) * 0.1)
+    want_y, want_state = oracle.full_causal_conv(x_seq, weight, bias, "silu", None, L)
+    w, b = to_dev_u16(weight, DEV), to_dev_u16(bias, DEV)
+    if layout == "compact":
+        st = torch.zeros((1, D, L), dtype=torch.bfloat16, device=DEV)
+    else:
+        st = torch.zeros((1, L, D), dtype=torch.bfloat16, device=DEV).permute(0, 2, 1)
+    ys = []
+    for t in range(T):
+        xt = to_dev_u16(x_seq[t:t + 1], DEV)
+        seq = torch.tensor([t], dtype=torch.int32, device=DEV)
+        ys.append(from_dev_u16(ccu.causal_conv1d_update(xt, st, w, b, "silu", cache_seqlens=seq,
+                                                        route=route)))
+    from oracle_pins import _rotate, bf16_ulp_distance
+
+    got_ring = from_dev_u16(st.contiguous())[0]
+    assert np.array_equal(_rotate(got_ring, T % L), want_state)
+    assert bf16_ulp_distance(np.concatenate(ys), want_y).max() <= 1
+
+
+@pytest.mark.parametrize("route", ["scalar", "vector", "staged", "bulk"])
+def test_ring_checked_negative_seqlens(route):
+    wl = synthetic.variant(synthetic.WORKLOADS["paged_n256_d8192_l3_s1024_pad10_silu"], name="ringchk",
+                           N=12, D=1024, S=16, indices="distinct_pad", pad_frac=0.2)
+    inp = synthetic.generate(wl, seed=9)
+    seq = ring_seqlens(np.random.default_rng(3), inp)
+    active = np.flatnonzero(inp.indices >= 0)
+    bad = active[:2]
+    seq[bad] = -3
+    ref_idx = inp.indices.copy()
+    ref_idx[bad] = -1  # the oracle's view: those rows behave as padding
+    ref_seq = seq.copy()
+    ref_seq[bad] = 0
+    want_out, want_state = oracle_ref(dataclasses.replace(inp, indices=ref_idx), cache_seqlens=ref_seq)
+    got_out, got_state, status, ok = run_gpu(inp, route=route, checked=True, cache_seqlens=seq)
+    assert ok and status & 1
+    assert_parity(inp, got_out, got_state, want_out, want_state, "ring checked")
