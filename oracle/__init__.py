@@ -60,6 +60,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.ccu_oracle_conv1d_update_circular.argtypes = [
         _u16p, _i64, _u16p, _i64, _i64, _i64, _u16p, _u16p, ctypes.c_int, _i32p, _i32p,
         _i64, _i64, _i64, _i64, _i64, _u16p, _f32p]
+    lib.ccu_oracle_conv1d_update_multi.restype = ctypes.c_int
+    lib.ccu_oracle_conv1d_update_multi.argtypes = [
+        _u16p, _i64, _i64, _i64, _u16p, _i64, _i64, _i64, _u16p, _u16p, ctypes.c_int, _i32p, _i32p,
+        _i64, _i64, _i64, _i64, _i64, _i64, _u16p, _i64, _i64, _i64, _u16p]
     lib.ccu_oracle_full_causal_conv.restype = ctypes.c_int
     lib.ccu_oracle_full_causal_conv.argtypes = [
         _u16p, _i64, _i64, _u16p, _u16p, ctypes.c_int, _i64, _u16p, _i64, _u16p, _u16p, _f32p]
@@ -146,6 +150,33 @@ def conv1d_update_circular(x: np.ndarray, ld: int, conv_state: np.ndarray, strid
     if rc != OK:
         raise ValueError(f"oracle refused the inputs (code {rc})")
     return (out, acc) if with_acc else out
+
+
+def conv1d_update_multi(x: np.ndarray, x_strides, conv_state: np.ndarray, strides, weight: np.ndarray,
+                        bias: Optional[np.ndarray], act: str, indices: Optional[np.ndarray],
+                        cache_seqlens: Optional[np.ndarray], N: int, D: int, T: int, S: int, L: int,
+                        W: int, *, with_inter: bool = False, lib: Optional[ctypes.CDLL] = None):
+    """T tokens per row in one call; returns out [N, D, T] (and intermediate states
+    [N, T, D, L] when ``with_inter``). ``x`` is flat memory addressed with ``x_strides``
+    (element strides of n, d, t)."""
+    lib = lib or load()
+    for a in (x, conv_state, weight):
+        assert a.dtype == np.uint16 and a.flags["C_CONTIGUOUS"]
+    if indices is not None:
+        indices = np.ascontiguousarray(indices, dtype=np.int32)
+    if cache_seqlens is not None:
+        cache_seqlens = np.ascontiguousarray(cache_seqlens, dtype=np.int32)
+    out = np.empty((N, D, T), dtype=np.uint16)
+    inter = np.zeros((N, T, D, L), dtype=np.uint16) if with_inter else None
+    rc = lib.ccu_oracle_conv1d_update_multi(
+        _ptr(x, ctypes.c_uint16), x_strides[0], x_strides[1], x_strides[2],
+        _ptr(conv_state, ctypes.c_uint16), strides[0], strides[1], strides[2],
+        _ptr(weight, ctypes.c_uint16), _ptr(bias, ctypes.c_uint16), ACT[act],
+        _ptr(indices, ctypes.c_int32), _ptr(cache_seqlens, ctypes.c_int32), N, D, T, S, L, W,
+        _ptr(out, ctypes.c_uint16), D * T, T, 1, _ptr(inter, ctypes.c_uint16))
+    if rc != OK:
+        raise ValueError(f"oracle refused the inputs (code {rc})")
+    return (out, inter) if with_inter else out
 
 
 def full_causal_conv(x_seq: np.ndarray, weight: np.ndarray, bias: Optional[np.ndarray], act: str,

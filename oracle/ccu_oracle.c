@@ -30,7 +30,10 @@
  *     keyword says only that a future version may use it so): the slot is a ring of L
  *     entries, p = cache_seqlens[n] mod L indexes its oldest entry, the history is the
  *     ring read from p onward followed by x, and the step overwrites only that oldest
- *     entry with x. Read this way, a ring read from p is exactly the linear state.
+ *     entry with x. Read this way, a ring read from p is exactly the linear state;
+ *   - the multi-token update x[N, D, T] the page says may come later: the T tokens are
+ *     appended to the history in order, output t is computed from the window ending at
+ *     token t, and the new state is the last L entries (T single steps in one call).
  *
  * Build: gcc -O2 -ffp-contract=off -fPIC -shared (no fast-math, no FMA contraction).
  */
@@ -210,6 +213,95 @@ int ccu_oracle_conv1d_update_circular(const uint16_t *x, int64_t ld, uint16_t *c
 
       /* the new input replaces the oldest entry; the others stay where they are */
       ring[p * stride_l] = history[L];
+    }
+  }
+  free(history);
+  return CCU_ORACLE_OK;
+}
+
+int ccu_oracle_conv1d_update_multi(const uint16_t *x, int64_t sxn, int64_t sxd, int64_t sxt,
+                                   uint16_t *conv_state, int64_t stride_s, int64_t stride_d,
+                                   int64_t stride_l, const uint16_t *weight, const uint16_t *bias,
+                                   int act, const int32_t *indices, const int32_t *cache_seqlens,
+                                   int64_t N, int64_t D, int64_t T, int64_t S, int64_t L, int64_t W,
+                                   uint16_t *out, int64_t son, int64_t sod, int64_t sot,
+                                   uint16_t *inter) {
+  if (N < 0 || D < 0 || T < 0 || S < 0 || W < 1 || L < W - 1 || L < 1) return CCU_ORACLE_BAD_ARGS;
+  if (act != CCU_ORACLE_ACT_IDENTITY && act != CCU_ORACLE_ACT_SILU) return CCU_ORACLE_BAD_ARGS;
+  if (N == 0 || D == 0 || T == 0) return CCU_ORACLE_OK;
+  if (x == NULL || conv_state == NULL || weight == NULL || out == NULL) return CCU_ORACLE_BAD_ARGS;
+  if (indices == NULL && S < N) return CCU_ORACLE_BAD_ARGS;
+  if (indices != NULL) {
+    int flags = ccu_oracle_check_indices(indices, N, S);
+    if (flags < 0) return flags;
+    if (flags != 0) return CCU_ORACLE_BAD_INDICES;
+  }
+  if (cache_seqlens != NULL) {
+    for (int64_t n = 0; n < N; ++n) {
+      int64_t s = indices ? (int64_t)indices[n] : n;
+      if (s != -1 && cache_seqlens[n] < 0) return CCU_ORACLE_BAD_ARGS;
+    }
+  }
+
+  /* the state entries in time order (oldest first), then the T tokens */
+  uint16_t *history = (uint16_t *)malloc((size_t)(L + T) * sizeof(uint16_t));
+  if (history == NULL) return CCU_ORACLE_NO_MEMORY;
+
+  for (int64_t n = 0; n < N; ++n) {
+    int64_t s = indices ? (int64_t)indices[n] : n;
+    if (s == -1) {
+      for (int64_t d = 0; d < D; ++d)
+        for (int64_t t = 0; t < T; ++t) out[n * son + d * sod + t * sot] = 0x0000u;
+      continue;
+    }
+    const int64_t q = cache_seqlens ? (int64_t)cache_seqlens[n] % L : 0;
+    for (int64_t d = 0; d < D; ++d) {
+      uint16_t *st = conv_state + s * stride_s + d * stride_d;
+      for (int64_t i = 0; i < L; ++i) {
+        /* linear state: entry i; ring: the ring read from its oldest entry q */
+        int64_t pos = cache_seqlens ? (q + i) % L : i;
+        history[i] = st[pos * stride_l];
+      }
+      for (int64_t t = 0; t < T; ++t) history[L + t] = x[n * sxn + d * sxd + t * sxt];
+
+      for (int64_t t = 0; t < T; ++t) {
+        /* token t is history[L + t]; its window is history[L + t + 1 - W .. L + t] */
+        float acc = 0.0f;
+        for (int64_t j = 0; j < W; ++j) {
+          float h = ccu_oracle_bf16_to_f32(history[L + t + 1 - W + j]);
+          float w = ccu_oracle_bf16_to_f32(weight[d * W + j]);
+          float term = h * w;
+          acc = acc + term;
+        }
+        if (bias != NULL) acc = acc + ccu_oracle_bf16_to_f32(bias[d]);
+        out[n * son + d * sod + t * sot] = ccu_oracle_f32_to_bf16(activation(acc, act));
+
+        if (inter != NULL) {
+          /* the state after token t, in the state's own order */
+          uint16_t *it = inter + ((n * T + t) * D + d) * L;
+          for (int64_t l = 0; l < L; ++l) {
+            if (cache_seqlens) {
+              /* ring after t+1 writes: position (q + k) mod L holds token k for the last
+               * writes, so read the time-ordered history back into ring positions */
+              int64_t age = (l - (q + t + 1)) % L; /* 0 = oldest entry after token t */
+              if (age < 0) age += L;
+              it[l] = history[t + 1 + age];
+            } else {
+              it[l] = history[t + 1 + l];
+            }
+          }
+        }
+      }
+
+      /* the new state: the last L history entries, in the state's own order */
+      for (int64_t i = 0; i < L; ++i) {
+        if (cache_seqlens) {
+          int64_t pos = (q + T + i) % L; /* after T writes the oldest entry sits at q + T */
+          st[pos * stride_l] = history[T + i];
+        } else {
+          st[i * stride_l] = history[T + i];
+        }
+      }
     }
   }
   free(history);

@@ -66,6 +66,26 @@ int ccu_oracle_conv1d_update_circular(const uint16_t *x, int64_t ld, uint16_t *c
                                       int64_t N, int64_t D, int64_t S, int64_t L, int64_t W,
                                       uint16_t *out, float *acc_out);
 
+/* T tokens per row in one call: the multi-token form of the update, x[N, D, T].
+ * history = concat(state entries, x[n, d, 0], ..., x[n, d, T-1]); output t is computed
+ * from the W history entries ending at token t; the new state is the last L entries of
+ * the history. With cache_seqlens (ring-buffer state), token t is written over ring
+ * position (cache_seqlens[n] + t) mod L, each token seeing the ring as it stands.
+ *   x        element (n, d, t) at x[n*sxn + d*sxd + t*sxt]
+ *   out      element (n, d, t) at out[n*son + d*sod + t*sot]
+ *   inter    NULL, or [N, T, D, L] compact: inter[((n*T + t)*D + d)*L + l] is entry l of
+ *            the state (in the state's own order, linear or ring) after token t; padding
+ *            rows leave their entries untouched
+ * Other arguments as ccu_oracle_conv1d_update / ccu_oracle_conv1d_update_circular
+ * (cache_seqlens NULL for the linear state). */
+int ccu_oracle_conv1d_update_multi(const uint16_t *x, int64_t sxn, int64_t sxd, int64_t sxt,
+                                   uint16_t *conv_state, int64_t stride_s, int64_t stride_d,
+                                   int64_t stride_l, const uint16_t *weight, const uint16_t *bias,
+                                   int act, const int32_t *indices, const int32_t *cache_seqlens,
+                                   int64_t N, int64_t D, int64_t T, int64_t S, int64_t L, int64_t W,
+                                   uint16_t *out, int64_t son, int64_t sod, int64_t sot,
+                                   uint16_t *inter);
+
 /* Full-sequence causal depthwise convolution over T steps, written directly
  * from the convolution sum (no state shifting):
  *   y[t, d] = act( sum_{j=0}^{W-1} w[d, j] * xx(t - (W-1) + j, d) + b[d] )

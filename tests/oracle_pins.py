@@ -368,8 +368,77 @@ def pin_circular_chain_vs_full(lib):
         assert np.array_equal(_rotate(ring[0], T % L), fin), f"ring after T steps (L={L})"
 
 
+def _multi_case(rng, N, D, T, L, S, ring, pad):
+    x = rand_bf16(rng, (N, T, D))  # token-major memory: x[n, d, t] at n*T*D + t*D + d
+    weight = rand_bf16(rng, (D, 4), 0.5)
+    bias = rand_bf16(rng, (D,), 0.1)
+    state = rand_bf16(rng, (S, D, L))
+    idx = rng.permutation(S)[:N].astype(np.int32)
+    if pad:
+        idx[::3] = -1
+    seq = rng.integers(0, 5 * L, size=N).astype(np.int32) if ring else None
+    return x, weight, bias, state, idx, seq
+
+
+def pin_multi_equals_sequential_steps(lib):
+    # One call with T tokens equals T single-token updates, token by token: outputs,
+    # final state and the state after every token.
+    rng = np.random.default_rng(13)
+    for L, T, ring in [(3, 1, False), (3, 4, False), (4, 2, True), (6, 5, False), (3, 7, True),
+                       (5, 3, True)]:
+        N, D, S, W = 5, 10, 8, 4
+        x, weight, bias, state, idx, seq = _multi_case(rng, N, D, T, L, S, ring, pad=True)
+        st_multi = state.copy()
+        out, inter = oracle.conv1d_update_multi(x, (T * D, 1, D), st_multi, (D * L, L, 1), weight, bias,
+                                                "silu", idx, seq, N, D, T, S, L, W, with_inter=True,
+                                                lib=lib)
+        st_seq = state.copy()
+        for t in range(T):
+            xt = np.ascontiguousarray(x[:, t, :])
+            if ring:
+                o = oracle.conv1d_update_circular(xt, D, st_seq, (D * L, L, 1), weight, bias, "silu", idx,
+                                                  seq + t, N, D, S, L, W, lib=lib)
+            else:
+                o = oracle.conv1d_update(xt, D, st_seq, (D * L, L, 1), weight, bias, "silu", idx,
+                                         N, D, S, L, W, lib=lib)
+            assert np.array_equal(out[:, :, t], o), f"token {t} output (L={L}, T={T}, ring={ring})"
+            for n, s in enumerate(idx):
+                if s >= 0:
+                    assert np.array_equal(inter[n, t], st_seq[s]), f"state after token {t}"
+        assert np.array_equal(st_multi, st_seq), f"final state (L={L}, T={T}, ring={ring})"
+
+
+def pin_multi_x_layouts(lib):
+    rng = np.random.default_rng(14)
+    N, D, T, L, S, W = 4, 9, 3, 4, 4, 4
+    x, weight, bias, state, idx, _ = _multi_case(rng, N, D, T, L, S, False, pad=False)
+    st_a = state.copy()
+    out_a = oracle.conv1d_update_multi(x, (T * D, 1, D), st_a, (D * L, L, 1), weight, bias, "identity",
+                                       idx, None, N, D, T, S, L, W, lib=lib)
+    x_dt = np.ascontiguousarray(np.transpose(x, (0, 2, 1)))  # [N, D, T] memory
+    st_b = state.copy()
+    out_b = oracle.conv1d_update_multi(x_dt, (D * T, T, 1), st_b, (D * L, L, 1), weight, bias,
+                                       "identity", idx, None, N, D, T, S, L, W, lib=lib)
+    assert np.array_equal(out_a, out_b) and np.array_equal(st_a, st_b)
+
+
+def pin_multi_vs_full(lib):
+    rng = np.random.default_rng(15)
+    D, T, L, W = 7, 9, 3, 4
+    x_seq = rand_bf16(rng, (T, D))
+    weight = rand_bf16(rng, (D, W))
+    init = rand_bf16(rng, (D, L))
+    st = init.reshape(1, D, L).copy()
+    out = oracle.conv1d_update_multi(np.ascontiguousarray(x_seq.reshape(1, T, D)), (T * D, 1, D), st,
+                                     (D * L, L, 1), weight, None, "identity", None, None, 1, D, T, 1,
+                                     L, W, lib=lib)
+    y, fin = oracle.full_causal_conv(x_seq, weight, None, "identity", init, L, lib=lib)
+    assert np.array_equal(out[0].T, y) and np.array_equal(st[0], fin)
+
+
 ALL_PINS = [pin_golden, pin_bf16_conversion, pin_silu, pin_one_hot, pin_chain_vs_full,
             pin_full_vs_convolve, pin_closed_form, pin_padding_and_untouched, pin_routing,
             pin_layouts, pin_padded_ld, pin_check_indices,
             pin_circular_equals_linear_through_rotation, pin_circular_writes_one_entry,
-            pin_circular_chain_vs_full]
+            pin_circular_chain_vs_full, pin_multi_equals_sequential_steps, pin_multi_x_layouts,
+            pin_multi_vs_full]

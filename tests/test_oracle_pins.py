@@ -95,6 +95,18 @@ MUTATIONS += [
 ]
 
 
+# Mistakes in the multi-token function.
+MUTATIONS += [
+    ("multi: token window off by one", "float h = ccu_oracle_bf16_to_f32(history[L + t + 1 - W + j]);",
+     "float h = ccu_oracle_bf16_to_f32(history[L + t - W + j]);"),
+    ("multi: final state not advanced", "st[i * stride_l] = history[T + i];",
+     "st[i * stride_l] = history[i];"),
+    ("multi: intermediate state one token late", "it[l] = history[t + 1 + l];",
+     "it[l] = history[t + 2 + l < L + T ? t + 2 + l : L + T - 1];"),
+    ("multi: ring final position", "int64_t pos = (q + T + i) % L;", "int64_t pos = (q + i) % L;"),
+]
+
+
 def _replace_nth(src, old, new, nth):
     at = -1
     for _ in range(nth):
