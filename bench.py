@@ -517,6 +517,61 @@ def per_workload_table(dev, stream, reps=50):
     return rows
 
 
+def multi_token_rows(dev, stream, reps=50):
+    """µs per call of the multi-token update, and of the same tokens as T single calls."""
+    import torch
+
+    import depthwise_causal_conv1d_gb300 as ccu
+
+    rows = {}
+    for name, wl in synthetic.MULTI_WORKLOADS.items():
+        inp = synthetic.generate(wl)
+        N, D, T, L = wl.N, wl.D, wl.T, wl.L
+        x = to_dev(inp.x, dev)  # [N, T, D] memory
+        st = to_dev(inp.conv_state, dev)
+        w, b = to_dev(inp.weight, dev), to_dev(inp.bias, dev)
+        idx = torch.from_numpy(inp.indices).to(dev)
+        out = torch.empty((N, T, D), dtype=torch.bfloat16, device=dev)
+        out1 = torch.empty((N, D), dtype=torch.bfloat16, device=dev)  # one token's output
+        act = ccu.CCU_ACT_SILU if wl.act == "silu" else ccu.CCU_ACT_IDENTITY
+
+        def multi():
+            stat = ccu.lib.ccu_conv1d_update_multi(
+                x.data_ptr(), T * D, 1, D, st.data_ptr(), D * L, L, 1, w.data_ptr(), b.data_ptr(), act,
+                idx.data_ptr(), None, N, D, T, wl.S, L, wl.W, out.data_ptr(), T * D, 1, D, None, None,
+                0, stream.cuda_stream)
+            if stat != 0:
+                ccu.raise_for_status(stat)
+
+        def singles():
+            for t in range(T):
+                stat = ccu.lib.ccu_conv1d_update(
+                    x[:, t].data_ptr(), T * D, st.data_ptr(), D * L, L, 1, w.data_ptr(), b.data_ptr(),
+                    act, idx.data_ptr(), None, N, D, wl.S, L, wl.W, out1.data_ptr(),
+                    stream.cuda_stream)
+                if stat != 0:
+                    ccu.raise_for_status(stat)
+
+        res = {}
+        for label, fn in (("multi", multi), ("singles", singles)):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                fn()
+            e.record(stream)
+            torch.cuda.synchronize()
+            res[label] = a.elapsed_time(e) * 1e3 / reps
+        nbytes = synthetic.algorithmic_bytes(wl, inp.indices)
+        rows[name] = {"N_x_D": N * D, "T": T, "bytes": nbytes, "us_per_call": round(res["multi"], 3),
+                      "GBps": round(nbytes / (res["multi"] * 1e-6) / 1e9, 1),
+                      "frac": round(nbytes / (res["multi"] * 1e-6) / 1e9 / PEAK_GBPS, 4),
+                      "same_tokens_as_T_single_calls_us": round(res["singles"], 3)}
+    return rows
+
+
 def cpu_baseline_sample(inp, target_s: float):
     """Time the single-threaded C oracle on a bounded sample of the workload's rows."""
     import oracle
@@ -618,6 +673,7 @@ def run_ours(args):
         line["clocks"] = sampler.summary(w0, w1)
         if rank == 0 and world == 1:
             line["per_workload"] = per_workload_table(dev, stream)
+            line["multi_token"] = multi_token_rows(dev, stream)
         if rank == 0:
             line["cpu_baseline"] = cpu_baseline_sample(inp, args.cpu_seconds)
     if rank == 0:

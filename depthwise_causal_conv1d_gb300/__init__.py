@@ -59,6 +59,10 @@ def _load() -> ctypes.CDLL:
     lib.ccu_conv1d_update_checked.argtypes = upd + [vp, vp]
     lib.ccu_conv1d_update_ex.argtypes = upd + [vp, i32, vp]
     lib.ccu_conv1d_select_route.argtypes = upd + [i32, ctypes.POINTER(i32)]
+    lib.ccu_conv1d_update_multi.argtypes = [vp, i64, i64, i64, vp, i64, i64, i64, vp, vp, ctypes.c_int,
+                                            vp, vp, i64, i64, i64, i64, i64, i64, vp, i64, i64, i64,
+                                            vp, vp, i32, vp]
+    lib.ccu_conv1d_update_multi.restype = ctypes.c_int
     for f in ("ccu_conv1d_update", "ccu_conv1d_update_checked", "ccu_conv1d_update_ex",
               "ccu_conv1d_select_route", "ccu_conv1d_check_indices"):
         getattr(lib, f).restype = ctypes.c_int
@@ -103,6 +107,16 @@ def ccu_conv1d_update_ex(x, ld, conv_state, stride_s, stride_d, stride_l, weight
     return lib.ccu_conv1d_update_ex(x, ld, conv_state, stride_s, stride_d, stride_l, weight, bias,
                                     act, indices, cache_seqlens, N, D, S, L, W, out, status_dev,
                                     route, stream)
+
+
+def ccu_conv1d_update_multi(x, x_stride_n, x_stride_d, x_stride_t, conv_state, stride_s, stride_d,
+                            stride_l, weight, bias, act, indices, cache_seqlens, N, D, T, S, L, W, out,
+                            out_stride_n, out_stride_d, out_stride_t, intermediate_states, status_dev,
+                            route, stream) -> int:
+    return lib.ccu_conv1d_update_multi(x, x_stride_n, x_stride_d, x_stride_t, conv_state, stride_s,
+                                       stride_d, stride_l, weight, bias, act, indices, cache_seqlens,
+                                       N, D, T, S, L, W, out, out_stride_n, out_stride_d, out_stride_t,
+                                       intermediate_states, status_dev, route, stream)
 
 
 def ccu_conv1d_select_route(x, ld, conv_state, stride_s, stride_d, stride_l, weight, bias, act,
@@ -189,7 +203,8 @@ def _check_tensor(name, t, dtype, torch):
 
 
 def causal_conv1d_update(x, conv_state, weight, bias=None, activation=None, *, cache_seqlens=None,
-                         conv_state_indices=None, out=None, route: str = "auto", status=None):
+                         conv_state_indices=None, out=None, route: str = "auto", status=None,
+                         intermediate_states=None):
     """One decode step: mutate ``conv_state`` in place and return the BF16 output ``[N, D]``.
 
     Follows the cuDNN page "Causal Conv1d Decode Update" ("Python API" and "Semantic
@@ -201,6 +216,10 @@ def causal_conv1d_update(x, conv_state, weight, bias=None, activation=None, *, c
     is at ``cache_seqlens[n] % L`` and only that entry is overwritten. ``out`` (optional, preallocated ``[N, D]`` BF16), ``route`` (kernel
     family) and ``status`` (int32 device word: turns on the device range check) are
     extensions of this binding. Runs on the current CUDA stream.
+
+    A 3-D ``x`` ``[N, D, T]`` (any strides) is the multi-token update: T tokens per row,
+    output ``[N, D, T]`` laid out like ``x``; ``intermediate_states`` (optional BF16
+    ``[N, T, D, L]`` contiguous) receives the state after every token.
     """
     import torch
 
@@ -208,9 +227,12 @@ def causal_conv1d_update(x, conv_state, weight, bias=None, activation=None, *, c
         raise ValueError(f"activation must be one of None, 'identity', 'silu', 'swish'; got {activation!r}")
     _check_tensor("x", x, torch.bfloat16, torch)
     if x.dim() == 3:
-        raise NotImplementedError("3D x [N, D, Tstep] (multi-token update) is not served")
+        return _update_multi(x, conv_state, weight, bias, activation, cache_seqlens,
+                             conv_state_indices, out, route, status, intermediate_states, torch)
     if x.dim() != 2:
-        raise ValueError(f"x must be 2D [N, D], got {x.dim()}D")
+        raise ValueError(f"x must be 2D [N, D] or 3D [N, D, T], got {x.dim()}D")
+    if intermediate_states is not None:
+        raise ValueError("intermediate_states needs a multi-token x [N, D, T]")
     if x.stride(1) != 1:
         raise ValueError("x must have unit stride along D")
     _check_tensor("conv_state", conv_state, torch.bfloat16, torch)
@@ -253,6 +275,53 @@ def causal_conv1d_update(x, conv_state, weight, bias=None, activation=None, *, c
         _ptr(x), ld, _ptr(conv_state), ss, sd, sl, _ptr(weight), _ptr(bias),
         _ACTIVATIONS[activation], _ptr(conv_state_indices), _ptr(cache_seqlens), N, D, S, L, W, _ptr(out),
         _ptr(status), ROUTES[route], stream)
+    raise_for_status(st)
+    return out
+
+
+def _update_multi(x, conv_state, weight, bias, activation, cache_seqlens, conv_state_indices, out,
+                  route, status, intermediate_states, torch):
+    if activation not in _ACTIVATIONS:
+        raise ValueError(f"activation must be one of None, 'identity', 'silu', 'swish'; got {activation!r}")
+    for name, t in (("conv_state", conv_state), ("weight", weight)):
+        _check_tensor(name, t, torch.bfloat16, torch)
+    if conv_state.dim() != 3:
+        raise ValueError("conv_state must be 3D [S, D, L]")
+    if weight.dim() != 2 or not weight.is_contiguous():
+        raise ValueError("weight must be a contiguous 2D [D, W] tensor")
+    N, D, T = x.shape
+    S, Ds, L = conv_state.shape
+    Dw, W = weight.shape
+    if Ds != D or Dw != D:
+        raise ValueError(f"channel counts differ: x {D}, conv_state {Ds}, weight {Dw}")
+    if bias is not None:
+        _check_tensor("bias", bias, torch.bfloat16, torch)
+        if bias.shape != (D,) or not bias.is_contiguous():
+            raise ValueError("bias must be a contiguous [D] tensor")
+    for name, t in (("conv_state_indices", conv_state_indices), ("cache_seqlens", cache_seqlens)):
+        if t is not None:
+            _check_tensor(name, t, torch.int32, torch)
+            if t.shape != (N,) or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous int32 [N] tensor")
+    if out is None:
+        out = torch.empty_like(x)  # same strides as a dense x
+    else:
+        _check_tensor("out", out, torch.bfloat16, torch)
+        if out.shape != (N, D, T):
+            raise ValueError("out must be [N, D, T]")
+    if intermediate_states is not None:
+        _check_tensor("intermediate_states", intermediate_states, torch.bfloat16, torch)
+        if intermediate_states.shape != (N, T, D, L) or not intermediate_states.is_contiguous():
+            raise ValueError("intermediate_states must be a contiguous [N, T, D, L] tensor")
+    if status is not None:
+        _check_tensor("status", status, torch.int32, torch)
+    if route not in ROUTES:
+        raise ValueError(f"route must be one of {sorted(ROUTES)}")
+    stream = torch.cuda.current_stream(x.device).cuda_stream
+    st = lib.ccu_conv1d_update_multi(
+        _ptr(x), *x.stride(), _ptr(conv_state), *conv_state.stride(), _ptr(weight), _ptr(bias),
+        _ACTIVATIONS[activation], _ptr(conv_state_indices), _ptr(cache_seqlens), N, D, T, S, L, W,
+        _ptr(out), *out.stride(), _ptr(intermediate_states), _ptr(status), ROUTES[route], stream)
     raise_for_status(st)
     return out
 

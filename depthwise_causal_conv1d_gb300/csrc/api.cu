@@ -210,6 +210,128 @@ ccu_status_t run(const Args &a, int route, cudaStream_t stream) {
   return CCU_OK;
 }
 
+// ---------------------------------------------------------------- multi-token update
+
+struct MultiArgs {
+  Args a;  // x, state, weight, bias, act, indices, seqlens, N, D, S, L, W, out, status
+  int64_t T, sxn, sxd, sxt, son, sod, sot;
+  const void *inter;
+};
+
+ccu_status_t validate_multi(const MultiArgs &m, bool *noop, Layout *layout) {
+  const Args &a = m.a;
+  g_last_error[0] = '\0';
+  if (a.act != CCU_ACT_IDENTITY && a.act != CCU_ACT_SILU)
+    return fail(CCU_ERR_INVALID_ARGUMENT, "act must be CCU_ACT_IDENTITY or CCU_ACT_SILU, got %d",
+                a.act);
+  if (a.N < 0 || a.D < 0 || a.S < 0 || m.T < 0)
+    return fail(CCU_ERR_INVALID_ARGUMENT, "N, D, T and S must be >= 0");
+  if (a.W < 1) return fail(CCU_ERR_INVALID_ARGUMENT, "W must be >= 1, got %lld", (long long)a.W);
+  if (a.L < a.W - 1)
+    return fail(CCU_ERR_INVALID_ARGUMENT, "L must be >= W - 1 (L=%lld, W=%lld)", (long long)a.L,
+                (long long)a.W);
+  if (a.W != kW)
+    return fail(CCU_ERR_NOT_IMPLEMENTED, "only width W == 4 is served, got W=%lld",
+                (long long)a.W);
+  if (a.status != nullptr && !aligned(a.status, 4))
+    return fail(CCU_ERR_INVALID_ARGUMENT, "status word must be 4-byte aligned");
+  if (a.N == 0 || a.D == 0 || m.T == 0) {
+    *noop = true;
+    return CCU_OK;
+  }
+  *noop = false;
+  if (m.sxn < 0 || m.sxd < 0 || m.sxt < 0 || m.son < 0 || m.sod < 0 || m.sot < 0)
+    return fail(CCU_ERR_INVALID_ARGUMENT, "x and out strides must be >= 0");
+  if (a.x == nullptr || a.w == nullptr || a.out == nullptr || (a.state == nullptr && a.S > 0))
+    return fail(CCU_ERR_INVALID_ARGUMENT, "x, conv_state, weight and out must not be NULL");
+  if (!aligned(a.x, 16) || !aligned(a.state, 16) || !aligned(a.w, 16) || !aligned(a.out, 16) ||
+      (a.bias != nullptr && !aligned(a.bias, 16)) || (m.inter != nullptr && !aligned(m.inter, 16)))
+    return fail(CCU_ERR_INVALID_ARGUMENT, "BF16 tensors must be 16-byte aligned");
+  if (a.idx != nullptr && !aligned(a.idx, 4))
+    return fail(CCU_ERR_INVALID_ARGUMENT, "conv_state_indices must be 4-byte aligned");
+  if (a.cache_seqlens != nullptr && !aligned(a.cache_seqlens, 4))
+    return fail(CCU_ERR_INVALID_ARGUMENT, "cache_seqlens must be 4-byte aligned");
+  if (a.idx == nullptr && a.S < a.N)
+    return fail(CCU_ERR_INVALID_ARGUMENT,
+                "without conv_state_indices row n uses slot n, so S must be >= N (S=%lld, N=%lld)",
+                (long long)a.S, (long long)a.N);
+  const int64_t lim = INT64_MAX / 4;
+  if (!mul_le(a.D, a.L, lim) || !mul_le(a.S, a.D * a.L, lim) || !mul_le(a.N, m.T, lim) ||
+      !mul_le(a.N * m.T, a.D * a.L, lim))
+    return fail(CCU_ERR_INVALID_ARGUMENT, "tensor sizes overflow 64-bit indexing");
+  if (a.ss == a.D * a.L && a.sd == a.L && a.sl == 1) {
+    *layout = Layout::Compact;
+  } else if (a.ss == a.L * a.D && a.sd == 1 && a.sl == a.D) {
+    *layout = Layout::ChannelLast;
+  } else {
+    return fail(CCU_ERR_NOT_IMPLEMENTED,
+                "conv_state strides (%lld, %lld, %lld) are neither compact (D*L, L, 1) nor "
+                "channel-last (L*D, 1, D)",
+                (long long)a.ss, (long long)a.sd, (long long)a.sl);
+  }
+  return CCU_OK;
+}
+
+// The vector multi-token kernel moves 8 channels of one token as one 16-byte vector.
+bool multi_vector_serves(const MultiArgs &m) {
+  const Args &a = m.a;
+  return a.D % 8 == 0 && a.L <= kVectorMaxL && m.sxd == 1 && m.sod == 1 && m.sxn % 8 == 0 &&
+         m.sxt % 8 == 0 && m.son % 8 == 0 && m.sot % 8 == 0;
+}
+
+ccu_status_t run_multi(const MultiArgs &m, int route, cudaStream_t stream) {
+  bool noop = false;
+  Layout layout = Layout::Compact;
+  ccu_status_t st = validate_multi(m, &noop, &layout);
+  if (st != CCU_OK || noop) return st;
+  int chosen;
+  if (route == CCU_ROUTE_AUTO) {
+    chosen = multi_vector_serves(m) ? CCU_ROUTE_VECTOR : CCU_ROUTE_SCALAR;
+  } else if (route == CCU_ROUTE_SCALAR || (route == CCU_ROUTE_VECTOR && multi_vector_serves(m))) {
+    chosen = route;
+  } else if (route >= 0 && route < CCU_ROUTE_COUNT) {
+    return fail(CCU_ERR_NOT_IMPLEMENTED, "route '%s' does not serve these multi-token arguments",
+                ccu_route_name(route));
+  } else {
+    return fail(CCU_ERR_INVALID_ARGUMENT, "unknown route %d", route);
+  }
+  const Args &a = m.a;
+  UpdateParams p;
+  p.x = static_cast<const uint16_t *>(a.x);
+  p.ld = 0;
+  p.state = static_cast<uint16_t *>(const_cast<void *>(a.state));
+  p.w = static_cast<const uint16_t *>(a.w);
+  p.bias = static_cast<const uint16_t *>(a.bias);
+  p.idx = a.idx;
+  p.seqlens = a.cache_seqlens;
+  p.out = static_cast<uint16_t *>(const_cast<void *>(a.out));
+  p.status = const_cast<int32_t *>(a.status);
+  p.N = a.N;
+  p.D = a.D;
+  p.S = a.S;
+  p.L = a.L;
+  p.ss = a.ss;
+  p.sd = a.sd;
+  p.sl = a.sl;
+  p.layout = (int)layout;
+  p.rows_per_cta = 1;
+  MultiParams mp;
+  mp.T = m.T;
+  mp.sxn = m.sxn;
+  mp.sxd = m.sxd;
+  mp.sxt = m.sxt;
+  mp.son = m.son;
+  mp.sod = m.sod;
+  mp.sot = m.sot;
+  mp.inter = static_cast<uint16_t *>(const_cast<void *>(m.inter));
+  cudaError_t e = chosen == CCU_ROUTE_VECTOR ? launch_multi_vector(p, mp, a.act, stream)
+                                             : launch_multi_scalar(p, mp, a.act, stream);
+  if (e != cudaSuccess)
+    return fail(CCU_ERR_CUDA, "launch of the multi-token %s kernel failed: %s",
+                ccu_route_name(chosen), cudaGetErrorString(e));
+  return CCU_OK;
+}
+
 }  // namespace
 
 void record_error(const char *msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
@@ -293,6 +415,29 @@ ccu_status_t ccu_conv1d_select_route(const void *x, int64_t ld, const void *conv
   st = ccu::choose(route, a, layout, &chosen);
   if (st == CCU_OK) *chosen_route = chosen;
   return st;
+}
+
+ccu_status_t ccu_conv1d_update_multi(const void *x, int64_t x_stride_n, int64_t x_stride_d,
+                                     int64_t x_stride_t, void *conv_state, int64_t stride_s,
+                                     int64_t stride_d, int64_t stride_l, const void *weight,
+                                     const void *bias, ccu_act_t act, const int32_t *indices,
+                                     const int32_t *cache_seqlens, int64_t N, int64_t D, int64_t T,
+                                     int64_t S, int64_t L, int64_t W, void *out,
+                                     int64_t out_stride_n, int64_t out_stride_d,
+                                     int64_t out_stride_t, void *intermediate_states,
+                                     int32_t *status_dev, int32_t route, ccu_stream_t stream) {
+  ccu::MultiArgs m;
+  m.a = Args{x,    0,       conv_state,    stride_s, stride_d, stride_l, weight, bias, (int)act,
+             indices, cache_seqlens, N, D, S, L, W, out, status_dev};
+  m.T = T;
+  m.sxn = x_stride_n;
+  m.sxd = x_stride_d;
+  m.sxt = x_stride_t;
+  m.son = out_stride_n;
+  m.sod = out_stride_d;
+  m.sot = out_stride_t;
+  m.inter = intermediate_states;
+  return ccu::run_multi(m, route, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int64_t ccu_conv1d_check_indices_scratch_bytes(int64_t S) {

@@ -32,6 +32,15 @@ struct UpdateParams {
   int rows_per_cta;       // rows each CTA walks (vector kernels)
 };
 
+// The extra arguments of the multi-token update (x[N, D, T] and out[N, D, T] by element
+// strides; intermediate_states [N, T, D, L] compact, or nullptr).
+struct MultiParams {
+  int64_t T;
+  int64_t sxn, sxd, sxt;
+  int64_t son, sod, sot;
+  uint16_t *inter;
+};
+
 // Launch description chosen on the host.
 struct LaunchShape {
   dim3 grid;
@@ -259,6 +268,10 @@ cudaError_t take_planes_error(int32_t *bits);
 void record_error(const char *msg);
 // Reads and clears the device error word that kernels without a status word report into.
 cudaError_t take_async_error(int32_t *bits);
+cudaError_t launch_multi_scalar(const UpdateParams &p, const MultiParams &m, int act,
+                                cudaStream_t stream);
+cudaError_t launch_multi_vector(const UpdateParams &p, const MultiParams &m, int act,
+                                cudaStream_t stream);
 cudaError_t launch_check_indices(const int32_t *idx, int64_t N, int64_t S, uint32_t *bitmap,
                                  int32_t *status, cudaStream_t stream);
 

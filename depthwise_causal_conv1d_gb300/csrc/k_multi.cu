@@ -1,0 +1,274 @@
+// Multi-token update: T tokens per row in one call, x[N, D, T].
+//
+// The T tokens are appended to the history in order: output t is computed from the width-4
+// window ending at token t, and the new state is the last L entries of the history (with
+// cache_seqlens, token t is written over ring position (q + t) mod L). Optionally the state
+// after every token is written to intermediate_states [N, T, D, L] (compact, in the
+// state's own entry order), so a speculative decoder can roll back to any token.
+//
+// The cuDNN page "Causal Conv1d Decode Update" names this extension without defining it
+// ("Semantic tensor contract": a future multi-token form may admit x[N, D, Tstep] without
+// changing the state or weight meanings; "Current native implementation": multi-token
+// updates and speculative intermediate-state returns are declined today).
+#include "ccu_internal.cuh"
+
+namespace ccu {
+
+int device_sm_count();
+
+namespace {
+
+// One thread per (row, channel), any x / out strides, any L: the correctness anchor.
+template <int ACT>
+__global__ void __launch_bounds__(256) k_multi_scalar(UpdateParams p, MultiParams m) {
+  const int64_t total = p.N * p.D;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t n = i / p.D;
+    const int64_t d = i - n * p.D;
+    const RowSlot r = resolve_row(p, n);
+    if (r.s < 0) {
+      for (int64_t t = 0; t < m.T; ++t) p.out[n * m.son + d * m.sod + t * m.sot] = 0;
+      continue;
+    }
+    uint16_t *st = p.state + r.s * p.ss + d * p.sd;
+    const int64_t L = p.L;
+    const bool ring = p.seqlens != nullptr;
+    const int64_t q = ring ? r.q : 0;
+    const uint16_t *xp = p.x + n * m.sxn + d * m.sxd;
+    const uint16_t *w = p.w + d * kW;
+    // Entry k of the time-ordered history (k < L: state entry k, oldest first; else token
+    // k - L), read before any of this channel's state is overwritten.
+    auto hist = [&](int64_t k) -> uint16_t {
+      if (k < L) return st[(ring ? (q + k) % L : k) * p.sl];
+      return xp[(k - L) * m.sxt];
+    };
+    uint16_t h0 = hist(L - 3), h1 = hist(L - 2), h2 = hist(L - 1);
+    for (int64_t t = 0; t < m.T; ++t) {
+      const uint16_t xv = xp[t * m.sxt];
+      float acc = 0.0f;
+      acc = __fmaf_rn(bf16_bits(h0), bf16_bits(w[0]), acc);
+      acc = __fmaf_rn(bf16_bits(h1), bf16_bits(w[1]), acc);
+      acc = __fmaf_rn(bf16_bits(h2), bf16_bits(w[2]), acc);
+      acc = __fmaf_rn(bf16_bits(xv), bf16_bits(w[3]), acc);
+      if (p.bias != nullptr) acc = acc + bf16_bits(p.bias[d]);
+      p.out[n * m.son + d * m.sod + t * m.sot] = round_bf16(activate<ACT>(acc));
+      h0 = h1;
+      h1 = h2;
+      h2 = xv;
+      if (m.inter != nullptr) {
+        // the state after token t in its own order: history[t+1 .. t+L]; a ring holds the
+        // entry of age (l - (q + t + 1)) mod L at position l
+        uint16_t *it = m.inter + ((n * m.T + t) * p.D + d) * L;
+        for (int64_t l = 0; l < L; ++l) {
+          int64_t age = l;
+          if (ring) {
+            age = (l - (q + t + 1)) % L;
+            if (age < 0) age += L;
+          }
+          it[l] = hist(t + 1 + age);
+        }
+      }
+    }
+    // The new state: the last L history entries. Linear: entry i takes history[T + i],
+    // ascending, so each entry is read before it is overwritten. Ring: the tokens land at
+    // (q + t) mod L in order; only the last L writes survive.
+    if (ring) {
+      for (int64_t t = (m.T > L ? m.T - L : 0); t < m.T; ++t) st[((q + t) % L) * p.sl] = xp[t * m.sxt];
+    } else {
+      for (int64_t l = 0; l < L; ++l) st[l * p.sl] = hist(m.T + l);
+    }
+  }
+}
+
+// Compact-order position of (channel c, entry l) in 4*L words, and the static transposes
+// between the channel-last planes and that order.
+template <int L>
+__device__ __forceinline__ void planes_to_compact(const uint32_t (&pl)[4 * L], uint32_t (&cw)[4 * L]) {
+#pragma unroll
+  for (int i = 0; i < 4 * L; ++i) {
+    const int e0 = 2 * i, e1 = 2 * i + 1;  // compact positions c*L + l
+    const uint32_t v0 = get16(pl, (e0 % L) * 8 + e0 / L);
+    const uint32_t v1 = get16(pl, (e1 % L) * 8 + e1 / L);
+    cw[i] = v0 | (v1 << 16);
+  }
+}
+
+template <int L>
+__device__ __forceinline__ void compact_to_planes(const uint32_t (&cw)[4 * L], uint32_t (&pl)[4 * L]) {
+#pragma unroll
+  for (int i = 0; i < 4 * L; ++i) {
+    const int e0 = 2 * i, e1 = 2 * i + 1;  // plane positions l*8 + c
+    const uint32_t v0 = get16(cw, (e0 % 8) * L + e0 / 8);
+    const uint32_t v1 = get16(cw, (e1 % 8) * L + e1 / 8);
+    pl[i] = v0 | (v1 << 16);
+  }
+}
+
+// 8 channels per thread, x and out channel-contiguous (16-byte vectors per token), state in
+// registers in compact order for the whole row, L and layout compile-time.
+template <int L, int ACT, int LAYOUT, bool RING>
+__global__ void __launch_bounds__(256) k_multi_vector(UpdateParams p, MultiParams m) {
+  const int64_t groups = p.D >> 3;
+  const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= groups) return;
+  const int64_t c0 = g << 3;
+  uint32_t wv[16];
+  {
+    const uint16_t *wp = p.w + c0 * kW;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint4 t = ld_keep(wp + 8 * k);
+      wv[4 * k] = t.x; wv[4 * k + 1] = t.y; wv[4 * k + 2] = t.z; wv[4 * k + 3] = t.w;
+    }
+  }
+  const bool has_bias = p.bias != nullptr;
+  uint32_t bv[4] = {0u, 0u, 0u, 0u};
+  if (has_bias) {
+    const uint4 t = ld_keep(p.bias + c0);
+    bv[0] = t.x; bv[1] = t.y; bv[2] = t.z; bv[3] = t.w;
+  }
+
+  for (int64_t n = blockIdx.y; n < p.N; n += gridDim.y) {
+    const RowSlot row = resolve_row(p, n);
+    if (row.s < 0) {
+      for (int64_t t = 0; t < m.T; ++t)
+        st_stream(p.out + n * m.son + t * m.sot + c0, make_uint4(0u, 0u, 0u, 0u));
+      continue;
+    }
+    // state of the 8 channels, compact order (c*L + l)
+    uint32_t ow[4 * L];
+    if constexpr (LAYOUT == (int)Layout::Compact) {
+      const uint16_t *sp = p.state + row.s * (p.D * L) + c0 * L;
+#pragma unroll
+      for (int k = 0; k < L; ++k) {
+        const uint4 u = ld_stream(sp + 8 * k);
+        ow[4 * k] = u.x; ow[4 * k + 1] = u.y; ow[4 * k + 2] = u.z; ow[4 * k + 3] = u.w;
+      }
+    } else {
+      const uint16_t *sp = p.state + row.s * (L * p.D) + c0;
+      uint32_t pl[4 * L];
+#pragma unroll
+      for (int l = 0; l < L; ++l) {
+        const uint4 u = ld_stream(sp + (int64_t)l * p.D);
+        pl[4 * l] = u.x; pl[4 * l + 1] = u.y; pl[4 * l + 2] = u.z; pl[4 * l + 3] = u.w;
+      }
+      planes_to_compact<L>(pl, ow);
+    }
+
+    const uint16_t *xrow = p.x + n * m.sxn + c0;
+    uint16_t *orow = p.out + n * m.son + c0;
+    // Tokens go in groups of kGroup: the group's x loads are issued together, before any
+    // of its outputs is computed or stored (stores to out could alias x as far as the
+    // compiler knows, which would otherwise keep one token's load behind the previous
+    // token's store).
+    constexpr int kGroup = 4;
+    for (int64_t t0 = 0; t0 < m.T; t0 += kGroup) {
+      uint32_t xg[kGroup][4];
+#pragma unroll
+      for (int k = 0; k < kGroup; ++k) {
+        if (t0 + k < m.T) {
+          const uint4 xv = ld_stream(xrow + (t0 + k) * m.sxt);
+          xg[k][0] = xv.x; xg[k][1] = xv.y; xg[k][2] = xv.z; xg[k][3] = xv.w;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kGroup; ++k) {
+        const int64_t t = t0 + k;
+        if (t >= m.T) break;
+        uint32_t nw[4 * L];
+        uint4 outv;
+        if constexpr (RING) {
+          outv = update8_compact_ring<L, ACT>(xg[k], ow, wv, bv, has_bias, (int)((row.q + t) % L), nw);
+        } else {
+          outv = update8_compact<L, ACT>(xg[k], ow, wv, bv, has_bias, nw);
+        }
+        st_stream(orow + t * m.sot, outv);
+#pragma unroll
+        for (int i = 0; i < 4 * L; ++i) ow[i] = nw[i];
+        if (m.inter != nullptr) {
+          uint16_t *it = m.inter + ((n * m.T + t) * p.D + c0) * L;
+#pragma unroll
+          for (int q = 0; q < L; ++q)
+            st_stream(it + 8 * q, make_uint4(ow[4 * q], ow[4 * q + 1], ow[4 * q + 2], ow[4 * q + 3]));
+        }
+      }
+    }
+
+    if constexpr (LAYOUT == (int)Layout::Compact) {
+      uint16_t *sp = p.state + row.s * (p.D * L) + c0 * L;
+#pragma unroll
+      for (int k = 0; k < L; ++k)
+        st_stream(sp + 8 * k, make_uint4(ow[4 * k], ow[4 * k + 1], ow[4 * k + 2], ow[4 * k + 3]));
+    } else {
+      uint16_t *sp = p.state + row.s * (L * p.D) + c0;
+      uint32_t pl[4 * L];
+      compact_to_planes<L>(ow, pl);
+#pragma unroll
+      for (int l = 0; l < L; ++l)
+        st_stream(sp + (int64_t)l * p.D, make_uint4(pl[4 * l], pl[4 * l + 1], pl[4 * l + 2], pl[4 * l + 3]));
+    }
+  }
+}
+
+template <int L, int ACT>
+cudaError_t launch_vec_L(const UpdateParams &p, const MultiParams &m, dim3 grid, dim3 block,
+                         cudaStream_t stream) {
+  const bool ring = p.seqlens != nullptr;
+  if (p.layout == (int)Layout::Compact) {
+    if (ring) k_multi_vector<L, ACT, (int)Layout::Compact, true><<<grid, block, 0, stream>>>(p, m);
+    else k_multi_vector<L, ACT, (int)Layout::Compact, false><<<grid, block, 0, stream>>>(p, m);
+  } else {
+    if (ring) k_multi_vector<L, ACT, (int)Layout::ChannelLast, true><<<grid, block, 0, stream>>>(p, m);
+    else k_multi_vector<L, ACT, (int)Layout::ChannelLast, false><<<grid, block, 0, stream>>>(p, m);
+  }
+  return cudaGetLastError();
+}
+
+template <int ACT>
+cudaError_t launch_vec_A(const UpdateParams &p, const MultiParams &m, dim3 grid, dim3 block,
+                         cudaStream_t stream) {
+  switch (p.L) {
+    case 3: return launch_vec_L<3, ACT>(p, m, grid, block, stream);
+    case 4: return launch_vec_L<4, ACT>(p, m, grid, block, stream);
+    case 5: return launch_vec_L<5, ACT>(p, m, grid, block, stream);
+    case 6: return launch_vec_L<6, ACT>(p, m, grid, block, stream);
+    case 7: return launch_vec_L<7, ACT>(p, m, grid, block, stream);
+    case 8: return launch_vec_L<8, ACT>(p, m, grid, block, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_multi_scalar(const UpdateParams &p, const MultiParams &m, int act,
+                                cudaStream_t stream) {
+  const int threads = 256;
+  int64_t blocks = (p.N * p.D + threads - 1) / threads;
+  const int64_t cap = (int64_t)device_sm_count() * 16;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (act == 1) {
+    k_multi_scalar<1><<<(unsigned)blocks, threads, 0, stream>>>(p, m);
+  } else {
+    k_multi_scalar<0><<<(unsigned)blocks, threads, 0, stream>>>(p, m);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_multi_vector(const UpdateParams &p, const MultiParams &m, int act,
+                                cudaStream_t stream) {
+  const int64_t groups = p.D / 8;
+  int threads = 256;
+  if (groups < threads) threads = (int)((groups + 31) / 32 * 32);
+  const int64_t gx = (groups + threads - 1) / threads;
+  // one row per CTA row-step: each row already carries T tokens of work
+  int64_t gy = (int64_t)device_sm_count() * 8 / gx;
+  if (gy < 1) gy = 1;
+  if (gy > p.N) gy = p.N;
+  if (gy > 65535) gy = 65535;
+  const dim3 grid((unsigned)gx, (unsigned)gy), block(threads);
+  return act == 1 ? launch_vec_A<1>(p, m, grid, block, stream) : launch_vec_A<0>(p, m, grid, block, stream);
+}
+
+}  // namespace ccu

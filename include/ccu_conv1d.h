@@ -195,6 +195,45 @@ CCU_API ccu_status_t ccu_conv1d_select_route(const void *x, int64_t ld, const vo
                                      const void *out, int32_t route, int32_t *chosen_route);
 
 /*
+ * ccu_conv1d_update_multi -- T tokens per row in one call (multi-token update, with the
+ * state after every token on request, for speculative decoding).
+ *
+ * The cuDNN page "Causal Conv1d Decode Update" says a future multi-token extension can
+ * admit x[N, D, Tstep] without changing the meaning of the state and the weights ("Semantic
+ * tensor contract"), and lists multi-token updates and speculative intermediate-state
+ * returns as not yet served ("Current native implementation"). This entry point serves
+ * them with that meaning: the T tokens of row n are appended to the slot's history in
+ * order; output t is the activation of the width-4 window ending at token t (plus bias);
+ * the new state is the last L history entries. It equals T calls of ccu_conv1d_update
+ * with x[:, :, 0], ..., x[:, :, T-1] (and, with cache_seqlens, cache_seqlens + t for token
+ * t: token t lands at ring position (cache_seqlens[n] + t) mod L).
+ *
+ *   x            BF16, element (n, d, t) at x[n*x_stride_n + d*x_stride_d + t*x_stride_t];
+ *                any non-negative strides. Channel-contiguous x (x_stride_d == 1, the
+ *                other two strides multiples of 8, 16-byte aligned) runs the vector kernel.
+ *   out          BF16, element (n, d, t) at out[n*out_stride_n + d*out_stride_d +
+ *                t*out_stride_t]; must not overlap itself or any input. Padding rows get
+ *                +0 for every token.
+ *   intermediate_states  NULL, or BF16 [N, T, D, L] contiguous, 16-byte aligned: entry
+ *                (n, t, d, l) is entry l of the slot's state (in the state's own order,
+ *                linear or ring) after token t. Padding rows' entries are not written.
+ *   T            tokens per row; T == 0 is a no-op.
+ *   status_dev   NULL, or a device status word as in ccu_conv1d_update_checked.
+ *   route        CCU_ROUTE_AUTO, CCU_ROUTE_SCALAR or CCU_ROUTE_VECTOR (others decline).
+ * Other arguments (state layouts, weight, bias, act, indices, cache_seqlens, N, D, S, L, W,
+ * stream) and returns as ccu_conv1d_update.
+ */
+CCU_API ccu_status_t ccu_conv1d_update_multi(const void *x, int64_t x_stride_n, int64_t x_stride_d,
+                                             int64_t x_stride_t, void *conv_state, int64_t stride_s,
+                                             int64_t stride_d, int64_t stride_l, const void *weight,
+                                             const void *bias, ccu_act_t act, const int32_t *indices,
+                                             const int32_t *cache_seqlens, int64_t N, int64_t D,
+                                             int64_t T, int64_t S, int64_t L, int64_t W, void *out,
+                                             int64_t out_stride_n, int64_t out_stride_d,
+                                             int64_t out_stride_t, void *intermediate_states,
+                                             int32_t *status_dev, int32_t route, ccu_stream_t stream);
+
+/*
  * ccu_conv1d_check_indices -- validate a slot-index vector on the device without trapping.
  *
  * Checks the two preconditions of the conv_state_indices paragraph of "Causal Conv1d

@@ -48,6 +48,7 @@ class Workload:
     layout: str = "compact"  # "compact" (D*L, L, 1) or "channel_last" (L*D, 1, D)
     seed: int = 0
     ring: bool = False  # ring-buffer state: draw cache_seqlens [N]
+    T: int = 1  # tokens per row; T > 1: x is drawn as [N, T, D] (token-major), ld == D
 
     @property
     def has_bias(self) -> bool:
@@ -85,6 +86,16 @@ RING_WORKLOADS = {
         dataclasses.replace(WORKLOADS["large_n4096_d16384_l3_perm_pad5_silu"],
                             name="large_n4096_d16384_l3_perm_pad5_silu_ring_chlast", ring=True,
                             layout="channel_last"),
+    ]
+}
+
+# Multi-token update: four tokens per row in one call (x token-major [N, T, D]).
+MULTI_WORKLOADS = {
+    w.name: w
+    for w in [
+        Workload("multi_n1024_d16384_t4_l3_bias_silu", N=1024, D=16384, W=4, L=3, S=1024, ld=16384,
+                 x_dist=("normal", 1.0), w_dist=("normal", 1.0), bias_std=0.1, act="silu",
+                 indices="perm_pad", pad_frac=0.05, T=4),
     ]
 }
 
@@ -168,7 +179,7 @@ class Inputs:
     """Host copies of one workload's tensors (BF16 as uint16 bit patterns)."""
 
     wl: Workload
-    x: np.ndarray  # [N, ld]; columns D..ld-1 hold NaN canaries
+    x: np.ndarray  # [N, ld] (columns D..ld-1 hold NaN canaries), or [N, T, D] when T > 1
     weight: np.ndarray  # [D, W]
     conv_state: np.ndarray  # logical [S, D, L], compact
     bias: Optional[np.ndarray]  # [D] or None
@@ -181,8 +192,11 @@ def generate(wl: Workload, seed: Optional[int] = None) -> Inputs:
     for a ring-buffer state cache_seqlens: counts uniform in [0, 2^20))."""
     rng = np.random.Generator(np.random.PCG64(wl.seed if seed is None else seed))
     N, D, W, L, S, ld = wl.N, wl.D, wl.W, wl.L, wl.S, wl.ld
-    x = np.full((N, ld), BF16_NAN_BITS, dtype=np.uint16)
-    x[:, :D] = _draw(rng, wl.x_dist, N * D).reshape(N, D)
+    if wl.T > 1:
+        x = _draw(rng, wl.x_dist, N * wl.T * D).reshape(N, wl.T, D)
+    else:
+        x = np.full((N, ld), BF16_NAN_BITS, dtype=np.uint16)
+        x[:, :D] = _draw(rng, wl.x_dist, N * D).reshape(N, D)
     weight = _draw(rng, wl.w_dist, D * W).reshape(D, W)
     conv_state = _draw(rng, wl.x_dist, S * D * L).reshape(S, D, L)
     bias = _draw(rng, ("normal", wl.bias_std), D) if wl.has_bias else None
@@ -200,7 +214,7 @@ def algorithmic_bytes(wl: Workload, indices: Optional[np.ndarray]) -> int:
     """Bytes the update must move at minimum, by the method's own accounting.
 
     Active row element: 2 B x read + 2L B state read + 2L B state write + 2 B out
-    write. Padding row element: 2 B out write. Plus weight (2*D*W B), bias (2*D B)
+    write. Padding row element: 2 B out write (per token). Plus weight (2*D*W B), bias (2*D B)
     and indices (4*N B), each read once. A ring-buffer state needs only the W-1 window
     entries read and one entry written: 2 + 2(W-1) + 2 + 2 B per active element, plus
     cache_seqlens (4*N B).
@@ -211,7 +225,9 @@ def algorithmic_bytes(wl: Workload, indices: Optional[np.ndarray]) -> int:
         per_active = 2 + 2 * (wl.W - 1) + 2 + 2
     else:
         per_active = 2 + 2 * wl.L + 2 * wl.L + 2
-    total = active * wl.D * per_active + n_pad * wl.D * 2
+    if wl.T > 1:  # T tokens of x and out per row; the state is read and written once
+        per_active = 4 * wl.T + (2 * (wl.W - 1) + 2 * min(wl.T, wl.L) if wl.ring else 4 * wl.L)
+    total = active * wl.D * per_active + n_pad * wl.D * 2 * wl.T
     total += 2 * wl.D * wl.W
     if wl.has_bias:
         total += 2 * wl.D

@@ -377,8 +377,10 @@ def test_typed_declines_through_binding():
     seq = torch.zeros((4,), dtype=torch.int32, device=DEV)
     with pytest.raises(ValueError, match="cache_seqlens"):
         ccu.causal_conv1d_update(x, st, w, cache_seqlens=seq[:3])
-    with pytest.raises(NotImplementedError, match="3D x"):
-        ccu.causal_conv1d_update(x.view(4, 64, 1), st, w)
+    with pytest.raises(ValueError, match="2D"):
+        ccu.causal_conv1d_update(x.view(4, 64, 1, 1), st, w)
+    with pytest.raises(ValueError, match="intermediate_states"):
+        ccu.causal_conv1d_update(x, st, w, intermediate_states=torch.empty((4, 1, 64, 3), dtype=torch.bfloat16, device=DEV))
     with pytest.raises(NotImplementedError, match="W == 4"):
         ccu.causal_conv1d_update(x, st, w[:, :3].contiguous())
     with pytest.raises(ValueError, match="L must be >= W - 1"):
@@ -503,3 +505,94 @@ def test_ring_checked_negative_seqlens(route):
     got_out, got_state, status, ok = run_gpu(inp, route=route, checked=True, cache_seqlens=seq)
     assert ok and status & 1
     assert_parity(inp, got_out, got_state, want_out, want_state, "ring checked")
+
+
+# ----------------------------------------------------------------------------- multi-token update
+
+MULTI = [
+    dict(N=6, D=264, T=4, L=3, S=8, ring=False, x_layout="tokens_major"),
+    dict(N=5, D=520, T=1, L=4, S=5, ring=True, x_layout="tokens_major"),
+    dict(N=7, D=64, T=7, L=4, S=9, ring=False, x_layout="channels_major"),
+    dict(N=3, D=2056, T=3, L=8, S=3, ring=True, x_layout="tokens_major"),
+    dict(N=4, D=37, T=5, L=5, S=6, ring=False, x_layout="tokens_major"),
+    dict(N=4, D=128, T=9, L=3, S=4, ring=True, x_layout="channels_major"),
+    dict(N=3, D=72, T=2, L=12, S=5, ring=False, x_layout="tokens_major"),
+]
+
+
+def _multi_inputs(case, seed):
+    rng = np.random.default_rng(seed)
+    N, D, T, L, S = case["N"], case["D"], case["T"], case["L"], case["S"]
+    x_tok = synthetic.f64_to_bf16_bits(rng.standard_normal((N, T, D)))  # token-major memory
+    weight = synthetic.f64_to_bf16_bits(rng.standard_normal((D, 4)) * 0.5)
+    bias = synthetic.f64_to_bf16_bits(rng.standard_normal(D) * 0.1)
+    state = synthetic.f64_to_bf16_bits(rng.standard_normal((S, D, L)))
+    idx = rng.permutation(S)[:N].astype(np.int32)
+    idx[1] = -1
+    seq = rng.integers(0, 50, size=N).astype(np.int32) if case["ring"] else None
+    return x_tok, weight, bias, state, idx, seq
+
+
+@pytest.mark.parametrize("route", ["auto", "scalar", "vector"])
+@pytest.mark.parametrize("layout", ["compact", "channel_last"])
+@pytest.mark.parametrize("ci", range(len(MULTI)))
+def test_multi_token(route, layout, ci):
+    import depthwise_causal_conv1d_gb300 as ccu
+
+    case = MULTI[ci]
+    N, D, T, L, S = case["N"], case["D"], case["T"], case["L"], case["S"]
+    if route == "vector" and (D % 8 or L > 8 or case["x_layout"] != "tokens_major"):
+        pytest.skip("the vector kernel needs channel-contiguous 16-byte token rows and L <= 8")
+    x_tok, weight, bias, state, idx, seq = _multi_inputs(case, 300 + ci)
+    # oracle on its own copies
+    st_ref = state.copy() if layout == "compact" else synthetic.to_channel_last(state)
+    strides = (D * L, L, 1) if layout == "compact" else (L * D, 1, D)
+    want_out, want_inter = oracle.conv1d_update_multi(x_tok, (T * D, 1, D), st_ref, strides, weight, bias,
+                                                      "silu", idx, seq, N, D, T, S, L, 4, with_inter=True)
+    want_state = st_ref if layout == "compact" else synthetic.from_channel_last(st_ref)
+    # device copies
+    if case["x_layout"] == "tokens_major":
+        x = to_dev_u16(x_tok, DEV).permute(0, 2, 1)  # [N, D, T] view of [N, T, D] memory
+    else:
+        x = to_dev_u16(np.ascontiguousarray(np.transpose(x_tok, (0, 2, 1))), DEV)  # [N, D, T] memory
+    if layout == "compact":
+        st = to_dev_u16(state, DEV)
+    else:
+        st = to_dev_u16(synthetic.to_channel_last(state), DEV).permute(0, 2, 1)
+    inter = torch.zeros((N, T, D, L), dtype=torch.bfloat16, device=DEV)
+    out = ccu.causal_conv1d_update(x, st, to_dev_u16(weight, DEV), to_dev_u16(bias, DEV), "silu",
+                                   conv_state_indices=torch.from_numpy(idx).to(DEV),
+                                   cache_seqlens=None if seq is None else torch.from_numpy(seq).to(DEV),
+                                   route=route, intermediate_states=inter)
+    torch.cuda.synchronize()
+    assert out.stride() == x.stride()
+    got_out = from_dev_u16(out.permute(0, 2, 1).contiguous().permute(0, 2, 1))
+    got_state = from_dev_u16(st.contiguous())
+    got_inter = from_dev_u16(inter)
+    from oracle_pins import bf16_ulp_distance
+
+    assert np.array_equal(got_state, want_state), "final state"
+    assert np.array_equal(got_inter, want_inter), "intermediate states"
+    assert bf16_ulp_distance(got_out, want_out).max() <= 1, "outputs"
+
+
+def test_multi_large_batch():
+    """A large multi-token batch (N=1024, D=16384, T=4, ring state) on the vector kernel."""
+    import depthwise_causal_conv1d_gb300 as ccu
+
+    case = dict(N=1024, D=16384, T=4, L=3, S=1024, ring=True, x_layout="tokens_major")
+    N, D, T, L, S = 1024, 16384, 4, 3, 1024
+    x_tok, weight, bias, state, idx, seq = _multi_inputs(case, 77)
+    st_ref = state.copy()
+    want_out = oracle.conv1d_update_multi(x_tok, (T * D, 1, D), st_ref, (D * L, L, 1), weight, bias,
+                                          "silu", idx, seq, N, D, T, S, L, 4)
+    x = to_dev_u16(x_tok, DEV).permute(0, 2, 1)
+    st = to_dev_u16(state, DEV)
+    out = ccu.causal_conv1d_update(x, st, to_dev_u16(weight, DEV), to_dev_u16(bias, DEV), "silu",
+                                   conv_state_indices=torch.from_numpy(idx).to(DEV),
+                                   cache_seqlens=torch.from_numpy(seq).to(DEV))
+    torch.cuda.synchronize()
+    from oracle_pins import bf16_ulp_distance
+
+    assert np.array_equal(from_dev_u16(st), st_ref)
+    assert bf16_ulp_distance(from_dev_u16(out.permute(0, 2, 1)).transpose(0, 2, 1), want_out).max() <= 1
