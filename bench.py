@@ -572,6 +572,48 @@ def multi_token_rows(dev, stream, reps=50):
     return rows
 
 
+def prefill_rows(dev, stream, reps=50):
+    """µs per call of the full-sequence prefill (with its channel-last final state)."""
+    import torch
+
+    import depthwise_causal_conv1d_gb300 as ccu
+
+    rows = {}
+    for name, spec in synthetic.PREFILL_WORKLOADS.items():
+        x_btd, weight, bias = synthetic.generate_prefill(spec)
+        B, T, D, L = spec["B"], spec["T"], spec["D"], spec["L"]
+        x = to_dev(x_btd, dev).permute(0, 2, 1)  # [B, D, T] view of token-major memory
+        w = to_dev(weight, dev)
+        b = to_dev(bias, dev) if bias is not None else None
+        out = torch.empty_like(x)
+        fin = torch.empty((B, L, D), dtype=torch.bfloat16, device=dev).permute(0, 2, 1)
+        act = ccu.CCU_ACT_SILU if spec["act"] == "silu" else ccu.CCU_ACT_IDENTITY
+
+        def call():
+            st = ccu.lib.ccu_causal_conv1d_fwd(
+                x.data_ptr(), *x.stride(), w.data_ptr(), None if b is None else b.data_ptr(), act,
+                None, 0, 0, 0, B, D, T, L, spec["W"], out.data_ptr(), *out.stride(), fin.data_ptr(),
+                *fin.stride(), 0, stream.cuda_stream)
+            if st != 0:
+                ccu.raise_for_status(st)
+
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            call()
+        e.record(stream)
+        torch.cuda.synchronize()
+        us = a.elapsed_time(e) * 1e3 / reps
+        nbytes = synthetic.prefill_bytes(spec)
+        rows[name] = {"B_x_T_x_D": B * T * D, "bytes": nbytes, "us_per_call": round(us, 3),
+                      "GBps": round(nbytes / (us * 1e-6) / 1e9, 1),
+                      "frac": round(nbytes / (us * 1e-6) / 1e9 / PEAK_GBPS, 4)}
+    return rows
+
+
 def cpu_baseline_sample(inp, target_s: float):
     """Time the single-threaded C oracle on a bounded sample of the workload's rows."""
     import oracle
@@ -674,6 +716,7 @@ def run_ours(args):
         if rank == 0 and world == 1:
             line["per_workload"] = per_workload_table(dev, stream)
             line["multi_token"] = multi_token_rows(dev, stream)
+            line["prefill"] = prefill_rows(dev, stream)
         if rank == 0:
             line["cpu_baseline"] = cpu_baseline_sample(inp, args.cpu_seconds)
     if rank == 0:

@@ -63,6 +63,10 @@ def _load() -> ctypes.CDLL:
                                             vp, vp, i64, i64, i64, i64, i64, i64, vp, i64, i64, i64,
                                             vp, vp, i32, vp]
     lib.ccu_conv1d_update_multi.restype = ctypes.c_int
+    lib.ccu_causal_conv1d_fwd.argtypes = [vp, i64, i64, i64, vp, vp, ctypes.c_int, vp, i64, i64, i64,
+                                          i64, i64, i64, i64, i64, vp, i64, i64, i64, vp, i64, i64, i64,
+                                          i32, vp]
+    lib.ccu_causal_conv1d_fwd.restype = ctypes.c_int
     for f in ("ccu_conv1d_update", "ccu_conv1d_update_checked", "ccu_conv1d_update_ex",
               "ccu_conv1d_select_route", "ccu_conv1d_check_indices"):
         getattr(lib, f).restype = ctypes.c_int
@@ -117,6 +121,17 @@ def ccu_conv1d_update_multi(x, x_stride_n, x_stride_d, x_stride_t, conv_state, s
                                        stride_d, stride_l, weight, bias, act, indices, cache_seqlens,
                                        N, D, T, S, L, W, out, out_stride_n, out_stride_d, out_stride_t,
                                        intermediate_states, status_dev, route, stream)
+
+
+def ccu_causal_conv1d_fwd(x, x_stride_b, x_stride_d, x_stride_t, weight, bias, act, initial_states,
+                          init_stride_b, init_stride_d, init_stride_l, B, D, T, L, W, out, out_stride_b,
+                          out_stride_d, out_stride_t, final_states, final_stride_b, final_stride_d,
+                          final_stride_l, route, stream) -> int:
+    return lib.ccu_causal_conv1d_fwd(x, x_stride_b, x_stride_d, x_stride_t, weight, bias, act,
+                                     initial_states, init_stride_b, init_stride_d, init_stride_l, B, D,
+                                     T, L, W, out, out_stride_b, out_stride_d, out_stride_t,
+                                     final_states, final_stride_b, final_stride_d, final_stride_l,
+                                     route, stream)
 
 
 def ccu_conv1d_select_route(x, ld, conv_state, stride_s, stride_d, stride_l, weight, bias, act,
@@ -324,6 +339,68 @@ def _update_multi(x, conv_state, weight, bias, activation, cache_seqlens, conv_s
         _ptr(out), *out.stride(), _ptr(intermediate_states), _ptr(status), ROUTES[route], stream)
     raise_for_status(st)
     return out
+
+
+def causal_conv1d_fwd(x, weight, bias=None, activation=None, *, initial_states=None,
+                      return_final_states=False, final_states_out=None, final_state_len=None, out=None,
+                      route: str = "auto"):
+    """Full-sequence prefill: causal depthwise convolution of ``x`` [B, D, T] (any strides).
+
+    Returns ``out`` [B, D, T] (laid out like ``x``) and, when ``return_final_states`` or
+    ``final_states_out`` is given, the final state [B, D, L]: the last L inputs, by default
+    L = W - 1 in the channel-last layout (strides (L*D, 1, D)) that the decode update
+    accepts without a copy. ``initial_states`` [B, D, L] (any strides) holds the inputs
+    before the sequence (zeros when None).
+    """
+    import torch
+
+    _check_tensor("x", x, torch.bfloat16, torch)
+    if x.dim() != 3:
+        raise ValueError("x must be 3D [B, D, T]")
+    _check_tensor("weight", weight, torch.bfloat16, torch)
+    if weight.dim() != 2 or not weight.is_contiguous():
+        raise ValueError("weight must be a contiguous 2D [D, W] tensor")
+    if activation not in _ACTIVATIONS:
+        raise ValueError(f"activation must be one of None, 'identity', 'silu', 'swish'; got {activation!r}")
+    B, D, T = x.shape
+    Dw, W = weight.shape
+    if Dw != D:
+        raise ValueError(f"channel counts differ: x {D}, weight {Dw}")
+    if bias is not None:
+        _check_tensor("bias", bias, torch.bfloat16, torch)
+        if bias.shape != (D,) or not bias.is_contiguous():
+            raise ValueError("bias must be a contiguous [D] tensor")
+    L = final_state_len if final_state_len is not None else W - 1
+    if initial_states is not None:
+        _check_tensor("initial_states", initial_states, torch.bfloat16, torch)
+        if initial_states.dim() != 3 or initial_states.shape[:2] != (B, D):
+            raise ValueError("initial_states must be [B, D, L]")
+        L = initial_states.shape[2] if final_state_len is None else L
+        if initial_states.shape[2] != L:
+            raise ValueError("initial_states and the final state must have the same length L")
+    fin = final_states_out
+    if fin is None and return_final_states:
+        fin = torch.empty((B, L, D), dtype=torch.bfloat16, device=x.device).permute(0, 2, 1)
+    if fin is not None:
+        _check_tensor("final_states_out", fin, torch.bfloat16, torch)
+        if fin.shape != (B, D, L):
+            raise ValueError("final states must be [B, D, L]")
+    if out is None:
+        out = torch.empty_like(x)
+    else:
+        _check_tensor("out", out, torch.bfloat16, torch)
+        if out.shape != (B, D, T):
+            raise ValueError("out must be [B, D, T]")
+    if route not in ROUTES:
+        raise ValueError(f"route must be one of {sorted(ROUTES)}")
+    ist = initial_states.stride() if initial_states is not None else (0, 0, 0)
+    fst = fin.stride() if fin is not None else (0, 0, 0)
+    stream = torch.cuda.current_stream(x.device).cuda_stream
+    st = lib.ccu_causal_conv1d_fwd(
+        _ptr(x), *x.stride(), _ptr(weight), _ptr(bias), _ACTIVATIONS[activation], _ptr(initial_states),
+        *ist, B, D, T, L, W, _ptr(out), *out.stride(), _ptr(fin), *fst, ROUTES[route], stream)
+    raise_for_status(st)
+    return (out, fin) if fin is not None else out
 
 
 def check_indices(conv_state_indices, S: int, status=None, scratch=None):

@@ -16,6 +16,8 @@
 
 namespace ccu {
 
+int device_sm_count();
+
 namespace {
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sm_count[kMaxDevices];
@@ -332,6 +334,97 @@ ccu_status_t run_multi(const MultiArgs &m, int route, cudaStream_t stream) {
   return CCU_OK;
 }
 
+// ---------------------------------------------------------------- full-sequence prefill
+
+struct PrefillArgs {
+  const void *x, *w, *bias, *init, *out, *fin;
+  int act;
+  int64_t sxb, sxd, sxt, sib, sid, sil, sob, sod, sot, sfb, sfd, sfl;
+  int64_t B, D, T, L, W;
+};
+
+// Tokens per thread: enough (batch row, channel group, chunk) items to fill the GPU several
+// times over, and at least 32 tokens so the 3-token halo stays a small overhead.
+int64_t prefill_chunk(int64_t B, int64_t lanes, int64_t T) {
+  const int64_t want = (int64_t)device_sm_count() * 2048 * 2;  // thread items to aim for
+  int64_t chunks = want / (B * lanes > 0 ? B * lanes : 1);
+  if (chunks < 1) chunks = 1;
+  int64_t chunk = (T + chunks - 1) / chunks;
+  chunk = (chunk + 3) / 4 * 4;
+  if (chunk < 32) chunk = 32;
+  return chunk;
+}
+
+ccu_status_t run_prefill(const PrefillArgs &a, int route, cudaStream_t stream) {
+  g_last_error[0] = '\0';
+  if (a.act != CCU_ACT_IDENTITY && a.act != CCU_ACT_SILU)
+    return fail(CCU_ERR_INVALID_ARGUMENT, "act must be CCU_ACT_IDENTITY or CCU_ACT_SILU, got %d",
+                a.act);
+  if (a.B < 0 || a.D < 0 || a.T < 0) return fail(CCU_ERR_INVALID_ARGUMENT, "B, D and T must be >= 0");
+  if (a.W < 1) return fail(CCU_ERR_INVALID_ARGUMENT, "W must be >= 1, got %lld", (long long)a.W);
+  if (a.L < a.W - 1)
+    return fail(CCU_ERR_INVALID_ARGUMENT, "L must be >= W - 1 (L=%lld, W=%lld)", (long long)a.L,
+                (long long)a.W);
+  if (a.W != kW)
+    return fail(CCU_ERR_NOT_IMPLEMENTED, "only width W == 4 is served, got W=%lld",
+                (long long)a.W);
+  if (a.B == 0 || a.D == 0 || a.T == 0) return CCU_OK;
+  const int64_t strides[] = {a.sxb, a.sxd, a.sxt, a.sib, a.sid, a.sil, a.sob, a.sod, a.sot,
+                             a.sfb, a.sfd, a.sfl};
+  for (int64_t v : strides)
+    if (v < 0) return fail(CCU_ERR_INVALID_ARGUMENT, "strides must be >= 0");
+  if (a.x == nullptr || a.w == nullptr || a.out == nullptr)
+    return fail(CCU_ERR_INVALID_ARGUMENT, "x, weight and out must not be NULL");
+  if (!aligned(a.x, 16) || !aligned(a.w, 16) || !aligned(a.out, 16) ||
+      (a.bias != nullptr && !aligned(a.bias, 16)) || (a.init != nullptr && !aligned(a.init, 16)) ||
+      (a.fin != nullptr && !aligned(a.fin, 16)))
+    return fail(CCU_ERR_INVALID_ARGUMENT, "BF16 tensors must be 16-byte aligned");
+  if (a.fin != nullptr && a.fin == a.init)
+    return fail(CCU_ERR_INVALID_ARGUMENT,
+                "final_states must not be the initial_states buffer (write the new state elsewhere)");
+  const int64_t lim = INT64_MAX / 4;
+  if (!mul_le(a.B, a.D, lim) || !mul_le(a.B * a.D, a.T, lim) || !mul_le(a.B * a.D, a.L, lim))
+    return fail(CCU_ERR_INVALID_ARGUMENT, "tensor sizes overflow 64-bit indexing");
+
+  const bool vec_ok = a.D % 8 == 0 && a.sxd == 1 && a.sod == 1 && a.sxb % 8 == 0 &&
+                      a.sxt % 8 == 0 && a.sob % 8 == 0 && a.sot % 8 == 0 && a.B <= 65535;
+  PrefillParams f;
+  f.B = a.B;
+  f.T = a.T;
+  f.sxb = a.sxb; f.sxd = a.sxd; f.sxt = a.sxt;
+  f.sob = a.sob; f.sod = a.sod; f.sot = a.sot;
+  f.init = static_cast<const uint16_t *>(a.init);
+  f.sib = a.sib; f.sid = a.sid; f.sil = a.sil;
+  f.fin = static_cast<uint16_t *>(const_cast<void *>(a.fin));
+  f.sfb = a.sfb; f.sfd = a.sfd; f.sfl = a.sfl;
+  bool vector;
+  if (route == CCU_ROUTE_AUTO) {
+    vector = vec_ok;
+  } else if (route == CCU_ROUTE_SCALAR) {
+    vector = false;
+  } else if (route == CCU_ROUTE_VECTOR && vec_ok) {
+    vector = true;
+  } else if (route >= 0 && route < CCU_ROUTE_COUNT) {
+    return fail(CCU_ERR_NOT_IMPLEMENTED, "route '%s' does not serve these prefill arguments",
+                ccu_route_name(route));
+  } else {
+    return fail(CCU_ERR_INVALID_ARGUMENT, "unknown route %d", route);
+  }
+  f.chunk = prefill_chunk(a.B, vector ? a.D / 8 : a.D, a.T);
+  if (vector && (a.T + f.chunk - 1) / f.chunk > 65535) vector = false;
+  UpdateParams p = {};
+  p.x = static_cast<const uint16_t *>(a.x);
+  p.w = static_cast<const uint16_t *>(a.w);
+  p.bias = static_cast<const uint16_t *>(a.bias);
+  p.out = static_cast<uint16_t *>(const_cast<void *>(a.out));
+  p.D = a.D;
+  p.L = a.L;
+  cudaError_t e = launch_prefill(p, f, a.act, vector, stream);
+  if (e != cudaSuccess)
+    return fail(CCU_ERR_CUDA, "launch of the prefill kernel failed: %s", cudaGetErrorString(e));
+  return CCU_OK;
+}
+
 }  // namespace
 
 void record_error(const char *msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
@@ -438,6 +531,25 @@ ccu_status_t ccu_conv1d_update_multi(const void *x, int64_t x_stride_n, int64_t 
   m.sot = out_stride_t;
   m.inter = intermediate_states;
   return ccu::run_multi(m, route, reinterpret_cast<cudaStream_t>(stream));
+}
+
+ccu_status_t ccu_causal_conv1d_fwd(const void *x, int64_t x_stride_b, int64_t x_stride_d,
+                                   int64_t x_stride_t, const void *weight, const void *bias,
+                                   ccu_act_t act, const void *initial_states, int64_t init_stride_b,
+                                   int64_t init_stride_d, int64_t init_stride_l, int64_t B, int64_t D,
+                                   int64_t T, int64_t L, int64_t W, void *out, int64_t out_stride_b,
+                                   int64_t out_stride_d, int64_t out_stride_t, void *final_states,
+                                   int64_t final_stride_b, int64_t final_stride_d,
+                                   int64_t final_stride_l, int32_t route, ccu_stream_t stream) {
+  ccu::PrefillArgs a;
+  a.x = x; a.w = weight; a.bias = bias; a.init = initial_states; a.out = out; a.fin = final_states;
+  a.act = (int)act;
+  a.sxb = x_stride_b; a.sxd = x_stride_d; a.sxt = x_stride_t;
+  a.sib = init_stride_b; a.sid = init_stride_d; a.sil = init_stride_l;
+  a.sob = out_stride_b; a.sod = out_stride_d; a.sot = out_stride_t;
+  a.sfb = final_stride_b; a.sfd = final_stride_d; a.sfl = final_stride_l;
+  a.B = B; a.D = D; a.T = T; a.L = L; a.W = W;
+  return ccu::run_prefill(a, route, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int64_t ccu_conv1d_check_indices_scratch_bytes(int64_t S) {

@@ -41,6 +41,18 @@ struct MultiParams {
   uint16_t *inter;
 };
 
+// The arguments of the full-sequence prefill beyond UpdateParams (x, w, bias, out, D, L):
+// x / out [B, D, T] and the optional initial / final states [B, D, L] by element strides.
+struct PrefillParams {
+  int64_t B, T, chunk;  // chunk: tokens per thread
+  int64_t sxb, sxd, sxt;
+  int64_t sob, sod, sot;
+  const uint16_t *init;  // nullptr: the inputs before the sequence are zero
+  int64_t sib, sid, sil;
+  uint16_t *fin;         // nullptr: no final state
+  int64_t sfb, sfd, sfl;
+};
+
 // Launch description chosen on the host.
 struct LaunchShape {
   dim3 grid;
@@ -272,6 +284,8 @@ cudaError_t launch_multi_scalar(const UpdateParams &p, const MultiParams &m, int
                                 cudaStream_t stream);
 cudaError_t launch_multi_vector(const UpdateParams &p, const MultiParams &m, int act,
                                 cudaStream_t stream);
+cudaError_t launch_prefill(const UpdateParams &p, const PrefillParams &f, int act, bool vector,
+                           cudaStream_t stream);
 cudaError_t launch_check_indices(const int32_t *idx, int64_t N, int64_t S, uint32_t *bitmap,
                                  int32_t *status, cudaStream_t stream);
 

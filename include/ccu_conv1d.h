@@ -234,6 +234,43 @@ CCU_API ccu_status_t ccu_conv1d_update_multi(const void *x, int64_t x_stride_n, 
                                              int32_t *status_dev, int32_t route, ccu_stream_t stream);
 
 /*
+ * ccu_causal_conv1d_fwd -- full-sequence prefill: the causal depthwise convolution over T
+ * tokens of B sequences, and the final state the decode update continues from.
+ *
+ * The cuDNN page "Causal Conv1d Decode Update" sends full-sequence prefill to a separate
+ * causal_conv1d operation whose width-four final state the update accepts directly, the
+ * L = 3 state in the channel-last stride (3*D, 1, D) without a copy (introduction;
+ * "Semantic tensor contract"). The page does not define that operation; this is the
+ * update's definition applied to every token of a sequence:
+ *
+ *   out[b, d, t]  = act( sum_{j=0}^{3} weight[d, j] * xx(b, d, t - 3 + j) + bias[d] )
+ *   xx(b, d, t)   = x[b, d, t] for t >= 0, initial_states[b, d, L + t] for t < 0 (zero when
+ *                   initial_states is NULL)
+ *   final_states[b, d, l] = xx(b, d, T - L + l),  l = 0..L-1
+ *
+ * So running the decode update on final_states with the next token continues the same
+ * convolution. All tensors are device memory; element (b, d, t) of x is at
+ * x[b*x_stride_b + d*x_stride_d + t*x_stride_t] (any non-negative strides; channel-
+ * contiguous x and out -- stride_d == 1, the other strides multiples of 8 -- run the vector
+ * kernel), and likewise for out, initial_states (b, d, l) and final_states (b, d, l). For the
+ * hand-off layout pass final strides (L*D, 1, D). initial_states and final_states may be
+ * NULL; final_states must not overlap initial_states, x or out, and out must not overlap x.
+ * W must be 4 (CCU_ERR_NOT_IMPLEMENTED otherwise) and L >= W - 1. B, D or T == 0 is a
+ * no-op. route: CCU_ROUTE_AUTO, CCU_ROUTE_SCALAR or CCU_ROUTE_VECTOR.
+ * Returns as ccu_conv1d_update.
+ */
+CCU_API ccu_status_t ccu_causal_conv1d_fwd(const void *x, int64_t x_stride_b, int64_t x_stride_d,
+                                           int64_t x_stride_t, const void *weight, const void *bias,
+                                           ccu_act_t act, const void *initial_states,
+                                           int64_t init_stride_b, int64_t init_stride_d,
+                                           int64_t init_stride_l, int64_t B, int64_t D, int64_t T,
+                                           int64_t L, int64_t W, void *out, int64_t out_stride_b,
+                                           int64_t out_stride_d, int64_t out_stride_t,
+                                           void *final_states, int64_t final_stride_b,
+                                           int64_t final_stride_d, int64_t final_stride_l,
+                                           int32_t route, ccu_stream_t stream);
+
+/*
  * ccu_conv1d_check_indices -- validate a slot-index vector on the device without trapping.
  *
  * Checks the two preconditions of the conv_state_indices paragraph of "Causal Conv1d

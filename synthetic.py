@@ -99,6 +99,29 @@ MULTI_WORKLOADS = {
     ]
 }
 
+# Full-sequence prefill: B sequences of T tokens (x token-major [B, T, D]), final state
+# L = 3 in the channel-last layout the decode update continues from.
+PREFILL_WORKLOADS = {
+    "prefill_b8_t4096_d4096_bias_silu": dict(B=8, T=4096, D=4096, L=3, W=4, act="silu", bias_std=0.1,
+                                             seed=0),
+}
+
+
+def generate_prefill(spec: dict):
+    """x [B, T, D], weight [D, W], bias [D] as BF16 bits, drawn in that order."""
+    rng = np.random.Generator(np.random.PCG64(spec["seed"]))
+    x = _draw(rng, ("normal", 1.0), spec["B"] * spec["T"] * spec["D"]).reshape(spec["B"], spec["T"], spec["D"])
+    weight = _draw(rng, ("normal", 1.0), spec["D"] * spec["W"]).reshape(spec["D"], spec["W"])
+    bias = _draw(rng, ("normal", spec["bias_std"]), spec["D"]) if spec["bias_std"] is not None else None
+    return x, weight, bias
+
+
+def prefill_bytes(spec: dict) -> int:
+    """x read + out write (2 B each per element), final state written, weight and bias read."""
+    B, T, D, L, W = spec["B"], spec["T"], spec["D"], spec["L"], spec["W"]
+    return B * T * D * 4 + B * D * L * 2 + D * W * 2 + (D * 2 if spec["bias_std"] is not None else 0)
+
+
 # The workload the benchmark times: the bandwidth-bound large-batch decode.
 BENCH_WORKLOAD = "large_n4096_d16384_l3_perm_pad5_silu"
 # The small page-shaped case used by the smoke run.

@@ -596,3 +596,90 @@ def test_multi_large_batch():
 
     assert np.array_equal(from_dev_u16(st), st_ref)
     assert bf16_ulp_distance(from_dev_u16(out.permute(0, 2, 1)).transpose(0, 2, 1), want_out).max() <= 1
+
+
+# ----------------------------------------------------------------------------- prefill
+
+PREFILL = [
+    dict(B=2, D=264, T=100, L=3, x_layout="tokens_major", init=None, fin="channel_last"),
+    dict(B=3, D=64, T=1, L=3, x_layout="tokens_major", init="compact", fin="channel_last"),
+    dict(B=1, D=128, T=2, L=5, x_layout="tokens_major", init="channel_last", fin="compact"),
+    dict(B=4, D=40, T=37, L=4, x_layout="channels_major", init="compact", fin="compact"),
+    dict(B=2, D=19, T=70, L=3, x_layout="tokens_major", init="compact", fin="channel_last"),
+    dict(B=2, D=2048, T=1030, L=3, x_layout="tokens_major", init="channel_last", fin="channel_last"),
+    dict(B=1, D=512, T=3, L=8, x_layout="tokens_major", init="compact", fin=None),
+]
+
+
+def _state_dev(arr_bdl, layout):
+    """[B, D, L] numpy -> device tensor [B, D, L] in the given layout."""
+    if layout == "compact":
+        return to_dev_u16(arr_bdl, DEV)
+    return to_dev_u16(np.ascontiguousarray(np.transpose(arr_bdl, (0, 2, 1))), DEV).permute(0, 2, 1)
+
+
+@pytest.mark.parametrize("route", ["auto", "scalar", "vector"])
+@pytest.mark.parametrize("act", ["identity", "silu"])
+@pytest.mark.parametrize("ci", range(len(PREFILL)))
+def test_prefill(route, act, ci):
+    import depthwise_causal_conv1d_gb300 as ccu
+
+    c = PREFILL[ci]
+    B, D, T, L = c["B"], c["D"], c["T"], c["L"]
+    if route == "vector" and (D % 8 or c["x_layout"] != "tokens_major"):
+        pytest.skip("the vector kernel needs channel-contiguous 16-byte token rows")
+    rng = np.random.default_rng(500 + ci)
+    x_btd = synthetic.f64_to_bf16_bits(rng.standard_normal((B, T, D)))
+    weight = synthetic.f64_to_bf16_bits(rng.standard_normal((D, 4)) * 0.5)
+    bias = synthetic.f64_to_bf16_bits(rng.standard_normal(D) * 0.1)
+    init = synthetic.f64_to_bf16_bits(rng.standard_normal((B, D, L))) if c["init"] else None
+    want_y, want_fin = [], []
+    for b in range(B):
+        y, fin = oracle.full_causal_conv(x_btd[b], weight, bias, act, None if init is None else init[b], L)
+        want_y.append(y.T)  # [D, T]
+        want_fin.append(fin)
+    want_y, want_fin = np.stack(want_y), np.stack(want_fin)
+    if c["x_layout"] == "tokens_major":
+        x = to_dev_u16(x_btd, DEV).permute(0, 2, 1)
+    else:
+        x = to_dev_u16(np.ascontiguousarray(np.transpose(x_btd, (0, 2, 1))), DEV)
+    init_dev = _state_dev(init, c["init"]) if init is not None else None
+    fin_dev = None
+    if c["fin"] is not None:
+        fin_dev = _state_dev(np.zeros((B, D, L), np.uint16), c["fin"])
+    res = ccu.causal_conv1d_fwd(x, to_dev_u16(weight, DEV), to_dev_u16(bias, DEV), act,
+                                initial_states=init_dev, final_states_out=fin_dev, route=route)
+    out = res[0] if isinstance(res, tuple) else res
+    torch.cuda.synchronize()
+    from oracle_pins import bf16_ulp_distance
+
+    got_y = from_dev_u16(out)
+    assert bf16_ulp_distance(got_y, want_y).max() <= (0 if act == "identity" else 1)
+    if fin_dev is not None:
+        assert np.array_equal(from_dev_u16(fin_dev), want_fin)
+
+
+def test_prefill_hands_off_to_decode():
+    """Prefill T tokens, hand the channel-last L=3 final state to the decode update for K
+    more tokens: the outputs equal one convolution over all T + K tokens."""
+    import depthwise_causal_conv1d_gb300 as ccu
+
+    rng = np.random.default_rng(9)
+    B, D, T, K = 4, 1024, 200, 5
+    x_all = synthetic.f64_to_bf16_bits(rng.standard_normal((B, T + K, D)))
+    weight = synthetic.f64_to_bf16_bits(rng.standard_normal((D, 4)) * 0.5)
+    bias = synthetic.f64_to_bf16_bits(rng.standard_normal(D) * 0.1)
+    w, b = to_dev_u16(weight, DEV), to_dev_u16(bias, DEV)
+    x_pre = to_dev_u16(np.ascontiguousarray(x_all[:, :T]), DEV).permute(0, 2, 1)
+    y_pre, state = ccu.causal_conv1d_fwd(x_pre, w, b, "silu", return_final_states=True)
+    assert state.stride() == (3 * D, 1, D)  # the layout the decode update takes without a copy
+    ys = [from_dev_u16(y_pre)]
+    for k in range(K):
+        xt = to_dev_u16(np.ascontiguousarray(x_all[:, T + k]), DEV)
+        ys.append(from_dev_u16(ccu.causal_conv1d_update(xt, state, w, b, "silu"))[:, :, None])
+    got = np.concatenate(ys, axis=2)
+    from oracle_pins import bf16_ulp_distance
+
+    for bb in range(B):
+        want, _ = oracle.full_causal_conv(x_all[bb], weight, bias, "silu", None, 3)
+        assert bf16_ulp_distance(got[bb], want.T).max() <= 1
