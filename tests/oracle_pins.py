@@ -436,9 +436,73 @@ def pin_multi_vs_full(lib):
     assert np.array_equal(out[0].T, y) and np.array_equal(st[0], fin)
 
 
+def pin_widths_one_hot_and_chain(lib):
+    # W = 2 and 3 (the page's other "semantically valid widths"), L from W - 1 up: one-hot
+    # weights reproduce x delayed by W-1-k steps; a chain of updates equals the direct
+    # convolution; the direct convolution equals numpy.convolve within the FP32 bound.
+    rng = np.random.default_rng(16)
+    for W in (2, 3):
+        for L in (W - 1, W, 5):
+            D, T = 6, 9
+            x_seq = rand_bf16(rng, (T, D))
+            init = rand_bf16(rng, (D, L))
+            for k in range(W):
+                weight = np.zeros((D, W), np.uint16)
+                weight[:, k] = 0x3F80
+                y, _ = _chain(lib, x_seq, weight, None, "identity", init, L)
+                for t in range(T):
+                    src = t - (W - 1 - k)
+                    want = x_seq[src] if src >= 0 else init[:, L + src]
+                    assert np.array_equal(f32(y[t]), f32(want)), f"one-hot W={W} L={L} k={k} t={t}"
+            weight = rand_bf16(rng, (D, W), 0.5)
+            bias = rand_bf16(rng, (D,), 0.1)
+            y_chain, st_chain = _chain(lib, x_seq, weight, bias, "silu", init, L)
+            y_full, st_full, acc = oracle.full_causal_conv(x_seq, weight, bias, "silu", init, L,
+                                                           with_acc=True, lib=lib)
+            assert np.array_equal(y_chain, y_full) and np.array_equal(st_chain, st_full), f"W={W} L={L}"
+            for d in range(D):
+                xx = np.concatenate([f32(init[d, L - (W - 1):]) if W > 1 else np.zeros(0),
+                                     f32(x_seq[:, d])])
+                exact = np.convolve(xx, f32(weight[d, ::-1]), mode="valid") + f32(bias[d:d + 1])[0]
+                mag = np.convolve(np.abs(xx), np.abs(f32(weight[d, ::-1])), mode="valid") + abs(
+                    f32(bias[d:d + 1])[0])
+                assert np.all(np.abs(acc[:, d] - exact) <= W * U24 * mag * (1 + 1e-6) + 1e-45)
+
+
+def pin_widths_multi_and_ring(lib):
+    # The multi-token and ring forms at W = 2, 3 equal the single-token linear steps.
+    rng = np.random.default_rng(17)
+    for W, L, T in [(2, 1, 3), (3, 2, 4), (2, 3, 2), (3, 5, 6)]:
+        N, D, S = 3, 5, 4
+        x = rand_bf16(rng, (N, T, D))
+        weight = rand_bf16(rng, (D, W))
+        state = rand_bf16(rng, (S, D, L))
+        idx = np.array([3, -1, 0], np.int32)
+        st_multi = state.copy()
+        out = oracle.conv1d_update_multi(x, (T * D, 1, D), st_multi, (D * L, L, 1), weight, None,
+                                         "identity", idx, None, N, D, T, S, L, W, lib=lib)
+        st_seq = state.copy()
+        for t in range(T):
+            o = oracle.conv1d_update(np.ascontiguousarray(x[:, t]), D, st_seq, (D * L, L, 1), weight,
+                                     None, "identity", idx, N, D, S, L, W, lib=lib)
+            assert np.array_equal(out[:, :, t], o), f"W={W} L={L} token {t}"
+        assert np.array_equal(st_multi, st_seq)
+        ring = state.copy()
+        seq = np.array([L + 1, 0, 7], np.int32)
+        out_r = oracle.conv1d_update_circular(np.ascontiguousarray(x[:, 0]), D, ring, (D * L, L, 1),
+                                              weight, None, "identity", idx, seq, N, D, S, L, W, lib=lib)
+        lin = state.copy()
+        for n, s in enumerate(idx):
+            if s >= 0:
+                lin[s] = _rotate(state[s], int(seq[n]) % L)
+        out_l = oracle.conv1d_update(np.ascontiguousarray(x[:, 0]), D, lin, (D * L, L, 1), weight, None,
+                                     "identity", idx, N, D, S, L, W, lib=lib)
+        assert np.array_equal(out_r, out_l), f"ring W={W} L={L}"
+
+
 ALL_PINS = [pin_golden, pin_bf16_conversion, pin_silu, pin_one_hot, pin_chain_vs_full,
             pin_full_vs_convolve, pin_closed_form, pin_padding_and_untouched, pin_routing,
             pin_layouts, pin_padded_ld, pin_check_indices,
             pin_circular_equals_linear_through_rotation, pin_circular_writes_one_entry,
             pin_circular_chain_vs_full, pin_multi_equals_sequential_steps, pin_multi_x_layouts,
-            pin_multi_vs_full]
+            pin_multi_vs_full, pin_widths_one_hot_and_chain, pin_widths_multi_and_ring]
