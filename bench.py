@@ -464,7 +464,8 @@ def per_workload_table(dev, stream, reps=50):
 
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
     rows = {}
-    for name, wl in {**synthetic.WORKLOADS, **synthetic.RING_WORKLOADS}.items():
+    for name, wl in {**synthetic.WORKLOADS, **synthetic.RING_WORKLOADS,
+                     **synthetic.WIDTH_WORKLOADS}.items():
         inp = synthetic.generate(wl)
         res = Resident(inp, dev, stream, layout=wl.layout)
         nbytes = synthetic.algorithmic_bytes(wl, inp.indices)
@@ -507,7 +508,7 @@ def per_workload_table(dev, stream, reps=50):
         torch.cuda.synchronize()
         graph_us = g0.elapsed_time(g1) * 1e3 / 2000
         rows[name] = {"N_x_D": wl.N * wl.D, "bytes": nbytes, "route": res.route_name,
-                      "state": f"{'ring' if wl.ring else 'linear'} {wl.layout}",
+                      "state": f"{'ring' if wl.ring else 'linear'} {wl.layout}", "W": wl.W, "L": wl.L,
                       "eager_us": round(eager_us, 3), "graph_us": round(graph_us, 3),
                       "cold_us": round(cold_us, 3),
                       "cold_GBps": round(nbytes / (cold_us * 1e-6) / 1e9, 1),

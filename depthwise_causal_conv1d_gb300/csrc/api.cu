@@ -64,8 +64,8 @@ ccu_status_t validate(const Args &a, bool *noop, Layout *layout) {
   if (a.L < a.W - 1)
     return fail(CCU_ERR_INVALID_ARGUMENT, "L must be >= W - 1 (L=%lld, W=%lld)", (long long)a.L,
                 (long long)a.W);
-  if (a.W != kW)
-    return fail(CCU_ERR_NOT_IMPLEMENTED, "only width W == 4 is served, got W=%lld",
+  if (a.W < 2 || a.W > kW)
+    return fail(CCU_ERR_NOT_IMPLEMENTED, "widths W = 2, 3 and 4 are served, got W=%lld",
                 (long long)a.W);
   if (a.status != nullptr && !aligned(a.status, 4))
     return fail(CCU_ERR_INVALID_ARGUMENT, "status word must be 4-byte aligned");
@@ -115,7 +115,7 @@ bool route_serves(int route, const Args &a, Layout /*layout*/) {
     case CCU_ROUTE_SCALAR: return true;
     case CCU_ROUTE_VECTOR: return vec8 && a.L <= kVectorMaxL;
     case CCU_ROUTE_STAGED: return vec8 && a.L <= kStagedMaxL;
-    case CCU_ROUTE_BULK: return vec8 && a.L <= kVectorMaxL;
+    case CCU_ROUTE_BULK: return vec8 && a.L <= kVectorMaxL && a.W == kW;
     default: return false;
   }
 }
@@ -192,6 +192,7 @@ ccu_status_t run(const Args &a, int route, cudaStream_t stream) {
   p.D = a.D;
   p.S = a.S;
   p.L = a.L;
+  p.W = a.W;
   p.ss = a.ss;
   p.sd = a.sd;
   p.sl = a.sl;
@@ -232,8 +233,8 @@ ccu_status_t validate_multi(const MultiArgs &m, bool *noop, Layout *layout) {
   if (a.L < a.W - 1)
     return fail(CCU_ERR_INVALID_ARGUMENT, "L must be >= W - 1 (L=%lld, W=%lld)", (long long)a.L,
                 (long long)a.W);
-  if (a.W != kW)
-    return fail(CCU_ERR_NOT_IMPLEMENTED, "only width W == 4 is served, got W=%lld",
+  if (a.W < 2 || a.W > kW)
+    return fail(CCU_ERR_NOT_IMPLEMENTED, "widths W = 2, 3 and 4 are served, got W=%lld",
                 (long long)a.W);
   if (a.status != nullptr && !aligned(a.status, 4))
     return fail(CCU_ERR_INVALID_ARGUMENT, "status word must be 4-byte aligned");
@@ -277,8 +278,8 @@ ccu_status_t validate_multi(const MultiArgs &m, bool *noop, Layout *layout) {
 // The vector multi-token kernel moves 8 channels of one token as one 16-byte vector.
 bool multi_vector_serves(const MultiArgs &m) {
   const Args &a = m.a;
-  return a.D % 8 == 0 && a.L <= kVectorMaxL && m.sxd == 1 && m.sod == 1 && m.sxn % 8 == 0 &&
-         m.sxt % 8 == 0 && m.son % 8 == 0 && m.sot % 8 == 0;
+  return a.D % 8 == 0 && a.L <= kVectorMaxL && a.W == kW && m.sxd == 1 && m.sod == 1 &&
+         m.sxn % 8 == 0 && m.sxt % 8 == 0 && m.son % 8 == 0 && m.sot % 8 == 0;
 }
 
 ccu_status_t run_multi(const MultiArgs &m, int route, cudaStream_t stream) {
@@ -312,6 +313,7 @@ ccu_status_t run_multi(const MultiArgs &m, int route, cudaStream_t stream) {
   p.D = a.D;
   p.S = a.S;
   p.L = a.L;
+  p.W = a.W;
   p.ss = a.ss;
   p.sd = a.sd;
   p.sl = a.sl;
@@ -365,8 +367,8 @@ ccu_status_t run_prefill(const PrefillArgs &a, int route, cudaStream_t stream) {
   if (a.L < a.W - 1)
     return fail(CCU_ERR_INVALID_ARGUMENT, "L must be >= W - 1 (L=%lld, W=%lld)", (long long)a.L,
                 (long long)a.W);
-  if (a.W != kW)
-    return fail(CCU_ERR_NOT_IMPLEMENTED, "only width W == 4 is served, got W=%lld",
+  if (a.W < 2 || a.W > kW)
+    return fail(CCU_ERR_NOT_IMPLEMENTED, "widths W = 2, 3 and 4 are served, got W=%lld",
                 (long long)a.W);
   if (a.B == 0 || a.D == 0 || a.T == 0) return CCU_OK;
   const int64_t strides[] = {a.sxb, a.sxd, a.sxt, a.sib, a.sid, a.sil, a.sob, a.sod, a.sot,
@@ -386,7 +388,7 @@ ccu_status_t run_prefill(const PrefillArgs &a, int route, cudaStream_t stream) {
   if (!mul_le(a.B, a.D, lim) || !mul_le(a.B * a.D, a.T, lim) || !mul_le(a.B * a.D, a.L, lim))
     return fail(CCU_ERR_INVALID_ARGUMENT, "tensor sizes overflow 64-bit indexing");
 
-  const bool vec_ok = a.D % 8 == 0 && a.sxd == 1 && a.sod == 1 && a.sxb % 8 == 0 &&
+  const bool vec_ok = a.D % 8 == 0 && a.W == kW && a.sxd == 1 && a.sod == 1 && a.sxb % 8 == 0 &&
                       a.sxt % 8 == 0 && a.sob % 8 == 0 && a.sot % 8 == 0 && a.B <= 65535;
   PrefillParams f;
   f.B = a.B;
@@ -419,6 +421,7 @@ ccu_status_t run_prefill(const PrefillArgs &a, int route, cudaStream_t stream) {
   p.out = static_cast<uint16_t *>(const_cast<void *>(a.out));
   p.D = a.D;
   p.L = a.L;
+  p.W = a.W;
   cudaError_t e = launch_prefill(p, f, a.act, vector, stream);
   if (e != cudaSuccess)
     return fail(CCU_ERR_CUDA, "launch of the prefill kernel failed: %s", cudaGetErrorString(e));

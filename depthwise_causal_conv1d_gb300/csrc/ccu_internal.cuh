@@ -10,7 +10,8 @@
 
 namespace ccu {
 
-// Filter width served by the kernels ("Current native implementation": width four).
+// The widest filter served (the page's native width, "Current native implementation");
+// widths 2 and 3 are served too. Kernels tuned for the large batch are width four only.
 constexpr int kW = 4;
 
 enum class Layout : int { Compact = 0, ChannelLast = 1 };
@@ -26,7 +27,7 @@ struct UpdateParams {
   const int32_t *seqlens; // [N] cache_seqlens (ring-buffer state) or nullptr (linear state)
   uint16_t *out;          // [N, D]
   int32_t *status;        // nullptr: unchecked; else device error word (range check on)
-  int64_t N, D, S, L;
+  int64_t N, D, S, L, W;  // W: filter width (2, 3 or 4)
   int64_t ss, sd, sl;     // element strides of the state (used by the scalar kernel)
   int layout;             // Layout
   int rows_per_cta;       // rows each CTA walks (vector kernels)
@@ -129,10 +130,11 @@ __device__ __forceinline__ uint32_t get16(const uint32_t *w, int pos) {
 
 // The update of 8 consecutive channels whose compact state [8][L] sits in 4*L words `ow`
 // (two BF16 per word, flat position c*L + l) and whose inputs sit in 4 words `xw`:
-//   out[c]      = act(sum_j h_c[L-3+j] * w[c][j] + bias[c]),  h_c = (state[c][0..L-1], x[c])
+//   out[c]      = act(sum_{j<W} h_c[L+1-W+j] * w[c][j] + bias[c]),  h_c = (state[c][0..L-1], x[c])
 //   new state   = state[c][1..L-1] followed by x[c]   (written to `nw`, same packing)
-// `wv` holds weight[8][4] (16 words), `bv` bias[8] (4 words). Returns the packed outputs.
-template <int L, int ACT>
+// `wv` holds weight[8][W] (4*W of its 16 words), `bv` bias[8] (4 words). Returns the
+// packed outputs.
+template <int L, int W, int ACT>
 __device__ __forceinline__ uint4 update8_compact(const uint32_t (&xw)[4], const uint32_t (&ow)[4 * L],
                                                  const uint32_t (&wv)[16], const uint32_t (&bv)[4],
                                                  bool has_bias, uint32_t (&nw)[4 * L]) {
@@ -141,10 +143,10 @@ __device__ __forceinline__ uint4 update8_compact(const uint32_t (&xw)[4], const 
   for (int c = 0; c < 8; ++c) {
     float acc = 0.0f;
 #pragma unroll
-    for (int j = 0; j < kW; ++j) {
-      const int hidx = L - (kW - 1) + j;  // index into the L + 1 history entries
+    for (int j = 0; j < W; ++j) {
+      const int hidx = L - (W - 1) + j;  // index into the L + 1 history entries
       const uint32_t h = (hidx == L) ? get16(xw, c) : get16(ow, c * L + hidx);
-      acc = __fmaf_rn(bf16_bits(h), bf16_bits(get16(wv, c * kW + j)), acc);
+      acc = __fmaf_rn(bf16_bits(h), bf16_bits(get16(wv, c * W + j)), acc);
     }
     if (has_bias) acc = acc + bf16_bits(get16(bv, c));
     y[c] = activate<ACT>(acc);
@@ -189,9 +191,9 @@ __device__ __forceinline__ RowSlot resolve_row(const UpdateParams &p, int64_t n)
 // The ring-buffer form of update8_compact for a ring position Q known at compile time:
 // the 8 channels' rings sit in `ow` (flat position c*L + l) and Q is the ring position of
 // the oldest entry. The history, oldest first, is ring[Q], ring[Q+1], ..., ring[Q+L-1]
-// (mod L) followed by x, so the width-4 window is ring[(Q+L-3) % L], ring[(Q+L-2) % L],
-// ring[(Q+L-1) % L], x. The new rings in `nw` equal the old ones with entry Q replaced by x.
-template <int L, int ACT, int Q>
+// (mod L) followed by x, so the width-W window is ring[(Q+L-(W-1)+k) % L] for
+// k = 0..W-2, then x. The new rings in `nw` equal the old ones with entry Q replaced by x.
+template <int L, int W, int ACT, int Q>
 __device__ __forceinline__ uint4 update8_ring_q(const uint32_t (&xw)[4], const uint32_t (&ow)[4 * L],
                                                 const uint32_t (&wv)[16], const uint32_t (&bv)[4],
                                                 bool has_bias, uint32_t (&nw)[4 * L]) {
@@ -200,11 +202,11 @@ __device__ __forceinline__ uint4 update8_ring_q(const uint32_t (&xw)[4], const u
   for (int c = 0; c < 8; ++c) {
     float acc = 0.0f;
 #pragma unroll
-    for (int k = 0; k < kW - 1; ++k) {
-      const uint32_t h = get16(ow, c * L + (Q + L - (kW - 1) + k) % L);
-      acc = __fmaf_rn(bf16_bits(h), bf16_bits(get16(wv, c * kW + k)), acc);
+    for (int k = 0; k < W - 1; ++k) {
+      const uint32_t h = get16(ow, c * L + (Q + L - (W - 1) + k) % L);
+      acc = __fmaf_rn(bf16_bits(h), bf16_bits(get16(wv, c * W + k)), acc);
     }
-    acc = __fmaf_rn(bf16_bits(get16(xw, c)), bf16_bits(get16(wv, c * kW + kW - 1)), acc);
+    acc = __fmaf_rn(bf16_bits(get16(xw, c)), bf16_bits(get16(wv, c * W + W - 1)), acc);
     if (has_bias) acc = acc + bf16_bits(get16(bv, c));
     y[c] = activate<ACT>(acc);
   }
@@ -221,24 +223,25 @@ __device__ __forceinline__ uint4 update8_ring_q(const uint32_t (&xw)[4], const u
 
 // Runtime ring position q in [0, L): one branch to the matching compile-time form (q is
 // the same for every lane of a row, so the branch does not diverge within a row).
-template <int L, int ACT>
+template <int L, int W, int ACT>
 __device__ __forceinline__ uint4 update8_compact_ring(const uint32_t (&xw)[4], const uint32_t (&ow)[4 * L],
                                                       const uint32_t (&wv)[16], const uint32_t (&bv)[4],
                                                       bool has_bias, int q, uint32_t (&nw)[4 * L]) {
   switch (q) {
-    case 0: return update8_ring_q<L, ACT, 0>(xw, ow, wv, bv, has_bias, nw);
-    case 1: return update8_ring_q<L, ACT, 1 % L>(xw, ow, wv, bv, has_bias, nw);
-    case 2: return update8_ring_q<L, ACT, 2 % L>(xw, ow, wv, bv, has_bias, nw);
-    case 3: return update8_ring_q<L, ACT, 3 % L>(xw, ow, wv, bv, has_bias, nw);
-    case 4: return update8_ring_q<L, ACT, 4 % L>(xw, ow, wv, bv, has_bias, nw);
-    case 5: return update8_ring_q<L, ACT, 5 % L>(xw, ow, wv, bv, has_bias, nw);
-    case 6: return update8_ring_q<L, ACT, 6 % L>(xw, ow, wv, bv, has_bias, nw);
-    default: return update8_ring_q<L, ACT, 7 % L>(xw, ow, wv, bv, has_bias, nw);
+    case 0: return update8_ring_q<L, W, ACT, 0>(xw, ow, wv, bv, has_bias, nw);
+    case 1: return update8_ring_q<L, W, ACT, 1 % L>(xw, ow, wv, bv, has_bias, nw);
+    case 2: return update8_ring_q<L, W, ACT, 2 % L>(xw, ow, wv, bv, has_bias, nw);
+    case 3: return update8_ring_q<L, W, ACT, 3 % L>(xw, ow, wv, bv, has_bias, nw);
+    case 4: return update8_ring_q<L, W, ACT, 4 % L>(xw, ow, wv, bv, has_bias, nw);
+    case 5: return update8_ring_q<L, W, ACT, 5 % L>(xw, ow, wv, bv, has_bias, nw);
+    case 6: return update8_ring_q<L, W, ACT, 6 % L>(xw, ow, wv, bv, has_bias, nw);
+    default: return update8_ring_q<L, W, ACT, 7 % L>(xw, ow, wv, bv, has_bias, nw);
   }
 }
 
-// Outputs of 8 channels from the three window entries (h[k][c]) and x (xs[c]).
-template <int ACT>
+// Outputs of 8 channels from the W-1 window entries before x (h[k][c], k < W-1) and x
+// (xs[c]); weight[8][W] packed in wv.
+template <int W, int ACT>
 __device__ __forceinline__ uint4 outputs8_window(const uint32_t (&h)[3][8], const uint32_t (&xs)[8],
                                                  const uint32_t (&wv)[16], const uint32_t (&bv)[4],
                                                  bool has_bias) {
@@ -247,14 +250,27 @@ __device__ __forceinline__ uint4 outputs8_window(const uint32_t (&h)[3][8], cons
   for (int c = 0; c < 8; ++c) {
     float acc = 0.0f;
 #pragma unroll
-    for (int k = 0; k < kW - 1; ++k)
-      acc = __fmaf_rn(bf16_bits(h[k][c]), bf16_bits(get16(wv, c * kW + k)), acc);
-    acc = __fmaf_rn(bf16_bits(xs[c]), bf16_bits(get16(wv, c * kW + kW - 1)), acc);
+    for (int k = 0; k < W - 1; ++k)
+      acc = __fmaf_rn(bf16_bits(h[k][c]), bf16_bits(get16(wv, c * W + k)), acc);
+    acc = __fmaf_rn(bf16_bits(xs[c]), bf16_bits(get16(wv, c * W + W - 1)), acc);
     if (has_bias) acc = acc + bf16_bits(get16(bv, c));
     y[c] = activate<ACT>(acc);
   }
   return make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
                     pack_bf16x2(y[6], y[7]));
+}
+
+// Load weight[c0 .. c0+7, 0..W-1]: 8*W BF16 = W 16-byte vectors, packed two per word.
+template <int W>
+__device__ __forceinline__ void load_weights_packed(const uint16_t *w, int64_t c0, uint32_t (&wv)[16]) {
+  const uint16_t *wp = w + c0 * W;
+#pragma unroll
+  for (int k = 0; k < W; ++k) {
+    const uint4 t = __ldg(reinterpret_cast<const uint4 *>(wp + 8 * k));
+    wv[4 * k] = t.x; wv[4 * k + 1] = t.y; wv[4 * k + 2] = t.z; wv[4 * k + 3] = t.w;
+  }
+#pragma unroll
+  for (int k = W; k < 4; ++k) wv[4 * k] = wv[4 * k + 1] = wv[4 * k + 2] = wv[4 * k + 3] = 0u;
 }
 
 // Unpack a 16-byte vector of 8 BF16 into 8 raw 16-bit values.

@@ -136,9 +136,9 @@ __global__ void __launch_bounds__(kThreads) k_update_bulk(UpdateParams p, int st
       }
       uint4 outv;
       if constexpr (RING) {
-        outv = update8_compact_ring<L, ACT>(xw, ow, wv[g], bv[g], has_bias, sl.q, nw);
+        outv = update8_compact_ring<L, kW, ACT>(xw, ow, wv[g], bv[g], has_bias, sl.q, nw);
       } else {
-        outv = update8_compact<L, ACT>(xw, ow, wv[g], bv[g], has_bias, nw);
+        outv = update8_compact<L, kW, ACT>(xw, ow, wv[g], bv[g], has_bias, nw);
       }
 #pragma unroll
       for (int q = 0; q < L; ++q) ss[q] = make_uint4(nw[4 * q], nw[4 * q + 1], nw[4 * q + 2], nw[4 * q + 3]);

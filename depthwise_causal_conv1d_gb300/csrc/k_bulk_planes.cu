@@ -149,12 +149,12 @@ __global__ void __launch_bounds__(kThreads) k_update_bulk_planes(UpdateParams p,
       }
       // Window buffers: the ring's three window planes, or the linear state's last three.
       constexpr int wb0 = RING ? 0 : NB - (kW - 1);
-      uint32_t h[kW - 1][8], xs[8];
+      uint32_t h[3][8], xs[8];
 #pragma unroll
       for (int j = 0; j < kW - 1; ++j)
         unpack8(reinterpret_cast<const uint4 *>(buf + (1 + wb0 + j) * kPlane)[q8], h[j]);
       unpack8(reinterpret_cast<const uint4 *>(buf)[q8], xs);
-      reinterpret_cast<uint4 *>(out_buf)[q8] = outputs8_window<ACT>(h, xs, wv[g], bv[g], has_bias);
+      reinterpret_cast<uint4 *>(out_buf)[q8] = outputs8_window<kW, ACT>(h, xs, wv[g], bv[g], has_bias);
     }
     fence_proxy_async();
     __syncwarp();

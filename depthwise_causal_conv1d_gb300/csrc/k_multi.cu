@@ -36,26 +36,28 @@ __global__ void __launch_bounds__(256) k_multi_scalar(UpdateParams p, MultiParam
     const bool ring = p.seqlens != nullptr;
     const int64_t q = ring ? r.q : 0;
     const uint16_t *xp = p.x + n * m.sxn + d * m.sxd;
-    const uint16_t *w = p.w + d * kW;
+    const int64_t W = p.W;
+    const uint16_t *w = p.w + d * W;
     // Entry k of the time-ordered history (k < L: state entry k, oldest first; else token
     // k - L), read before any of this channel's state is overwritten.
     auto hist = [&](int64_t k) -> uint16_t {
       if (k < L) return st[(ring ? (q + k) % L : k) * p.sl];
       return xp[(k - L) * m.sxt];
     };
-    uint16_t h0 = hist(L - 3), h1 = hist(L - 2), h2 = hist(L - 1);
+    // the W-1 window entries before the first token (newest last), in hw[3-(W-1) .. 2]
+    uint16_t hw[3] = {0, 0, 0};
+    for (int64_t k = 0; k < W - 1; ++k) hw[3 - (W - 1) + k] = hist(L - (W - 1) + k);
     for (int64_t t = 0; t < m.T; ++t) {
       const uint16_t xv = xp[t * m.sxt];
       float acc = 0.0f;
-      acc = __fmaf_rn(bf16_bits(h0), bf16_bits(w[0]), acc);
-      acc = __fmaf_rn(bf16_bits(h1), bf16_bits(w[1]), acc);
-      acc = __fmaf_rn(bf16_bits(h2), bf16_bits(w[2]), acc);
-      acc = __fmaf_rn(bf16_bits(xv), bf16_bits(w[3]), acc);
+      for (int64_t k = 0; k < W - 1; ++k)
+        acc = __fmaf_rn(bf16_bits(hw[3 - (W - 1) + k]), bf16_bits(w[k]), acc);
+      acc = __fmaf_rn(bf16_bits(xv), bf16_bits(w[W - 1]), acc);
       if (p.bias != nullptr) acc = acc + bf16_bits(p.bias[d]);
       p.out[n * m.son + d * m.sod + t * m.sot] = round_bf16(activate<ACT>(acc));
-      h0 = h1;
-      h1 = h2;
-      h2 = xv;
+      hw[0] = hw[1];
+      hw[1] = hw[2];
+      hw[2] = xv;
       if (m.inter != nullptr) {
         // the state after token t in its own order: history[t+1 .. t+L]; a ring holds the
         // entry of age (l - (q + t + 1)) mod L at position l
@@ -114,14 +116,7 @@ __global__ void __launch_bounds__(256) k_multi_vector(UpdateParams p, MultiParam
   if (g >= groups) return;
   const int64_t c0 = g << 3;
   uint32_t wv[16];
-  {
-    const uint16_t *wp = p.w + c0 * kW;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint4 t = ld_keep(wp + 8 * k);
-      wv[4 * k] = t.x; wv[4 * k + 1] = t.y; wv[4 * k + 2] = t.z; wv[4 * k + 3] = t.w;
-    }
-  }
+  load_weights_packed<kW>(p.w, c0, wv);
   const bool has_bias = p.bias != nullptr;
   uint32_t bv[4] = {0u, 0u, 0u, 0u};
   if (has_bias) {
@@ -179,9 +174,9 @@ __global__ void __launch_bounds__(256) k_multi_vector(UpdateParams p, MultiParam
         uint32_t nw[4 * L];
         uint4 outv;
         if constexpr (RING) {
-          outv = update8_compact_ring<L, ACT>(xg[k], ow, wv, bv, has_bias, (int)((row.q + t) % L), nw);
+          outv = update8_compact_ring<L, kW, ACT>(xg[k], ow, wv, bv, has_bias, (int)((row.q + t) % L), nw);
         } else {
-          outv = update8_compact<L, ACT>(xg[k], ow, wv, bv, has_bias, nw);
+          outv = update8_compact<L, kW, ACT>(xg[k], ow, wv, bv, has_bias, nw);
         }
         st_stream(orow + t * m.sot, outv);
 #pragma unroll

@@ -1,7 +1,7 @@
 // Full-sequence prefill: the causal depthwise convolution over T tokens per batch row,
 // and the final state that the decode update continues from.
 //
-//   y[b, d, t] = act( sum_{j=0}^{3} w[d, j] * xx(b, d, t - 3 + j) + bias[d] )
+//   y[b, d, t] = act( sum_{j=0}^{W-1} w[d, j] * xx(b, d, t - (W-1) + j) + bias[d] )
 //   xx(b, d, t) = x[b, d, t] for t >= 0; initial_states[b, d, L + t] for t < 0 (zero
 //                 when no initial state is given)
 //   final_states[b, d, l] = xx(b, d, T - L + l), l = 0..L-1
@@ -52,21 +52,22 @@ __global__ void __launch_bounds__(256) k_prefill_scalar(UpdateParams p, PrefillP
     const int64_t b = rest / chunks;
     const int64_t t0 = k * f.chunk;
     const int64_t t1 = t0 + f.chunk < f.T ? t0 + f.chunk : f.T;
-    const uint16_t *w = p.w + d * kW;
-    uint32_t h0 = input_at(p, f, b, d, t0 - 3), h1 = input_at(p, f, b, d, t0 - 2),
-             h2 = input_at(p, f, b, d, t0 - 1);
+    const int64_t W = p.W;
+    const uint16_t *w = p.w + d * W;
+    // the W-1 inputs before the chunk (newest last) in hw[3-(W-1) .. 2]
+    uint32_t hw[3] = {0u, 0u, 0u};
+    for (int64_t k = 0; k < W - 1; ++k) hw[3 - (W - 1) + k] = input_at(p, f, b, d, t0 - (W - 1) + k);
     for (int64_t t = t0; t < t1; ++t) {
       const uint32_t xv = p.x[b * f.sxb + d * f.sxd + t * f.sxt];
       float acc = 0.0f;
-      acc = __fmaf_rn(bf16_bits(h0), bf16_bits(w[0]), acc);
-      acc = __fmaf_rn(bf16_bits(h1), bf16_bits(w[1]), acc);
-      acc = __fmaf_rn(bf16_bits(h2), bf16_bits(w[2]), acc);
-      acc = __fmaf_rn(bf16_bits(xv), bf16_bits(w[3]), acc);
+      for (int64_t k = 0; k < W - 1; ++k)
+        acc = __fmaf_rn(bf16_bits(hw[3 - (W - 1) + k]), bf16_bits(w[k]), acc);
+      acc = __fmaf_rn(bf16_bits(xv), bf16_bits(w[W - 1]), acc);
       if (p.bias != nullptr) acc = acc + bf16_bits(p.bias[d]);
       p.out[b * f.sob + d * f.sod + t * f.sot] = round_bf16(activate<ACT>(acc));
-      h0 = h1;
-      h1 = h2;
-      h2 = xv;
+      hw[0] = hw[1];
+      hw[1] = hw[2];
+      hw[2] = xv;
     }
     if (f.fin != nullptr && t1 == f.T) write_final(p, f, b, d);
   }
@@ -82,8 +83,8 @@ __device__ __forceinline__ void widen8(const uint4 v, float (&f)[8]) {
   }
 }
 
-// 8 channels per thread; x and out channel-contiguous (one 16-byte vector per token).
-// The prefill moves 4 bytes per element, a quarter of the decode update's 16, so its
+// 8 channels per thread, width 4; x and out channel-contiguous (one 16-byte vector per
+// token). The prefill moves 4 bytes per element, a quarter of the decode update's 16, so its
 // arithmetic is kept lean: weights and bias are widened to floats once, the width-4 window
 // is kept as floats, and tokens go four at a time so the window slides by register
 // renaming; the next four tokens' loads are issued before the current four are computed

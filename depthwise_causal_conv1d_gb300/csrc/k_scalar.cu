@@ -1,5 +1,5 @@
-// Scalar kernels: the correctness anchor of the update (any D, any ld, any L >= 3, both
-// state layouts through explicit strides) and the index checker.
+// Scalar kernels: the correctness anchor of the update (any D, any ld, any W in 2..4 and
+// L >= W - 1, both state layouts through explicit strides) and the index checker.
 //
 // Update definition: cuDNN page "Causal Conv1d Decode Update", introduction (update
 // block) and the conv_state_indices paragraph.
@@ -11,7 +11,7 @@ int device_sm_count();
 
 namespace {
 
-// One thread per (row, channel), grid-stride. Each thread reads the three newest state
+// One thread per (row, channel), grid-stride. Each thread reads the W-1 newest state
 // entries and x, computes the output, then shifts its own channel's state in place.
 template <int ACT>
 __global__ void __launch_bounds__(256) k_update_scalar(UpdateParams p) {
@@ -29,17 +29,16 @@ __global__ void __launch_bounds__(256) k_update_scalar(UpdateParams p) {
     const int64_t L = p.L;
     const uint16_t xv = p.x[n * p.ld + d];
     // history = [st[0], ..., st[L-1], x] (linear), or the ring read from its oldest entry
-    // q followed by x; the width-4 window is the last four entries of the history.
+    // q followed by x; the width-W window is the last W entries of the history.
     const int64_t q = p.seqlens != nullptr ? r.q : 0;
-    const uint16_t h0 = st[((q + L - 3) % L) * p.sl];
-    const uint16_t h1 = st[((q + L - 2) % L) * p.sl];
-    const uint16_t h2 = st[((q + L - 1) % L) * p.sl];
-    const uint16_t *w = p.w + d * kW;
+    const int64_t W = p.W;
+    const uint16_t *w = p.w + d * W;
     float acc = 0.0f;
-    acc = __fmaf_rn(bf16_bits(h0), bf16_bits(w[0]), acc);
-    acc = __fmaf_rn(bf16_bits(h1), bf16_bits(w[1]), acc);
-    acc = __fmaf_rn(bf16_bits(h2), bf16_bits(w[2]), acc);
-    acc = __fmaf_rn(bf16_bits(xv), bf16_bits(w[3]), acc);
+    for (int64_t k = 0; k < W - 1; ++k) {
+      const uint16_t h = st[((q + L - (W - 1) + k) % L) * p.sl];
+      acc = __fmaf_rn(bf16_bits(h), bf16_bits(w[k]), acc);
+    }
+    acc = __fmaf_rn(bf16_bits(xv), bf16_bits(w[W - 1]), acc);
     if (p.bias != nullptr) acc = acc + bf16_bits(p.bias[d]);
     p.out[n * p.D + d] = round_bf16(activate<ACT>(acc));
     if (p.seqlens != nullptr) {

@@ -25,18 +25,19 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
+// weight[c0 .. c0+7, 0..W-1] (W 16-byte vectors) widened to floats wf[c][j], and the bias.
 __device__ __forceinline__ void load_weights8(const UpdateParams &p, int64_t c0, float (&wf)[8][kW],
                                               float (&bf)[8]) {
-  const uint16_t *wp = p.w + c0 * kW;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
+  const int W = (int)p.W;
+  const uint16_t *wp = p.w + c0 * W;
+  for (int k = 0; k < W; ++k) {
     const uint4 t = ld_keep(wp + 8 * k);
     const uint32_t v[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int e = 8 * k + 2 * i;
-      wf[e / kW][e % kW] = bf16_lo(v[i]);
-      wf[(e + 1) / kW][(e + 1) % kW] = bf16_hi(v[i]);
+      const int e = 8 * k + 2 * i;  // flat c*W + j of the low half
+      wf[e / W][e % W] = bf16_lo(v[i]);
+      wf[(e + 1) / W][(e + 1) % W] = bf16_hi(v[i]);
     }
   }
 #pragma unroll
@@ -52,18 +53,17 @@ __device__ __forceinline__ void load_weights8(const UpdateParams &p, int64_t c0,
   }
 }
 
+// Outputs of 8 channels from the W-1 window entries h[k][c] (k < W-1) and x.
 template <int ACT>
 __device__ __forceinline__ uint4 outputs8(const uint32_t (&h)[3][8], const uint32_t (&xs)[8],
                                           const float (&wf)[8][kW], const float (&bf)[8],
-                                          bool has_bias) {
+                                          bool has_bias, int W) {
   float y[8];
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
     float acc = 0.0f;
-    acc = __fmaf_rn(bf16_bits(h[0][c]), wf[c][0], acc);
-    acc = __fmaf_rn(bf16_bits(h[1][c]), wf[c][1], acc);
-    acc = __fmaf_rn(bf16_bits(h[2][c]), wf[c][2], acc);
-    acc = __fmaf_rn(bf16_bits(xs[c]), wf[c][3], acc);
+    for (int k = 0; k < W - 1; ++k) acc = __fmaf_rn(bf16_bits(h[k][c]), wf[c][k], acc);
+    acc = __fmaf_rn(bf16_bits(xs[c]), wf[c][W - 1], acc);
     if (has_bias) acc = acc + bf[c];
     y[c] = activate<ACT>(acc);
   }
@@ -109,21 +109,16 @@ __global__ void __launch_bounds__(256) k_update_staged_compact(UpdateParams p) {
 
     if (mine) {
       uint32_t h[3][8], xs[8];
+      const int W = (int)p.W;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         const int64_t base = (int64_t)(8 * tid + c) * L;
-        if (ring) {  // the window is the ring read from q: positions q+L-3 .. q+L-1 mod L
-          h[0][c] = s_state[base + (q + L - 3) % L];
-          h[1][c] = s_state[base + (q + L - 2) % L];
-          h[2][c] = s_state[base + (q + L - 1) % L];
-        } else {
-          h[0][c] = s_state[base + L - 3];
-          h[1][c] = s_state[base + L - 2];
-          h[2][c] = s_state[base + L - 1];
-        }
+        // the window: the last W-1 state entries (the ring read from q: q+L-W+1 .. q+L-1)
+        for (int k = 0; k < W - 1; ++k)
+          h[k][c] = s_state[base + (q + L - (W - 1) + k) % L];
         xs[c] = s_x[8 * tid + c];
       }
-      st_stream(outp, outputs8<ACT>(h, xs, wf, bf, has_bias));
+      st_stream(outp, outputs8<ACT>(h, xs, wf, bf, has_bias, W));
     }
 
     for (int64_t v = tid; v < nvec; v += T) {
@@ -183,20 +178,20 @@ __global__ void __launch_bounds__(256) k_update_staged_chlast(UpdateParams p) {
     }
     const uint4 xv = ld_stream(p.x + n * p.ld + c0);
     uint16_t *sp = p.state + s * (L * p.D) + c0;
+    const int W = (int)p.W;
+    uint32_t h[3][8], xs[8];
+    unpack8(xv, xs);
     if (p.seqlens != nullptr) {
-      // Ring in planes: read the three window planes, write x over the oldest plane.
+      // Ring in planes: read the W-1 window planes, write x over the oldest plane.
       const int64_t q = row.q;
-      uint32_t h[3][8], xs[8];
-#pragma unroll
-      for (int k = 0; k < 3; ++k) unpack8(ld_stream(sp + ((q + L - 3 + k) % L) * p.D), h[k]);
-      unpack8(xv, xs);
+      for (int k = 0; k < W - 1; ++k) unpack8(ld_stream(sp + ((q + L - (W - 1) + k) % L) * p.D), h[k]);
       st_stream(sp + q * p.D, xv);
-      st_stream(outp, outputs8<ACT>(h, xs, wf, bf, has_bias));
+      st_stream(outp, outputs8<ACT>(h, xs, wf, bf, has_bias, W));
       continue;
     }
-    // window planes L-3..L-1 (plane 0 is read only when L == 3: it is then in the window)
-    uint4 win[3];
-    if (L == kW - 1) win[0] = ld_stream(sp);
+    // Linear: plane l <- plane l+1, four planes in flight; the window planes L-W+1 .. L-1 are
+    // kept as they pass (plane 0 is read only when L == W - 1: it is then in the window).
+    if (L == W - 1) unpack8(ld_stream(sp), h[0]);
     for (int64_t l = 1; l < L; l += 4) {
       uint4 t[4];
 #pragma unroll
@@ -206,30 +201,13 @@ __global__ void __launch_bounds__(256) k_update_staged_chlast(UpdateParams p) {
       for (int k = 0; k < 4; ++k) {
         if (l + k < L) {
           st_stream(sp + (l + k - 1) * p.D, t[k]);
-          const int64_t wi = (l + k) - (L - 3);
-          if (wi >= 0 && wi < 3) win[wi] = t[k];
+          const int64_t wi = (l + k) - (L - (W - 1));
+          if (wi >= 0 && wi < W - 1) unpack8(t[k], h[wi]);
         }
       }
     }
     st_stream(sp + (L - 1) * p.D, xv);
-
-    uint32_t h[3][8], xs[8];
-    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-    for (int k = 0; k < 3; ++k) {
-      const uint32_t v[4] = {win[k].x, win[k].y, win[k].z, win[k].w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        h[k][2 * i] = v[i] & 0xffffu;
-        h[k][2 * i + 1] = v[i] >> 16;
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      xs[2 * i] = xw[i] & 0xffffu;
-      xs[2 * i + 1] = xw[i] >> 16;
-    }
-    st_stream(outp, outputs8<ACT>(h, xs, wf, bf, has_bias));
+    st_stream(outp, outputs8<ACT>(h, xs, wf, bf, has_bias, W));
   }
 }
 

@@ -23,25 +23,18 @@ __device__ __forceinline__ constexpr int elem_pos(int c, int l) {
   return LAYOUT == (int)Layout::Compact ? c * L + l : l * 8 + c;
 }
 
-// RING: conv_state is a ring buffer indexed by cache_seqlens (see resolve_row).
-template <int L, int ACT, int LAYOUT, bool RING>
+// W: filter width (2..4). RING: conv_state is a ring buffer indexed by cache_seqlens.
+template <int L, int W, int ACT, int LAYOUT, bool RING>
 __global__ void __launch_bounds__(256) k_update_vector(UpdateParams p) {
   const int64_t groups = p.D >> 3;  // 8-channel groups per row (D % 8 == 0)
   const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (g >= groups) return;
   const int64_t c0 = g << 3;
 
-  // weight[c0 .. c0+7, 0..3]: 32 BF16 in four 16-byte vectors, kept packed (two per
-  // word) and widened at use; bias likewise. Both are reused for every row.
+  // weight[c0 .. c0+7, 0..W-1] in W 16-byte vectors, kept packed (two per word) and
+  // widened at use; bias likewise. Both are reused for every row.
   uint32_t wv[16];
-  {
-    const uint16_t *wp = p.w + c0 * kW;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint4 t = ld_keep(wp + 8 * k);
-      wv[4 * k] = t.x; wv[4 * k + 1] = t.y; wv[4 * k + 2] = t.z; wv[4 * k + 3] = t.w;
-    }
-  }
+  load_weights_packed<W>(p.w, c0, wv);
   const bool has_bias = p.bias != nullptr;
   uint32_t bv[4] = {0u, 0u, 0u, 0u};
   if (has_bias) {
@@ -57,7 +50,7 @@ __global__ void __launch_bounds__(256) k_update_vector(UpdateParams p) {
   constexpr bool kPlanes = (LAYOUT == (int)Layout::ChannelLast);
   // State words held per row: compact 4L; channel-last linear 4L (plane 0 unused when
   // L > 3); channel-last ring: the three window planes.
-  constexpr int kWords = (kPlanes && RING) ? 4 * (kW - 1) : 4 * L;
+  constexpr int kWords = (kPlanes && RING) ? 4 * (W - 1) : 4 * L;
   struct Row {
     RowSlot slot;
     uint32_t xw[4];
@@ -79,15 +72,15 @@ __global__ void __launch_bounds__(256) k_update_vector(UpdateParams p) {
     } else if constexpr (RING) {
       const uint16_t *sp = p.state + r.slot.s * (L * p.D) + c0;
 #pragma unroll
-      for (int k = 0; k < kW - 1; ++k) {
-        const uint4 u = ld_stream(sp + (int64_t)((r.slot.q + L - (kW - 1) + k) % L) * p.D);
+      for (int k = 0; k < W - 1; ++k) {
+        const uint4 u = ld_stream(sp + (int64_t)((r.slot.q + L - (W - 1) + k) % L) * p.D);
         r.ow[4 * k] = u.x; r.ow[4 * k + 1] = u.y; r.ow[4 * k + 2] = u.z; r.ow[4 * k + 3] = u.w;
       }
     } else {
-      // Plane 0 is read only when L == 3: it is then inside the width-4 window; otherwise
-      // it is outside the window and is overwritten by plane 1.
+      // Plane 0 is read only when L == W - 1: it is then inside the window; otherwise it
+      // is outside the window and is overwritten by plane 1.
       const uint16_t *sp = p.state + r.slot.s * (L * p.D) + c0;
-      constexpr int first = (L == kW - 1) ? 0 : 1;
+      constexpr int first = (L == W - 1) ? 0 : 1;
 #pragma unroll
       for (int l = 0; l < L; ++l) {
         if (l < first) {
@@ -110,9 +103,9 @@ __global__ void __launch_bounds__(256) k_update_vector(UpdateParams p) {
     if constexpr (!kPlanes) {
       uint32_t nw[4 * L];
       if constexpr (RING) {
-        outv = update8_compact_ring<L, ACT>(r.xw, r.ow, wv, bv, has_bias, r.slot.q, nw);
+        outv = update8_compact_ring<L, W, ACT>(r.xw, r.ow, wv, bv, has_bias, r.slot.q, nw);
       } else {
-        outv = update8_compact<L, ACT>(r.xw, r.ow, wv, bv, has_bias, nw);
+        outv = update8_compact<L, W, ACT>(r.xw, r.ow, wv, bv, has_bias, nw);
       }
       uint16_t *sp = p.state + r.slot.s * (p.D * L) + c0 * L;
 #pragma unroll
@@ -120,16 +113,16 @@ __global__ void __launch_bounds__(256) k_update_vector(UpdateParams p) {
         st_stream(sp + 8 * k, make_uint4(nw[4 * k], nw[4 * k + 1], nw[4 * k + 2], nw[4 * k + 3]));
     } else {
       uint16_t *sp = p.state + r.slot.s * (L * p.D) + c0;
-      // window planes: the ring's three, or the linear state's last three
-      constexpr int wp0 = RING ? 0 : L - (kW - 1);
-      uint32_t h[kW - 1][8], xs[8];
+      // window planes: the ring's W-1, or the linear state's last W-1
+      constexpr int wp0 = RING ? 0 : L - (W - 1);
+      uint32_t h[3][8], xs[8];
 #pragma unroll
-      for (int k = 0; k < kW - 1; ++k)
+      for (int k = 0; k < W - 1; ++k)
         unpack8(make_uint4(r.ow[4 * (wp0 + k)], r.ow[4 * (wp0 + k) + 1], r.ow[4 * (wp0 + k) + 2],
                            r.ow[4 * (wp0 + k) + 3]),
                 h[k]);
       unpack8(make_uint4(r.xw[0], r.xw[1], r.xw[2], r.xw[3]), xs);
-      outv = outputs8_window<ACT>(h, xs, wv, bv, has_bias);
+      outv = outputs8_window<W, ACT>(h, xs, wv, bv, has_bias);
       if constexpr (RING) {
         st_stream(sp + (int64_t)r.slot.q * p.D, make_uint4(r.xw[0], r.xw[1], r.xw[2], r.xw[3]));
       } else {
@@ -157,34 +150,48 @@ __global__ void __launch_bounds__(256) k_update_vector(UpdateParams p) {
   }
 }
 
-template <int L, int ACT>
-cudaError_t launch_L(const UpdateParams &p, dim3 grid, dim3 block, cudaStream_t stream) {
+template <int L, int W, int ACT>
+cudaError_t launch_LW(const UpdateParams &p, dim3 grid, dim3 block, cudaStream_t stream) {
   const bool ring = p.seqlens != nullptr;
   if (p.layout == (int)Layout::Compact) {
     if (ring) {
-      k_update_vector<L, ACT, (int)Layout::Compact, true><<<grid, block, 0, stream>>>(p);
+      k_update_vector<L, W, ACT, (int)Layout::Compact, true><<<grid, block, 0, stream>>>(p);
     } else {
-      k_update_vector<L, ACT, (int)Layout::Compact, false><<<grid, block, 0, stream>>>(p);
+      k_update_vector<L, W, ACT, (int)Layout::Compact, false><<<grid, block, 0, stream>>>(p);
     }
   } else {
     if (ring) {
-      k_update_vector<L, ACT, (int)Layout::ChannelLast, true><<<grid, block, 0, stream>>>(p);
+      k_update_vector<L, W, ACT, (int)Layout::ChannelLast, true><<<grid, block, 0, stream>>>(p);
     } else {
-      k_update_vector<L, ACT, (int)Layout::ChannelLast, false><<<grid, block, 0, stream>>>(p);
+      k_update_vector<L, W, ACT, (int)Layout::ChannelLast, false><<<grid, block, 0, stream>>>(p);
     }
   }
   return cudaGetLastError();
 }
 
+// L from W - 1 (the shortest state the contract allows) up to kVectorMaxL.
+template <int W, int ACT>
+cudaError_t launch_W(const UpdateParams &p, dim3 grid, dim3 block, cudaStream_t stream) {
+  switch (p.L) {
+    case 1: if constexpr (W - 1 <= 1) return launch_LW<1, W, ACT>(p, grid, block, stream); break;
+    case 2: if constexpr (W - 1 <= 2) return launch_LW<2, W, ACT>(p, grid, block, stream); break;
+    case 3: return launch_LW<3, W, ACT>(p, grid, block, stream);
+    case 4: return launch_LW<4, W, ACT>(p, grid, block, stream);
+    case 5: return launch_LW<5, W, ACT>(p, grid, block, stream);
+    case 6: return launch_LW<6, W, ACT>(p, grid, block, stream);
+    case 7: return launch_LW<7, W, ACT>(p, grid, block, stream);
+    case 8: return launch_LW<8, W, ACT>(p, grid, block, stream);
+    default: break;
+  }
+  return cudaErrorInvalidValue;
+}
+
 template <int ACT>
 cudaError_t launch_act(const UpdateParams &p, dim3 grid, dim3 block, cudaStream_t stream) {
-  switch (p.L) {
-    case 3: return launch_L<3, ACT>(p, grid, block, stream);
-    case 4: return launch_L<4, ACT>(p, grid, block, stream);
-    case 5: return launch_L<5, ACT>(p, grid, block, stream);
-    case 6: return launch_L<6, ACT>(p, grid, block, stream);
-    case 7: return launch_L<7, ACT>(p, grid, block, stream);
-    case 8: return launch_L<8, ACT>(p, grid, block, stream);
+  switch (p.W) {
+    case 2: return launch_W<2, ACT>(p, grid, block, stream);
+    case 3: return launch_W<3, ACT>(p, grid, block, stream);
+    case 4: return launch_W<4, ACT>(p, grid, block, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -66,7 +66,7 @@ typedef struct CUstream_st *ccu_stream_t;
 typedef enum ccu_status {
   CCU_OK = 0,
   CCU_ERR_INVALID_ARGUMENT = 1, /* the arguments break the tensor contract */
-  CCU_ERR_NOT_IMPLEMENTED = 2,  /* valid, but not served (e.g. a width W != 4) */
+  CCU_ERR_NOT_IMPLEMENTED = 2,  /* valid, but not served (e.g. a width W > 4) */
   CCU_ERR_CUDA = 3              /* a CUDA launch or runtime call failed */
 } ccu_status_t;
 
@@ -79,10 +79,11 @@ typedef enum ccu_act { CCU_ACT_IDENTITY = 0, CCU_ACT_SILU = 1 } ccu_act_t;
 typedef enum ccu_route {
   CCU_ROUTE_AUTO = 0,
   CCU_ROUTE_SCALAR = 1, /* one thread per (row, channel); any D, ld, L and layout */
-  CCU_ROUTE_VECTOR = 2, /* 8 channels per thread, 16-byte vectors; D % 8 == 0, L <= 8 */
+  CCU_ROUTE_VECTOR = 2, /* 8 channels per thread, 16-byte vectors; D % 8 == 0, L <= 8
+                           (multi-token and prefill: width 4 only) */
   CCU_ROUTE_STAGED = 3, /* shared-memory staged tiles; D % 8 == 0, any L <= 256 */
   CCU_ROUTE_BULK = 4,   /* persistent CTAs, bulk async copies through shared memory;
-                           D % 8 == 0, L <= 8, both layouts */
+                           D % 8 == 0, L <= 8, width 4, both layouts */
   CCU_ROUTE_COUNT = 5
 } ccu_route_t;
 
@@ -128,7 +129,8 @@ typedef enum ccu_route {
  *               for non-padding rows (checked entry: a negative value is reported as
  *               CCU_DEVERR_RANGE and the row treated as padding).
  *   N, D, S     rows, channels, cache slots. N == 0 or D == 0 is a no-op.
- *   L, W        state length and filter width, L >= W - 1. Served: W == 4, any L >= 3.
+ *   L, W        state length and filter width, L >= W - 1. Served: W = 2, 3 or 4 (the page's
+ *               native width is 4; it names other widths as semantically valid), any L.
  *   out         BF16, contiguous [N, D], written for every row (+0 for padding rows).
  *               16-byte aligned; must not overlap any input.
  *
@@ -243,7 +245,7 @@ CCU_API ccu_status_t ccu_conv1d_update_multi(const void *x, int64_t x_stride_n, 
  * "Semantic tensor contract"). The page does not define that operation; this is the
  * update's definition applied to every token of a sequence:
  *
- *   out[b, d, t]  = act( sum_{j=0}^{3} weight[d, j] * xx(b, d, t - 3 + j) + bias[d] )
+ *   out[b, d, t]  = act( sum_{j=0}^{W-1} weight[d, j] * xx(b, d, t - (W-1) + j) + bias[d] )
  *   xx(b, d, t)   = x[b, d, t] for t >= 0, initial_states[b, d, L + t] for t < 0 (zero when
  *                   initial_states is NULL)
  *   final_states[b, d, l] = xx(b, d, T - L + l),  l = 0..L-1
@@ -255,7 +257,8 @@ CCU_API ccu_status_t ccu_conv1d_update_multi(const void *x, int64_t x_stride_n, 
  * kernel), and likewise for out, initial_states (b, d, l) and final_states (b, d, l). For the
  * hand-off layout pass final strides (L*D, 1, D). initial_states and final_states may be
  * NULL; final_states must not overlap initial_states, x or out, and out must not overlap x.
- * W must be 4 (CCU_ERR_NOT_IMPLEMENTED otherwise) and L >= W - 1. B, D or T == 0 is a
+ * W = 2, 3 or 4 (CCU_ERR_NOT_IMPLEMENTED otherwise; the vector kernel serves W = 4, other
+ * widths run on the scalar kernel) and L >= W - 1. B, D or T == 0 is a
  * no-op. route: CCU_ROUTE_AUTO, CCU_ROUTE_SCALAR or CCU_ROUTE_VECTOR.
  * Returns as ccu_conv1d_update.
  */

@@ -89,6 +89,17 @@ RING_WORKLOADS = {
     ]
 }
 
+# Other widths (the shortest state each allows, L = W - 1) on the large-batch decode.
+WIDTH_WORKLOADS = {
+    w.name: w
+    for w in [
+        dataclasses.replace(WORKLOADS["large_n4096_d16384_l3_perm_pad5_silu"],
+                            name="large_n4096_d16384_w3_l2_perm_pad5_silu", W=3, L=2),
+        dataclasses.replace(WORKLOADS["large_n4096_d16384_l3_perm_pad5_silu"],
+                            name="large_n4096_d16384_w2_l1_perm_pad5_silu", W=2, L=1),
+    ]
+}
+
 # Multi-token update: four tokens per row in one call (x token-major [N, T, D]).
 MULTI_WORKLOADS = {
     w.name: w

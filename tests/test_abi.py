@@ -96,8 +96,8 @@ def select(ccu, route=0, **kw):
 
 DECLINES = [
     ("misaligned cache_seqlens", dict(cache_seqlens=0x700002), 1, "cache_seqlens must be 4-byte"),
-    ("width 3", dict(W=3, L=3), 2, "W == 4"),
-    ("width 2", dict(W=2, L=1), 2, "W == 4"),
+    ("width 5", dict(W=5, L=4), 2, "W = 2, 3 and 4"),
+    ("width 1", dict(W=1, L=1), 2, "W = 2, 3 and 4"),
     ("L < W-1", dict(L=2), 1, "L must be >= W - 1"),
     ("ld < D", dict(ld=32), 1, "ld must be >= D"),
     ("padded ld not multiple of 8", dict(ld=68), 1, "multiple of 8"),
@@ -144,6 +144,16 @@ def test_decline_from_launching_entry_points_without_gpu(ccu):
 def test_noop_sizes(ccu):
     assert select(ccu, N=0) == (0, 0)
     assert select(ccu, D=0, x=None, weight=None) == (0, 0)
+
+
+def test_widths_2_and_3_are_served(ccu):
+    assert select(ccu, W=3, L=2) == (0, 2)
+    assert select(ccu, W=2, L=1) == (0, 2)
+    assert select(ccu, W=2, L=1, D=63) == (0, 1)
+    assert select(ccu, W=3, L=12) == (0, 3)
+    assert select(ccu, W=3, L=3, N=4096, D=16384, S=4096) == (0, 2)  # bulk kernels: width 4
+    assert select(ccu, route=4, W=3, L=3)[0] == 2
+    assert select(ccu, W=3, L=1)[0] == 1  # L < W - 1
 
 
 def test_ring_buffer_state_is_served(ccu):

@@ -381,8 +381,9 @@ def test_typed_declines_through_binding():
         ccu.causal_conv1d_update(x.view(4, 64, 1, 1), st, w)
     with pytest.raises(ValueError, match="intermediate_states"):
         ccu.causal_conv1d_update(x, st, w, intermediate_states=torch.empty((4, 1, 64, 3), dtype=torch.bfloat16, device=DEV))
-    with pytest.raises(NotImplementedError, match="W == 4"):
-        ccu.causal_conv1d_update(x, st, w[:, :3].contiguous())
+    with pytest.raises(NotImplementedError, match="W = 2, 3 and 4"):
+        ccu.causal_conv1d_update(x, torch.randn((4, 64, 4), device=DEV).to(torch.bfloat16),
+                                 torch.randn((64, 5), device=DEV).to(torch.bfloat16))
     with pytest.raises(ValueError, match="L must be >= W - 1"):
         ccu.causal_conv1d_update(x, st[:, :, :2].contiguous(), w)
     base = torch.randn((4 * 72 + 8,), device=DEV).to(torch.bfloat16)
@@ -683,3 +684,80 @@ def test_prefill_hands_off_to_decode():
     for bb in range(B):
         want, _ = oracle.full_causal_conv(x_all[bb], weight, bias, "silu", None, 3)
         assert bf16_ulp_distance(got[bb], want.T).max() <= 1
+
+
+# ----------------------------------------------------------------------------- widths 2 and 3
+
+WIDTH_CASES = [(W, L) for W in (2, 3) for L in sorted({W - 1, W, 5, 9})]
+
+
+@pytest.mark.parametrize("ring", [False, True])
+@pytest.mark.parametrize("route", ["scalar", "vector", "staged"])
+@pytest.mark.parametrize("layout", ["compact", "channel_last"])
+@pytest.mark.parametrize("W,L", WIDTH_CASES)
+def test_widths(W, L, layout, route, ring):
+    if route == "vector" and L > 8:
+        pytest.skip("vector kernels are compiled for L <= 8")
+    wl = synthetic.variant(synthetic.WORKLOADS["paged_n256_d8192_l3_s1024_pad10_silu"], name="width",
+                           N=9, D=264, ld=264, S=12, W=W, L=L, pad_frac=0.25)
+    inp = synthetic.generate(wl, seed=W * 100 + L)
+    if ring:
+        _check_ring(inp, ring_seqlens(np.random.default_rng(L), inp), layout, route,
+                    what=f"W={W} L={L} ring {route} {layout}")
+    else:
+        _check(inp, layout=layout, route=route, what=f"W={W} L={L} {route} {layout}")
+
+
+@pytest.mark.parametrize("W", [2, 3])
+def test_widths_large_batch_auto_route(W):
+    wl = synthetic.variant(synthetic.WORKLOADS[synthetic.BENCH_WORKLOAD], name="wide", N=512, S=512, W=W)
+    inp = synthetic.generate(wl, seed=W)
+    _check(inp, what=f"W={W} large")
+
+
+@pytest.mark.parametrize("W,L,T", [(2, 1, 3), (3, 2, 5), (3, 4, 2)])
+def test_widths_multi_token(W, L, T):
+    import depthwise_causal_conv1d_gb300 as ccu
+
+    rng = np.random.default_rng(W + L + T)
+    N, D, S = 5, 96, 6
+    x_tok = synthetic.f64_to_bf16_bits(rng.standard_normal((N, T, D)))
+    weight = synthetic.f64_to_bf16_bits(rng.standard_normal((D, W)))
+    state = synthetic.f64_to_bf16_bits(rng.standard_normal((S, D, L)))
+    idx = np.array([4, -1, 0, 2, 5], np.int32)
+    st_ref = state.copy()
+    want_out, want_inter = oracle.conv1d_update_multi(x_tok, (T * D, 1, D), st_ref, (D * L, L, 1), weight,
+                                                      None, "silu", idx, None, N, D, T, S, L, W,
+                                                      with_inter=True)
+    st = to_dev_u16(state, DEV)
+    inter = torch.zeros((N, T, D, L), dtype=torch.bfloat16, device=DEV)
+    out = ccu.causal_conv1d_update(to_dev_u16(x_tok, DEV).permute(0, 2, 1), st, to_dev_u16(weight, DEV),
+                                   None, "silu", conv_state_indices=torch.from_numpy(idx).to(DEV),
+                                   intermediate_states=inter)
+    torch.cuda.synchronize()
+    from oracle_pins import bf16_ulp_distance
+
+    assert np.array_equal(from_dev_u16(st), st_ref) and np.array_equal(from_dev_u16(inter), want_inter)
+    assert bf16_ulp_distance(from_dev_u16(out), want_out).max() <= 1
+
+
+@pytest.mark.parametrize("W", [2, 3])
+def test_widths_prefill(W):
+    import depthwise_causal_conv1d_gb300 as ccu
+
+    rng = np.random.default_rng(40 + W)
+    B, D, T, L = 2, 136, 50, W - 1
+    x_btd = synthetic.f64_to_bf16_bits(rng.standard_normal((B, T, D)))
+    weight = synthetic.f64_to_bf16_bits(rng.standard_normal((D, W)))
+    bias = synthetic.f64_to_bf16_bits(rng.standard_normal(D) * 0.1)
+    init = synthetic.f64_to_bf16_bits(rng.standard_normal((B, D, L)))
+    out, fin = ccu.causal_conv1d_fwd(to_dev_u16(x_btd, DEV).permute(0, 2, 1), to_dev_u16(weight, DEV),
+                                     to_dev_u16(bias, DEV), "silu", initial_states=to_dev_u16(init, DEV),
+                                     return_final_states=True)
+    torch.cuda.synchronize()
+    from oracle_pins import bf16_ulp_distance
+
+    for b in range(B):
+        y, f = oracle.full_causal_conv(x_btd[b], weight, bias, "silu", init[b], L)
+        assert bf16_ulp_distance(from_dev_u16(out[b]), y.T).max() <= 1
+        assert np.array_equal(from_dev_u16(fin[b]), f)
