@@ -459,10 +459,14 @@ def time_e2e_zero_copy(res: Resident, inp, steps: int, warmup: int, world: int, 
 
 
 def per_workload_table(dev, stream, reps=50):
-    """µs per call for every workload: eager (warm), CUDA-graph replay, and cold L2."""
+    """µs per call for every workload: eager (warm), CUDA-graph replay, and cold L2.
+
+    cold: a 2x-L2 buffer is written before each call (L2 left full of dirty lines, which
+    the call then also writes back); cold_clean: the buffer is read instead.
+    """
     import torch
 
-    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+    flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
     rows = {}
     for name, wl in {**synthetic.WORKLOADS, **synthetic.RING_WORKLOADS,
                      **synthetic.WIDTH_WORKLOADS}.items():
@@ -492,6 +496,19 @@ def per_workload_table(dev, stream, reps=50):
             cold.append((c0, c1))
         torch.cuda.synchronize()
         cold_us = statistics.median(c0.elapsed_time(c1) * 1e3 for c0, c1 in cold)
+        # clean cold: L2 filled by reading a buffer twice its size, so the call does not also
+        # pay for writing back the flush's dirty lines
+        clean = []
+        for _ in range(reps):
+            with torch.cuda.stream(stream):
+                flush.sum()
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            c0.record(stream)
+            res.call()
+            c1.record(stream)
+            clean.append((c0, c1))
+        torch.cuda.synchronize()
+        clean_us = statistics.median(c0.elapsed_time(c1) * 1e3 for c0, c1 in clean)
         # CUDA graph: 100 calls captured, replayed 20 times
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
@@ -510,7 +527,7 @@ def per_workload_table(dev, stream, reps=50):
         rows[name] = {"N_x_D": wl.N * wl.D, "bytes": nbytes, "route": res.route_name,
                       "state": f"{'ring' if wl.ring else 'linear'} {wl.layout}", "W": wl.W, "L": wl.L,
                       "eager_us": round(eager_us, 3), "graph_us": round(graph_us, 3),
-                      "cold_us": round(cold_us, 3),
+                      "cold_us": round(cold_us, 3), "cold_clean_us": round(clean_us, 3),
                       "cold_GBps": round(nbytes / (cold_us * 1e-6) / 1e9, 1),
                       "warm_frac": round(nbytes / (eager_us * 1e-6) / 1e9 / PEAK_GBPS, 4)}
         del g, res

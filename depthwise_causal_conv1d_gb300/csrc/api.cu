@@ -121,8 +121,9 @@ bool route_serves(int route, const Args &a, Layout /*layout*/) {
 }
 
 // Below this many (row, channel) elements a call is launch-bound and the plain vector
-// kernel's shorter start-up wins; above it the bulk-copy pipeline keeps more bytes in flight.
-constexpr int64_t kBulkMinElements = 1 << 22;
+// kernel's shorter start-up wins; above it the bulk-copy pipeline keeps more bytes in flight
+// (cold L2, D = 16384: tied at 64 rows, 12.3 vs 14.8 us at 128 rows, 24.6 vs 35.4 us at 512).
+constexpr int64_t kBulkMinElements = 1 << 20;
 
 ccu_status_t choose(int requested, const Args &a, Layout layout, int *chosen) {
   if (requested < 0 || requested >= CCU_ROUTE_COUNT)

@@ -177,6 +177,8 @@ ROUTE_CASES = [
     ("channel-last L12", dict(L=12, stride_s=768, stride_d=1, stride_l=64), "staged"),
     ("padded ld", dict(ld=72), "vector"),
     ("large batch compact", dict(N=4096, D=16384, S=4096), "bulk"),
+    ("mid batch compact", dict(N=256, D=8192, S=256), "bulk"),
+    ("below the bulk threshold", dict(N=64, D=8192, S=64), "vector"),
     ("large batch channel-last", dict(N=4096, D=16384, S=4096, stride_s=3 * 16384, stride_d=1,
                                       stride_l=16384), "vector"),
     ("large batch L9", dict(N=4096, D=16384, S=4096, L=9), "staged"),
