@@ -2,8 +2,9 @@
 //
 // The contract checked here is the one of the cuDNN page "Causal Conv1d Decode Update":
 // "Semantic tensor contract" (shapes, ld rule, L >= W - 1, the two state layouts) and
-// "Current native implementation" (width four, 16-byte pointer alignment for BF16
-// tensors, 4 bytes for indices). The declines follow the
+// "Current native implementation" (16-byte pointer alignment for BF16 tensors, 4 bytes
+// for indices; widths 2 and 3 and the multi-token, ring-buffer and prefill forms the page
+// names but does not serve are served here too). The declines follow the
 // cuDNN page "Composing multi-kernel blocks", section "The shape of a block": a contract
 // violation is CCU_ERR_INVALID_ARGUMENT, a valid but unserved request
 // CCU_ERR_NOT_IMPLEMENTED, and nothing is launched or changed in either case.

@@ -54,13 +54,6 @@ struct PrefillParams {
   int64_t sfb, sfd, sfl;
 };
 
-// Launch description chosen on the host.
-struct LaunchShape {
-  dim3 grid;
-  dim3 block;
-  size_t smem;
-};
-
 // ---------------------------------------------------------------------------------------
 // Device helpers. BF16 values travel as raw 16-bit patterns packed two per 32-bit word
 // (the lower address in the low half, as memory is little-endian).

@@ -1,5 +1,6 @@
-// Bulk-copy kernel for large batches (compact state layout, L = 3..8, D % 8 == 0; the
-// channel-last layout has its own bulk kernel in k_bulk_planes.cu).
+// Bulk-copy kernel for large batches (compact state layout, width 4, L = 3..8, D % 8 == 0,
+// linear or ring-buffer state; the channel-last layout has its own bulk kernel in
+// k_bulk_planes.cu).
 //
 // Every warp is an independent pipeline. Its work items are slices (row n, 256*G
 // consecutive channels); lane 0 moves whole slices between global and shared memory with

@@ -1,4 +1,5 @@
-// Staged kernels for any state length L (3..256) with 8-channel groups (D % 8 == 0).
+// Staged kernels for any state length L (W-1..256) and width W (2..4) with 8-channel groups
+// (D % 8 == 0); linear or ring-buffer state.
 //
 // Compact layout: a CTA owns a tile of C channels of one row at a time. The tile's state
 // slab (C*L contiguous BF16) and its x values are copied into shared memory with

@@ -1,7 +1,7 @@
 // Vector kernels: each thread owns 8 consecutive channels of one row at a time and moves
-// x, weight, bias, state and out as 16-byte vectors. L (3..8), the state layout and the
-// activation are compile-time, so the history lives in registers and the shift is a
-// fixed permutation of 16-bit lanes.
+// x, weight, bias, state and out as 16-byte vectors. L (W-1..8), the width W (2..4), the
+// state layout, linear or ring state and the activation are compile-time, so the history
+// lives in registers and the shift is a fixed permutation of 16-bit lanes.
 //
 // Update definition: cuDNN page "Causal Conv1d Decode Update", introduction (update
 // block); layouts from its "Semantic tensor contract" (compact state, and the
@@ -13,15 +13,6 @@ namespace ccu {
 int device_sm_count();
 
 namespace {
-
-// Position of state element (channel c of the thread's 8, entry l) inside the thread's
-// registers: 4*L words, two BF16 per word.
-//   compact      [8 channels][L]: flat c*L + l
-//   channel-last [L planes][8 channels]: plane l is one 16-byte vector
-template <int L, int LAYOUT>
-__device__ __forceinline__ constexpr int elem_pos(int c, int l) {
-  return LAYOUT == (int)Layout::Compact ? c * L + l : l * 8 + c;
-}
 
 // W: filter width (2..4). RING: conv_state is a ring buffer indexed by cache_seqlens.
 template <int L, int W, int ACT, int LAYOUT, bool RING>
