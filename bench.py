@@ -69,6 +69,10 @@ def parse_args():
                     help="device-resident timing only: no e2e, table, CPU baseline or clocks")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--table", choices=["prefill", "multi"], default=None,
+                    help="time only the prefill or the multi-token rows, with --route, and print "
+                         "them as one JSON line (profiling)")
+    ap.add_argument("--table-reps", type=int, default=50, help="timed calls per row of --table")
     return ap.parse_args()
 
 
@@ -535,7 +539,7 @@ def per_workload_table(dev, stream, reps=50):
     return rows
 
 
-def multi_token_rows(dev, stream, reps=50):
+def multi_token_rows(dev, stream, reps=50, route=0, singles_too=True):
     """µs per call of the multi-token update, and of the same tokens as T single calls."""
     import torch
 
@@ -557,7 +561,7 @@ def multi_token_rows(dev, stream, reps=50):
             stat = ccu.lib.ccu_conv1d_update_multi(
                 x.data_ptr(), T * D, 1, D, st.data_ptr(), D * L, L, 1, w.data_ptr(), b.data_ptr(), act,
                 idx.data_ptr(), None, N, D, T, wl.S, L, wl.W, out.data_ptr(), T * D, 1, D, None, None,
-                0, stream.cuda_stream)
+                route, stream.cuda_stream)
             if stat != 0:
                 ccu.raise_for_status(stat)
 
@@ -571,7 +575,7 @@ def multi_token_rows(dev, stream, reps=50):
                     ccu.raise_for_status(stat)
 
         res = {}
-        for label, fn in (("multi", multi), ("singles", singles)):
+        for label, fn in (("multi", multi), ("singles", singles))[:2 if singles_too else 1]:
             for _ in range(3):
                 fn()
             torch.cuda.synchronize()
@@ -586,11 +590,11 @@ def multi_token_rows(dev, stream, reps=50):
         rows[name] = {"N_x_D": N * D, "T": T, "bytes": nbytes, "us_per_call": round(res["multi"], 3),
                       "GBps": round(nbytes / (res["multi"] * 1e-6) / 1e9, 1),
                       "frac": round(nbytes / (res["multi"] * 1e-6) / 1e9 / PEAK_GBPS, 4),
-                      "same_tokens_as_T_single_calls_us": round(res["singles"], 3)}
+                      "same_tokens_as_T_single_calls_us": round(res.get("singles", float("nan")), 3)}
     return rows
 
 
-def prefill_rows(dev, stream, reps=50):
+def prefill_rows(dev, stream, reps=50, route=0):
     """µs per call of the full-sequence prefill (with its channel-last final state)."""
     import torch
 
@@ -611,7 +615,7 @@ def prefill_rows(dev, stream, reps=50):
             st = ccu.lib.ccu_causal_conv1d_fwd(
                 x.data_ptr(), *x.stride(), w.data_ptr(), None if b is None else b.data_ptr(), act,
                 None, 0, 0, 0, B, D, T, L, spec["W"], out.data_ptr(), *out.stride(), fin.data_ptr(),
-                *fin.stride(), 0, stream.cuda_stream)
+                *fin.stride(), route, stream.cuda_stream)
             if st != 0:
                 ccu.raise_for_status(st)
 
@@ -745,6 +749,24 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_table(args):
+    """Only the prefill or the multi-token rows (one JSON line); for profiling one kernel."""
+    import torch
+
+    import depthwise_causal_conv1d_gb300 as ccu
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    route = ccu.ROUTES[args.route]
+    if args.table == "prefill":
+        rows = prefill_rows(dev, stream, args.table_reps, route)
+    else:
+        rows = multi_token_rows(dev, stream, args.table_reps, route, singles_too=False)
+    print(json.dumps({"table": args.table, "route": args.route, "reps": args.table_reps, "rows": rows}),
+          flush=True)
+
+
 def run_reference(args):
     """The reference arm: the CPU oracle, as it stands, on the host cores (rank 0 only)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -789,6 +811,8 @@ def main():
         args.warmup = 3  # at least three untimed warm-up steps
     if args.impl == "reference":
         run_reference(args)
+    elif args.table is not None:
+        run_table(args)
     else:
         run_ours(args)
 

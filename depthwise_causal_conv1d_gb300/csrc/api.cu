@@ -347,6 +347,9 @@ struct PrefillArgs {
   int64_t B, D, T, L, W;
 };
 
+// Prefill sizes (B*D*T) from which AUTO takes the bulk-copy kernel.
+constexpr int64_t kPrefillBulkMinElements = int64_t(1) << 20;
+
 // Tokens per thread: enough (batch row, channel group, chunk) items to fill the GPU several
 // times over, and at least 32 tokens so the 3-token halo stays a small overhead.
 int64_t prefill_chunk(int64_t B, int64_t lanes, int64_t T) {
@@ -401,13 +404,16 @@ ccu_status_t run_prefill(const PrefillArgs &a, int route, cudaStream_t stream) {
   f.sib = a.sib; f.sid = a.sid; f.sil = a.sil;
   f.fin = static_cast<uint16_t *>(const_cast<void *>(a.fin));
   f.sfb = a.sfb; f.sfd = a.sfd; f.sfl = a.sfl;
-  bool vector;
+  bool vector, bulk = false;
   if (route == CCU_ROUTE_AUTO) {
     vector = vec_ok;
+    bulk = vec_ok && a.B * a.D * a.T >= kPrefillBulkMinElements;
   } else if (route == CCU_ROUTE_SCALAR) {
     vector = false;
   } else if (route == CCU_ROUTE_VECTOR && vec_ok) {
     vector = true;
+  } else if (route == CCU_ROUTE_BULK && vec_ok) {
+    vector = bulk = true;
   } else if (route >= 0 && route < CCU_ROUTE_COUNT) {
     return fail(CCU_ERR_NOT_IMPLEMENTED, "route '%s' does not serve these prefill arguments",
                 ccu_route_name(route));
@@ -424,7 +430,8 @@ ccu_status_t run_prefill(const PrefillArgs &a, int route, cudaStream_t stream) {
   p.D = a.D;
   p.L = a.L;
   p.W = a.W;
-  cudaError_t e = launch_prefill(p, f, a.act, vector, stream);
+  cudaError_t e = bulk ? launch_prefill_bulk(p, f, a.act, stream)
+                       : launch_prefill(p, f, a.act, vector, stream);
   if (e != cudaSuccess)
     return fail(CCU_ERR_CUDA, "launch of the prefill kernel failed: %s", cudaGetErrorString(e));
   return CCU_OK;

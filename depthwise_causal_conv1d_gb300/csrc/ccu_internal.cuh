@@ -73,21 +73,39 @@ __device__ __forceinline__ uint16_t round_bf16(float v) {
   return *reinterpret_cast<uint16_t *>(&b);
 }
 
+// PTX approximations (documented in the PTX ISA: ex2.approx has a relative error of about
+// 2^-22 over the normal range, rcp.approx about one float ulp), flushing subnormals.
+__device__ __forceinline__ float ex2_approx_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_approx_ftz(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // The activation, a compile-time choice: identity kernels carry no SiLU code.
 // SiLU is a * sigmoid(a). With e = exp(-|a|) in (0, 1], sigmoid(a) = 1 / (1 + e) for
-// a >= 0 and e / (1 + e) for a < 0, so a * sigmoid(a) = (a >= 0 ? a : a * e) / (1 + e):
-// no overflow for any finite a (a / (1 + exp(-a)) overflows to -0 below a ~ -88.7, where
-// the true value is still a representable float). The exponential and the division use
-// the hardware approximations (__expf, __fdividef with a denominator in [1, 2]): a few
-// float ulps of error, far below the half BF16 ulp (2^15 float ulps) the result keeps, so
-// the rounded output stays within one BF16 ulp of the exact value. The accurate library
-// versions made this path issue-bound on the large batch.
+// a >= 0 and e / (1 + e) for a < 0, so a * sigmoid(a) = (a >= 0 ? a : a * e) / (1 + e)
+// = max(a, a * e) / (1 + e), since e <= 1 makes a >= a * e exactly when a >= 0. No step
+// overflows for any finite a (a / (1 + exp(-a)) overflows to -0 below a ~ -88.7, where the
+// true value is still a representable float). The exponential is taken as
+// 2^(32 - |a| log2 e) = e * 2^32, a normal float for |a| < 109, and brought back with a
+// power-of-two multiply: exact while e is normal, and below 2^-126 an absolute error under
+// 1e-45, far below the BF16 subnormal step of ~9e-41 that a * e is rounded to (the
+// flushing approximation alone would zero e below a ~ -87.3, where a * e still rounds to a
+// nonzero BF16). Below a ~ -109 the true value rounds to -0 in BF16 as well. 1 + e lies in
+// [1, 2], where rcp.approx is accurate. The error is a few float ulps, far below the half
+// BF16 ulp (2^15 float ulps) the result keeps, so the rounded output stays within one BF16
+// ulp of the exact value. Eight arithmetic operations: the kernels that move 4 bytes per
+// element are issue-bound on the SiLU.
 template <int ACT>
 __device__ __forceinline__ float activate(float a) {
   if constexpr (ACT == 1) {
-    const float e = __expf(-fabsf(a));
-    const float num = a >= 0.0f ? a : a * e;
-    return __fdividef(num, 1.0f + e);
+    const float e = ex2_approx_ftz(fmaf(fabsf(a), -1.4426950408889634f, 32.0f)) * 0x1p-32f;
+    return fmaxf(a, a * e) * rcp_approx_ftz(1.0f + e);
   } else {
     return a;
   }
@@ -295,6 +313,10 @@ cudaError_t launch_multi_vector(const UpdateParams &p, const MultiParams &m, int
                                 cudaStream_t stream);
 cudaError_t launch_prefill(const UpdateParams &p, const PrefillParams &f, int act, bool vector,
                            cudaStream_t stream);
+// Bulk-copy prefill (width 4, channel-contiguous x and out); sets the run length itself.
+cudaError_t launch_prefill_bulk(const UpdateParams &p, const PrefillParams &f, int act,
+                                cudaStream_t stream);
+cudaError_t take_prefill_error(int32_t *bits);
 cudaError_t launch_check_indices(const int32_t *idx, int64_t N, int64_t S, uint32_t *bitmap,
                                  int32_t *status, cudaStream_t stream);
 

@@ -239,11 +239,12 @@ cudaError_t launch_A(const UpdateParams &p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t take_async_error(int32_t *bits) {
-  int32_t zero = 0, planes = 0;
+  int32_t zero = 0, planes = 0, prefill = 0;
   cudaError_t e = cudaMemcpyFromSymbol(bits, g_async_error, sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_async_error, &zero, sizeof(int32_t));
   if (e == cudaSuccess) e = take_planes_error(&planes);
-  if (e == cudaSuccess) *bits |= planes;
+  if (e == cudaSuccess) e = take_prefill_error(&prefill);
+  if (e == cudaSuccess) *bits |= planes | prefill;
   return e;
 }
 

@@ -13,14 +13,17 @@
 // contract"). The page does not define that operation; the convolution above is the
 // update's definition applied to every token of a sequence.
 //
-// Work split: a thread owns 8 channels (vector kernel) or 1 channel (scalar kernel) of one
-// batch row and a chunk of consecutive tokens; it reads the 3 inputs before its chunk
-// (the halo) and then slides the width-4 window through the chunk.
-#include "ccu_internal.cuh"
+// Work split: a thread owns 8 channels (vector and bulk kernels) or 1 channel (scalar
+// kernel) of one batch row and a chunk of consecutive tokens; it reads the W-1 inputs before
+// its chunk (the halo) and then slides the window through the chunk.
+#include <atomic>
+
+#include "ccu_bulk.cuh"
 
 namespace ccu {
 
 int device_sm_count();
+int current_device();
 
 namespace {
 
@@ -83,15 +86,72 @@ __device__ __forceinline__ void widen8(const uint4 v, float (&f)[8]) {
   }
 }
 
+// The width-4 weights of channels c0..c0+7 as floats: wf[j][c] = weight[c0 + c, j].
+__device__ __forceinline__ void load_weights_f(const UpdateParams &p, int64_t c0, float (&wf)[kW][8]) {
+  const uint16_t *wp = p.w + c0 * kW;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint4 t = ld_keep(wp + 8 * k);
+    const uint32_t v[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = 8 * k + 2 * i;  // flat c*4 + j of the low half
+      wf[e % kW][e / kW] = bf16_lo(v[i]);
+      wf[(e + 1) % kW][(e + 1) / kW] = bf16_hi(v[i]);
+    }
+  }
+}
+
+// Outputs of 8 channels for one token from the window a, b, c (oldest first) and the token's
+// inputs x. The accumulation order is the update's: ((0 + a*w0) + b*w1) + c*w2 + x*w3, then
+// the bias (each product of two BF16 values is exact in FP32).
+template <int ACT>
+__device__ __forceinline__ uint4 outputs8f(const float (&wf)[kW][8], const float (&bf)[8],
+                                           bool has_bias, const float (&a)[8], const float (&b)[8],
+                                           const float (&c)[8], const float (&x)[8]) {
+  float y[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float acc = __fmaf_rn(a[i], wf[0][i], 0.0f);
+    acc = __fmaf_rn(b[i], wf[1][i], acc);
+    acc = __fmaf_rn(c[i], wf[2][i], acc);
+    acc = __fmaf_rn(x[i], wf[3][i], acc);
+    if (has_bias) acc = acc + bf[i];
+    y[i] = activate<ACT>(acc);
+  }
+  return make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                    pack_bf16x2(y[6], y[7]));
+}
+
+// The window before token t0 for channels c0..c0+7: inputs t0-3, t0-2, t0-1 (from x, or the
+// initial state / zeros before the sequence).
+__device__ __forceinline__ void load_halo(const UpdateParams &p, const PrefillParams &f, int64_t b,
+                                          int64_t c0, int64_t t0, float (&h0)[8], float (&h1)[8],
+                                          float (&h2)[8]) {
+  const uint16_t *xb = p.x + b * f.sxb + c0;
+  float *hs[3] = {h0, h1, h2};
+#pragma unroll
+  for (int k = 0; k < kW - 1; ++k) {
+    const int64_t t = t0 - (kW - 1) + k;
+    if (t >= 0) {
+      float tmp[8];
+      widen8(ld_keep(xb + t * f.sxt), tmp);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) hs[k][c] = tmp[c];
+    } else {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) hs[k][c] = bf16_bits(input_at(p, f, b, c0 + c, t));
+    }
+  }
+}
+
 // 8 channels per thread, width 4; x and out channel-contiguous (one 16-byte vector per
 // token). The prefill moves 4 bytes per element, a quarter of the decode update's 16, so its
 // arithmetic is kept lean: weights and bias are widened to floats once, the width-4 window
 // is kept as floats, and tokens go four at a time so the window slides by register
 // renaming; the next four tokens' loads are issued before the current four are computed
 // (measured on B=8, T=4096, D=4096 with SiLU: 298 us for the first version, 159 us with
-// float windows, 105 us with the loads one group ahead). The accumulation order is the
-// update's: ((0 + h0*w0) + h1*w1) + h2*w2 + x*w3, then the bias (each product of two
-// BF16 values is exact in FP32).
+// float windows, 105 us with the loads one group ahead).
 template <int ACT>
 __global__ void __launch_bounds__(256) k_prefill_vector(UpdateParams p, PrefillParams f) {
   const int64_t groups = p.D >> 3;
@@ -104,20 +164,7 @@ __global__ void __launch_bounds__(256) k_prefill_vector(UpdateParams p, PrefillP
   const int64_t t1 = t0 + f.chunk < f.T ? t0 + f.chunk : f.T;
 
   float wf[kW][8];  // wf[j][c] = weight[c0 + c, j]
-  {
-    const uint16_t *wp = p.w + c0 * kW;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint4 t = ld_keep(wp + 8 * k);
-      const uint32_t v[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int e = 8 * k + 2 * i;  // flat c*4 + j of the low half
-        wf[e % kW][e / kW] = bf16_lo(v[i]);
-        wf[(e + 1) % kW][(e + 1) / kW] = bf16_hi(v[i]);
-      }
-    }
-  }
+  load_weights_f(p, c0, wf);
   const bool has_bias = p.bias != nullptr;
   float bf[8];
   if (has_bias) {
@@ -126,38 +173,12 @@ __global__ void __launch_bounds__(256) k_prefill_vector(UpdateParams p, PrefillP
 
   // The window before the chunk: inputs t0-3, t0-2, t0-1 (from x, or the initial state).
   float h0[8], h1[8], h2[8];
+  load_halo(p, f, b, c0, t0, h0, h1, h2);
   const uint16_t *xb = p.x + b * f.sxb + c0;
-  {
-    float *hs[3] = {h0, h1, h2};
-#pragma unroll
-    for (int k = 0; k < kW - 1; ++k) {
-      const int64_t t = t0 - (kW - 1) + k;
-      if (t >= 0) {
-        float tmp[8];
-        widen8(ld_keep(xb + t * f.sxt), tmp);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) hs[k][c] = tmp[c];
-      } else {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) hs[k][c] = bf16_bits(input_at(p, f, b, c0 + c, t));
-      }
-    }
-  }
 
   auto outputs = [&](const float (&a)[8], const float (&bb)[8], const float (&cc)[8],
                      const float (&xx)[8]) -> uint4 {
-    float y[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      float acc = __fmaf_rn(a[c], wf[0][c], 0.0f);
-      acc = __fmaf_rn(bb[c], wf[1][c], acc);
-      acc = __fmaf_rn(cc[c], wf[2][c], acc);
-      acc = __fmaf_rn(xx[c], wf[3][c], acc);
-      if (has_bias) acc = acc + bf[c];
-      y[c] = activate<ACT>(acc);
-    }
-    return make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
-                      pack_bf16x2(y[6], y[7]));
+    return outputs8f<ACT>(wf, bf, has_bias, a, bb, cc, xx);
   };
 
   uint16_t *ob = p.out + b * f.sob + c0;
@@ -206,6 +227,248 @@ __global__ void __launch_bounds__(256) k_prefill_vector(UpdateParams p, PrefillP
   }
 }
 
+// ------------------------------------------------------------------ bulk-copy prefill
+//
+// Width 4, channel-contiguous x and out. The vector kernel above keeps its next four tokens
+// in registers, and at 128 registers a thread only 16 warps fit on an SM: too few bytes in
+// flight for HBM. Here x travels through shared memory instead. Each warp is a pipeline over
+// a run of consecutive tokens of one sequence and 256 channels (8 per lane): lane 0 brings
+// kTG tokens at a time (one 512-byte cp.async.bulk per token) into a kP-stage ring that
+// completes on per-stage mbarriers, the lanes slide their float windows through the stage
+// from shared memory and store the outputs as 16-byte streaming stores, and the stage is
+// refilled kP groups ahead. A warp's run is long (the runs are sized so that there is about
+// one per warp), so the 3-token halo and the weights are read once per run. Every mbarrier
+// wait is bounded: on expiry the warp raises CCU_DEVERR_TIMEOUT, waits (bounded) for its own
+// copies and returns.
+
+__device__ int32_t g_prefill_error = 0;  // CCU_DEVERR_* bits raised by the bulk prefill
+
+constexpr int kPThreads = 512;                 // 16 warps per CTA
+constexpr int kPWarps = kPThreads / 32;
+constexpr int64_t kRunCh = 256;                // channels per warp (8 per lane)
+constexpr int64_t kRowBytes = 2 * kRunCh;      // one token of a run
+constexpr int kTG = 8;                         // tokens per stage
+constexpr int kP = 3;                          // stages per warp
+constexpr int64_t kStageBytes = kTG * kRowBytes;
+constexpr int64_t kHeadBytes = 128;  // per warp: kP mbarriers, then the producer cursor
+constexpr int64_t kWarpBytes = kHeadBytes + kP * kStageBytes;
+
+// One run: batch row b, channels c_base .. c_base+cn-1, tokens t0 .. t1-1.
+struct Run {
+  int64_t b, c_base, cn, t0, t1;
+};
+
+// Run i, with the channel slice fastest so that neighbouring warps read neighbouring bytes
+// of the same tokens.
+__device__ __forceinline__ Run run_of(const UpdateParams &p, const PrefillParams &f, int64_t i,
+                                      int64_t slices, int64_t chunks) {
+  Run r;
+  const int64_t s = i % slices;
+  const int64_t rest = i / slices;
+  r.b = rest / chunks;
+  r.c_base = s * kRunCh;
+  const int64_t rem = p.D - r.c_base;
+  r.cn = rem < kRunCh ? rem : kRunCh;
+  r.t0 = (rest % chunks) * f.chunk;
+  r.t1 = r.t0 + f.chunk < f.T ? r.t0 + f.chunk : f.T;
+  return r;
+}
+
+// Lane 0's producer cursor: the next group's first x row, the tokens of its run from there,
+// the row bytes, the warp's run index m, the stage of the next load and the loads issued but
+// not yet consumed. It lives in shared memory, out of the registers the lanes need for their
+// windows and weights.
+struct Cursor {
+  const uint16_t *src;
+  int64_t left, m;
+  uint32_t bytes;
+  int st, inflight;
+};
+static_assert(kP * 8 + 8 + sizeof(Cursor) <= kHeadBytes, "warp header too small");
+
+template <int ACT>
+__global__ void __launch_bounds__(kPThreads, 1) k_prefill_bulk(UpdateParams p, PrefillParams f,
+                                                               int64_t chunks) {
+  using namespace bulk;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  unsigned char *wbase = smem + (int64_t)warp * kWarpBytes;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(wbase);
+  Cursor *cur = reinterpret_cast<Cursor *>(wbase + 8 * ((kP + 1) & ~1));
+  unsigned char *bufs = wbase + kHeadBytes;
+
+  const int64_t slices = (p.D + kRunCh - 1) / kRunCh;
+  const int64_t runs = f.B * slices * chunks;
+  const int64_t first_run = (int64_t)blockIdx.x * kPWarps + warp;
+  const int64_t stride = (int64_t)gridDim.x * kPWarps;
+  const int64_t mine = runs > first_run ? (runs - first_run + stride - 1) / stride : 0;
+  if (mine == 0) return;
+
+  // Lane 0: point the cursor at the start of the warp's m-th run.
+  auto start_run = [&](Cursor &c, int64_t m) {
+    const Run r = run_of(p, f, first_run + m * stride, slices, chunks);
+    c.src = p.x + r.b * f.sxb + r.t0 * f.sxt + r.c_base;
+    c.left = r.t1 - r.t0;
+    c.bytes = (uint32_t)(r.cn * 2);
+    c.m = m;
+  };
+  // Lane 0: load the cursor's group (up to kTG tokens) into its stage and advance.
+  auto issue_next = [&]() {
+    Cursor c = *cur;
+    if (c.m >= mine) return;
+    const int nt = c.left < kTG ? (int)c.left : kTG;
+    uint64_t *bar = &bars[c.st];
+    unsigned char *buf = bufs + c.st * kStageBytes;
+    mbar_arrive_expect_tx(bar, c.bytes * (uint32_t)nt);
+    for (int k = 0; k < nt; ++k) bulk_load(buf + k * kRowBytes, c.src + k * f.sxt, c.bytes, bar);
+    ++c.inflight;
+    if (++c.st == kP) c.st = 0;
+    c.left -= nt;
+    c.src += nt * f.sxt;
+    if (c.left == 0) {
+      if (c.m + 1 < mine) {
+        start_run(c, c.m + 1);
+      } else {
+        c.m = mine;
+      }
+    }
+    *cur = c;
+  };
+  if (lane == 0) {
+    for (int k = 0; k < kP; ++k) mbar_init(&bars[k], 1);
+    fence_mbar_init();
+    Cursor c;
+    start_run(c, 0);
+    c.st = 0;
+    c.inflight = 0;
+    *cur = c;
+    for (int k = 0; k < kP; ++k) issue_next();
+  }
+  __syncwarp();
+
+  const bool has_bias = p.bias != nullptr;
+  float wf[kW][8], bf[8], h0[8], h1[8], h2[8];
+  int64_t w_base = -1;
+  int st = 0;
+  uint32_t phase = 0;
+  bool failed = false;
+  for (int64_t m = 0; m < mine && !failed; ++m) {
+    // A new run: weights (when the channels change) and the halo.
+    const Run r = run_of(p, f, first_run + m * stride, slices, chunks);
+    const bool active = 8 * lane < r.cn;
+    const int64_t c0 = r.c_base + 8 * lane;
+    if (active) {
+      if (r.c_base != w_base) {
+        load_weights_f(p, c0, wf);
+        if (has_bias) widen8(ld_keep(p.bias + c0), bf);
+      }
+      load_halo(p, f, r.b, c0, r.t0, h0, h1, h2);
+    }
+    w_base = r.c_base;
+    const bool ends = f.fin != nullptr && r.t1 == f.T;
+    const int64_t b = r.b;
+    uint16_t *ob = p.out + b * f.sob + r.t0 * f.sot + c0;
+    for (int64_t left = r.t1 - r.t0; left > 0; left -= kTG) {
+      const bool ok = mbar_wait(&bars[st], phase);
+      if (!__all_sync(kFull, ok)) {
+        failed = true;
+        break;
+      }
+      if (active) {
+        const uint4 *row = reinterpret_cast<const uint4 *>(bufs + st * kStageBytes) + lane;
+        if (left >= kTG) {
+#pragma unroll
+          for (int k = 0; k < kTG; ++k) {  // unrolled: the window slides by register renaming
+            float xk[8];
+            widen8(row[k * (kRowBytes / 16)], xk);
+            st_stream(ob + k * f.sot, outputs8f<ACT>(wf, bf, has_bias, h0, h1, h2, xk));
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              h0[c] = h1[c];
+              h1[c] = h2[c];
+              h2[c] = xk[c];
+            }
+          }
+        } else {
+          for (int k = 0; k < (int)left; ++k) {
+            float xk[8];
+            widen8(row[k * (kRowBytes / 16)], xk);
+            st_stream(ob + k * f.sot, outputs8f<ACT>(wf, bf, has_bias, h0, h1, h2, xk));
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              h0[c] = h1[c];
+              h1[c] = h2[c];
+              h2[c] = xk[c];
+            }
+          }
+        }
+        if (ends && left <= kTG) {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) write_final(p, f, b, c0 + c);
+        }
+      }
+      ob += kTG * f.sot;
+      // Every lane has read the stage; order those reads before the refill's async writes.
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        --cur->inflight;
+        issue_next();
+      }
+      if (++st == kP) {
+        st = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+
+  if (failed && lane == 0) {
+    atomicOr(&g_prefill_error, kDevErrTimeout);
+    for (int q = cur->inflight; q > 0; --q) {  // the warp's loads still in flight
+      mbar_wait(&bars[st], phase);
+      if (++st == kP) {
+        st = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+}
+
+constexpr int kMaxDevices = 64;
+std::atomic<bool> g_bulk_opted_in[kMaxDevices][2];
+
+template <int ACT>
+cudaError_t launch_prefill_bulk_act(const UpdateParams &p, PrefillParams f, cudaStream_t stream) {
+  const size_t smem = (size_t)kPWarps * kWarpBytes;
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!g_bulk_opted_in[dev][ACT].load(std::memory_order_acquire)) {
+    cudaError_t e = cudaFuncSetAttribute(k_prefill_bulk<ACT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    g_bulk_opted_in[dev][ACT].store(true, std::memory_order_release);
+  }
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_prefill_bulk<ACT>,
+                                                                kPThreads, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  const int64_t ctas = (int64_t)device_sm_count() * per_sm;
+  // Runs: split each (batch row, channel slice) pair's tokens so that there is about one run
+  // per warp; a run is a whole number of kTG-token groups.
+  const int64_t pairs = f.B * ((p.D + kRunCh - 1) / kRunCh);
+  int64_t chunks = ctas * kPWarps / pairs;
+  if (chunks < 1) chunks = 1;
+  int64_t chunk = (f.T + chunks - 1) / chunks;
+  chunk = (chunk + kTG - 1) / kTG * kTG;
+  chunks = (f.T + chunk - 1) / chunk;
+  f.chunk = chunk;
+  int64_t grid = (pairs * chunks + kPWarps - 1) / kPWarps;
+  if (grid > ctas) grid = ctas;
+  k_prefill_bulk<ACT><<<(unsigned)grid, kPThreads, smem, stream>>>(p, f, chunks);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_prefill(const UpdateParams &p, const PrefillParams &f, int act, bool vector,
@@ -237,6 +500,18 @@ cudaError_t launch_prefill(const UpdateParams &p, const PrefillParams &f, int ac
     }
   }
   return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_bulk(const UpdateParams &p, const PrefillParams &f, int act,
+                                cudaStream_t stream) {
+  return act == 1 ? launch_prefill_bulk_act<1>(p, f, stream) : launch_prefill_bulk_act<0>(p, f, stream);
+}
+
+cudaError_t take_prefill_error(int32_t *bits) {
+  int32_t zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(bits, g_prefill_error, sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_prefill_error, &zero, sizeof(int32_t));
+  return e;
 }
 
 }  // namespace ccu

@@ -254,12 +254,16 @@ CCU_API ccu_status_t ccu_conv1d_update_multi(const void *x, int64_t x_stride_n, 
  * convolution. All tensors are device memory; element (b, d, t) of x is at
  * x[b*x_stride_b + d*x_stride_d + t*x_stride_t] (any non-negative strides; channel-
  * contiguous x and out -- stride_d == 1, the other strides multiples of 8 -- run the vector
- * kernel), and likewise for out, initial_states (b, d, l) and final_states (b, d, l). For the
+ * or the bulk-copy kernel), and likewise for out, initial_states (b, d, l) and final_states
+ * (b, d, l). For the
  * hand-off layout pass final strides (L*D, 1, D). initial_states and final_states may be
  * NULL; final_states must not overlap initial_states, x or out, and out must not overlap x.
  * W = 2, 3 or 4 (CCU_ERR_NOT_IMPLEMENTED otherwise; the vector kernel serves W = 4, other
  * widths run on the scalar kernel) and L >= W - 1. B, D or T == 0 is a
- * no-op. route: CCU_ROUTE_AUTO, CCU_ROUTE_SCALAR or CCU_ROUTE_VECTOR.
+ * no-op. route: CCU_ROUTE_AUTO, CCU_ROUTE_SCALAR, CCU_ROUTE_VECTOR or CCU_ROUTE_BULK (x staged
+ * through shared memory by cp.async.bulk; the vector kernel's conditions; AUTO takes it from
+ * B*D*T >= 2^20). The bulk kernel bounds its waits: on expiry it stops and raises
+ * CCU_DEVERR_TIMEOUT, read with ccu_conv1d_take_device_error.
  * Returns as ccu_conv1d_update.
  */
 CCU_API ccu_status_t ccu_causal_conv1d_fwd(const void *x, int64_t x_stride_b, int64_t x_stride_d,
@@ -333,7 +337,8 @@ CCU_API int64_t ccu_conv1d_check_indices_scratch_bytes(int64_t S);
 /*
  * ccu_conv1d_take_device_error -- read and clear the library's own device error word.
  *
- * Kernels that wait on their own asynchronous copies (the bulk family) never wait without
+ * Kernels that wait on their own asynchronous copies (the bulk family of the update and
+ * of the prefill) never wait without
  * limit; if a wait gives up they OR CCU_DEVERR_TIMEOUT into the caller's status word when
  * there is one (checked entry points), and otherwise into this per-process, per-device
  * word. This call SYNCHRONIZES the current device (it copies the word to the host).

@@ -167,7 +167,45 @@ def test_extreme_values():
         _check(inp, what=f"extreme {act}")
 
 
-# ----------------------------------------------------------------------------- chained decode
+def _every_finite_bf16():
+    bits = np.arange(1 << 16, dtype=np.uint32)
+    return bits[((bits >> 7) & 0xFF) != 0xFF].astype(np.uint16)  # 65280 values, +-0 included
+
+
+@pytest.mark.parametrize("path", ["scalar", "vector", "staged", "bulk", "multi", "prefill_vector",
+                                  "prefill_bulk"])
+def test_silu_every_finite_bf16_input(path):
+    """SiLU of every finite BF16 value (subnormals, +-0, both tails) through each kernel
+    family: weights (0, 0, 0, 1), a zero state and no bias make the accumulator equal x, so
+    out = silu(x); within 1 BF16 ulp of the oracle's double-precision SiLU."""
+    import depthwise_causal_conv1d_gb300 as ccu
+    from oracle_pins import bf16_ulp_distance
+
+    vals = _every_finite_bf16()
+    D = vals.size
+    weight = np.zeros((D, 4), np.uint16)
+    weight[:, 3] = 0x3F80  # 1.0
+    want = oracle.conv1d_update(vals.reshape(1, D), D, np.zeros((1, D, 3), np.uint16), (3 * D, 3, 1),
+                                weight, None, "silu", None, 1, D, 1, 3, 4)[0]
+    w = to_dev_u16(weight, DEV)
+    x2 = np.stack([vals, vals[::-1]])  # two tokens / two rows
+    want2 = np.stack([want, want[::-1]])
+    if path in ("scalar", "vector", "staged", "bulk"):
+        st = torch.zeros((2, D, 3), dtype=torch.bfloat16, device=DEV)
+        got = ccu.causal_conv1d_update(to_dev_u16(x2, DEV), st, w, None, "silu", route=path)
+    elif path == "multi":
+        st = torch.zeros((1, D, 3), dtype=torch.bfloat16, device=DEV)
+        got = ccu.causal_conv1d_update(to_dev_u16(x2[None], DEV).permute(0, 2, 1), st, w, None, "silu")
+        got = got.permute(0, 2, 1)[0]
+    else:
+        x = to_dev_u16(x2[None], DEV).permute(0, 2, 1)  # [1, D, 2], token-major memory
+        got = ccu.causal_conv1d_fwd(x, w, None, "silu", route=path.split("_")[1])
+        got = got.permute(0, 2, 1)[0]
+    torch.cuda.synchronize()
+    dist = bf16_ulp_distance(from_dev_u16(got), want2)
+    assert dist.max() <= 1, vals[np.argmax(dist.max(axis=0))]
+
+
 
 @pytest.mark.parametrize("L,act,layout", [(3, "identity", "compact"), (3, "silu", "channel_last"),
                                           (4, "silu", "compact"), (8, "identity", "channel_last"),
@@ -619,7 +657,7 @@ def _state_dev(arr_bdl, layout):
     return to_dev_u16(np.ascontiguousarray(np.transpose(arr_bdl, (0, 2, 1))), DEV).permute(0, 2, 1)
 
 
-@pytest.mark.parametrize("route", ["auto", "scalar", "vector"])
+@pytest.mark.parametrize("route", ["auto", "scalar", "vector", "bulk"])
 @pytest.mark.parametrize("act", ["identity", "silu"])
 @pytest.mark.parametrize("ci", range(len(PREFILL)))
 def test_prefill(route, act, ci):
@@ -627,8 +665,8 @@ def test_prefill(route, act, ci):
 
     c = PREFILL[ci]
     B, D, T, L = c["B"], c["D"], c["T"], c["L"]
-    if route == "vector" and (D % 8 or c["x_layout"] != "tokens_major"):
-        pytest.skip("the vector kernel needs channel-contiguous 16-byte token rows")
+    if route in ("vector", "bulk") and (D % 8 or c["x_layout"] != "tokens_major"):
+        pytest.skip("the vector and bulk kernels need channel-contiguous 16-byte token rows")
     rng = np.random.default_rng(500 + ci)
     x_btd = synthetic.f64_to_bf16_bits(rng.standard_normal((B, T, D)))
     weight = synthetic.f64_to_bf16_bits(rng.standard_normal((D, 4)) * 0.5)
@@ -658,6 +696,33 @@ def test_prefill(route, act, ci):
     assert bf16_ulp_distance(got_y, want_y).max() <= (0 if act == "identity" else 1)
     if fin_dev is not None:
         assert np.array_equal(from_dev_u16(fin_dev), want_fin)
+
+
+@pytest.mark.parametrize("T", [3, 21])
+def test_prefill_bulk_more_runs_than_warps(T):
+    """B * D / 256 channel runs above the GPU's warp count: every warp of the bulk kernel
+    walks several runs, restarting its window and weights at each (the last slice of every
+    row is partial: D = 16384 + 72)."""
+    import depthwise_causal_conv1d_gb300 as ccu
+
+    rng = np.random.default_rng(77 + T)
+    B, D, L = 40, 16384 + 72, 3
+    x_btd = synthetic.f64_to_bf16_bits(rng.standard_normal((B, T, D)))
+    weight = synthetic.f64_to_bf16_bits(rng.standard_normal((D, 4)) * 0.5)
+    bias = synthetic.f64_to_bf16_bits(rng.standard_normal(D) * 0.1)
+    init = synthetic.f64_to_bf16_bits(rng.standard_normal((B, D, L)))
+    x = to_dev_u16(x_btd, DEV).permute(0, 2, 1)
+    y, fin = ccu.causal_conv1d_fwd(x, to_dev_u16(weight, DEV), to_dev_u16(bias, DEV), "silu",
+                                   initial_states=to_dev_u16(init, DEV), return_final_states=True,
+                                   route="bulk")
+    torch.cuda.synchronize()
+    from oracle_pins import bf16_ulp_distance
+
+    got_y, got_fin = from_dev_u16(y), from_dev_u16(fin)
+    for b in range(B):
+        want_y, want_fin = oracle.full_causal_conv(x_btd[b], weight, bias, "silu", init[b], L)
+        assert bf16_ulp_distance(got_y[b], want_y.T).max() <= 1, b
+        assert np.array_equal(got_fin[b], want_fin), b
 
 
 def test_prefill_hands_off_to_decode():
