@@ -111,6 +111,24 @@ __device__ __forceinline__ float activate(float a) {
   }
 }
 
+// The same SiLU on a pair of channels: the multiplies and adds go through the paired FP32
+// instructions (two IEEE operations each, rounded exactly as the scalar ones), so the result
+// equals activate<ACT> on each half bit for bit.
+template <int ACT>
+__device__ __forceinline__ float2 activate2(float2 a) {
+  if constexpr (ACT == 1) {
+    const float2 es = make_float2(ex2_approx_ftz(fmaf(fabsf(a.x), -1.4426950408889634f, 32.0f)),
+                                  ex2_approx_ftz(fmaf(fabsf(a.y), -1.4426950408889634f, 32.0f)));
+    const float2 e = __fmul2_rn(es, make_float2(0x1p-32f, 0x1p-32f));
+    const float2 d = __fadd2_rn(e, make_float2(1.0f, 1.0f));
+    const float2 ae = __fmul2_rn(a, e);
+    return __fmul2_rn(make_float2(fmaxf(a.x, ae.x), fmaxf(a.y, ae.y)),
+                      make_float2(rcp_approx_ftz(d.x), rcp_approx_ftz(d.y)));
+  } else {
+    return a;
+  }
+}
+
 // Streaming (evict-first) 16-byte global accesses for data touched once per call.
 __device__ __forceinline__ uint4 ld_stream(const uint16_t *p) {
   return __ldcs(reinterpret_cast<const uint4 *>(p));

@@ -76,8 +76,88 @@ __global__ void __launch_bounds__(256) k_prefill_scalar(UpdateParams p, PrefillP
   }
 }
 
+// Widen 8 packed BF16 to 4 float pairs (channels 2i, 2i+1).
+__device__ __forceinline__ void widen8(const uint4 v, float2 (&f)[4]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) f[i] = make_float2(bf16_lo(w[i]), bf16_hi(w[i]));
+}
+
+// The width-4 weights of channels c0..c0+7 as float pairs: wf[j][i] = weight[c0 + 2i (+1), j].
+__device__ __forceinline__ void load_weights_f(const UpdateParams &p, int64_t c0, float2 (&wf)[kW][4]) {
+  const uint16_t *wp = p.w + c0 * kW;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {  // 16 bytes = channels 2k, 2k+1, all four taps each
+    const uint4 t = ld_keep(wp + 8 * k);
+    wf[0][k] = make_float2(bf16_lo(t.x), bf16_lo(t.z));
+    wf[1][k] = make_float2(bf16_hi(t.x), bf16_hi(t.z));
+    wf[2][k] = make_float2(bf16_lo(t.y), bf16_lo(t.w));
+    wf[3][k] = make_float2(bf16_hi(t.y), bf16_hi(t.w));
+  }
+}
+
+// Outputs of 8 channels (4 pairs) for one token from the window a, b, c (oldest first) and
+// the token's inputs x. The accumulation order is the update's: ((0 + a*w0) + b*w1) + c*w2 +
+// x*w3, then the bias (each product of two BF16 values is exact in FP32); the paired FP32
+// instructions round each half exactly as the scalar ones.
+template <int ACT>
+__device__ __forceinline__ uint4 outputs8f(const float2 (&wf)[kW][4], const float2 (&bf)[4],
+                                           bool has_bias, const float2 (&a)[4], const float2 (&b)[4],
+                                           const float2 (&c)[4], const float2 (&x)[4]) {
+  uint32_t y[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 acc = __ffma2_rn(a[i], wf[0][i], make_float2(0.0f, 0.0f));
+    acc = __ffma2_rn(b[i], wf[1][i], acc);
+    acc = __ffma2_rn(c[i], wf[2][i], acc);
+    acc = __ffma2_rn(x[i], wf[3][i], acc);
+    if (has_bias) acc = __fadd2_rn(acc, bf[i]);
+    const float2 v = activate2<ACT>(acc);
+    y[i] = pack_bf16x2(v.x, v.y);
+  }
+  return make_uint4(y[0], y[1], y[2], y[3]);
+}
+
+// The window before token t0 for channels c0..c0+7: inputs t0-3, t0-2, t0-1 (from x, or the
+// initial state / zeros before the sequence).
+__device__ __forceinline__ void load_halo(const UpdateParams &p, const PrefillParams &f, int64_t b,
+                                          int64_t c0, int64_t t0, float2 (&h0)[4], float2 (&h1)[4],
+                                          float2 (&h2)[4]) {
+  const uint16_t *xb = p.x + b * f.sxb + c0;
+  float2 *hs[3] = {h0, h1, h2};
+#pragma unroll
+  for (int k = 0; k < kW - 1; ++k) {
+    const int64_t t = t0 - (kW - 1) + k;
+    if (t >= 0) {
+      float2 tmp[4];
+      widen8(ld_keep(xb + t * f.sxt), tmp);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) hs[k][i] = tmp[i];
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        hs[k][i] = make_float2(bf16_bits(input_at(p, f, b, c0 + 2 * i, t)),
+                               bf16_bits(input_at(p, f, b, c0 + 2 * i + 1, t)));
+    }
+  }
+}
+
+// The window slides by one token: (h0, h1, h2) <- (h1, h2, x).
+__device__ __forceinline__ void slide(float2 (&h0)[4], float2 (&h1)[4], float2 (&h2)[4],
+                                      const float2 (&x)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    h0[i] = h1[i];
+    h1[i] = h2[i];
+    h2[i] = x[i];
+  }
+}
+
+// Scalar-float forms of the helpers below, for the vector kernel (paired FP32 arithmetic
+// made it spill at 128 registers).
+
 // Widen 8 packed BF16 to floats.
-__device__ __forceinline__ void widen8(const uint4 v, float (&f)[8]) {
+__device__ __forceinline__ void widen8s(const uint4 v, float (&f)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -87,7 +167,7 @@ __device__ __forceinline__ void widen8(const uint4 v, float (&f)[8]) {
 }
 
 // The width-4 weights of channels c0..c0+7 as floats: wf[j][c] = weight[c0 + c, j].
-__device__ __forceinline__ void load_weights_f(const UpdateParams &p, int64_t c0, float (&wf)[kW][8]) {
+__device__ __forceinline__ void load_weights_s(const UpdateParams &p, int64_t c0, float (&wf)[kW][8]) {
   const uint16_t *wp = p.w + c0 * kW;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
@@ -106,7 +186,7 @@ __device__ __forceinline__ void load_weights_f(const UpdateParams &p, int64_t c0
 // inputs x. The accumulation order is the update's: ((0 + a*w0) + b*w1) + c*w2 + x*w3, then
 // the bias (each product of two BF16 values is exact in FP32).
 template <int ACT>
-__device__ __forceinline__ uint4 outputs8f(const float (&wf)[kW][8], const float (&bf)[8],
+__device__ __forceinline__ uint4 outputs8s(const float (&wf)[kW][8], const float (&bf)[8],
                                            bool has_bias, const float (&a)[8], const float (&b)[8],
                                            const float (&c)[8], const float (&x)[8]) {
   float y[8];
@@ -125,7 +205,7 @@ __device__ __forceinline__ uint4 outputs8f(const float (&wf)[kW][8], const float
 
 // The window before token t0 for channels c0..c0+7: inputs t0-3, t0-2, t0-1 (from x, or the
 // initial state / zeros before the sequence).
-__device__ __forceinline__ void load_halo(const UpdateParams &p, const PrefillParams &f, int64_t b,
+__device__ __forceinline__ void load_halo_s(const UpdateParams &p, const PrefillParams &f, int64_t b,
                                           int64_t c0, int64_t t0, float (&h0)[8], float (&h1)[8],
                                           float (&h2)[8]) {
   const uint16_t *xb = p.x + b * f.sxb + c0;
@@ -135,7 +215,7 @@ __device__ __forceinline__ void load_halo(const UpdateParams &p, const PrefillPa
     const int64_t t = t0 - (kW - 1) + k;
     if (t >= 0) {
       float tmp[8];
-      widen8(ld_keep(xb + t * f.sxt), tmp);
+      widen8s(ld_keep(xb + t * f.sxt), tmp);
 #pragma unroll
       for (int c = 0; c < 8; ++c) hs[k][c] = tmp[c];
     } else {
@@ -164,21 +244,21 @@ __global__ void __launch_bounds__(256) k_prefill_vector(UpdateParams p, PrefillP
   const int64_t t1 = t0 + f.chunk < f.T ? t0 + f.chunk : f.T;
 
   float wf[kW][8];  // wf[j][c] = weight[c0 + c, j]
-  load_weights_f(p, c0, wf);
+  load_weights_s(p, c0, wf);
   const bool has_bias = p.bias != nullptr;
   float bf[8];
   if (has_bias) {
-    widen8(ld_keep(p.bias + c0), bf);
+    widen8s(ld_keep(p.bias + c0), bf);
   }
 
   // The window before the chunk: inputs t0-3, t0-2, t0-1 (from x, or the initial state).
   float h0[8], h1[8], h2[8];
-  load_halo(p, f, b, c0, t0, h0, h1, h2);
+  load_halo_s(p, f, b, c0, t0, h0, h1, h2);
   const uint16_t *xb = p.x + b * f.sxb + c0;
 
   auto outputs = [&](const float (&a)[8], const float (&bb)[8], const float (&cc)[8],
                      const float (&xx)[8]) -> uint4 {
-    return outputs8f<ACT>(wf, bf, has_bias, a, bb, cc, xx);
+    return outputs8s<ACT>(wf, bf, has_bias, a, bb, cc, xx);
   };
 
   uint16_t *ob = p.out + b * f.sob + c0;
@@ -195,10 +275,10 @@ __global__ void __launch_bounds__(256) k_prefill_vector(UpdateParams p, PrefillP
       for (int k = 0; k < 4; ++k) nx[k] = ld_stream(xb + (t + 4 + k) * f.sxt);
     }
     float x0[8], x1[8], x2[8], x3[8];
-    widen8(cx[0], x0);
-    widen8(cx[1], x1);
-    widen8(cx[2], x2);
-    widen8(cx[3], x3);
+    widen8s(cx[0], x0);
+    widen8s(cx[1], x1);
+    widen8s(cx[2], x2);
+    widen8s(cx[3], x3);
     st_stream(ob + t * f.sot, outputs(h0, h1, h2, x0));
     st_stream(ob + (t + 1) * f.sot, outputs(h1, h2, x0, x1));
     st_stream(ob + (t + 2) * f.sot, outputs(h2, x0, x1, x2));
@@ -212,7 +292,7 @@ __global__ void __launch_bounds__(256) k_prefill_vector(UpdateParams p, PrefillP
   }
   for (; t < t1; ++t) {  // the chunk's last 0..3 tokens
     float x0[8];
-    widen8(ld_stream(xb + t * f.sxt), x0);
+    widen8s(ld_stream(xb + t * f.sxt), x0);
     st_stream(ob + t * f.sot, outputs(h0, h1, h2, x0));
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
@@ -236,14 +316,16 @@ __global__ void __launch_bounds__(256) k_prefill_vector(UpdateParams p, PrefillP
 // kTG tokens at a time (one 512-byte cp.async.bulk per token) into a kP-stage ring that
 // completes on per-stage mbarriers, the lanes slide their float windows through the stage
 // from shared memory and store the outputs as 16-byte streaming stores, and the stage is
-// refilled kP groups ahead. A warp's run is long (the runs are sized so that there is about
-// one per warp), so the 3-token halo and the weights are read once per run. Every mbarrier
-// wait is bounded: on expiry the warp raises CCU_DEVERR_TIMEOUT, waits (bounded) for its own
-// copies and returns.
+// refilled kP groups ahead. The warps share the groups evenly (see Run below); a warp's runs
+// are long, so the 3-token halo and the weights are read rarely. At 4 bytes per element the
+// SiLU prefill is bound by instruction issue rather than by HBM, so the arithmetic runs on
+// channel pairs with the paired FP32 instructions (half the multiply-add instructions,
+// identical rounding). Every mbarrier wait is bounded: on expiry the warp raises
+// CCU_DEVERR_TIMEOUT, waits (bounded) for its own copies and returns.
 
 __device__ int32_t g_prefill_error = 0;  // CCU_DEVERR_* bits raised by the bulk prefill
 
-constexpr int kPThreads = 512;                 // 16 warps per CTA
+constexpr int kPThreads = 384;                 // 12 warps per CTA, up to 170 registers each
 constexpr int kPWarps = kPThreads / 32;
 constexpr int64_t kRunCh = 256;                // channels per warp (8 per lane)
 constexpr int64_t kRowBytes = 2 * kRunCh;      // one token of a run
@@ -253,42 +335,47 @@ constexpr int64_t kStageBytes = kTG * kRowBytes;
 constexpr int64_t kHeadBytes = 128;  // per warp: kP mbarriers, then the producer cursor
 constexpr int64_t kWarpBytes = kHeadBytes + kP * kStageBytes;
 
-// One run: batch row b, channels c_base .. c_base+cn-1, tokens t0 .. t1-1.
+// The work is the flattened space of groups (pair, g): pair = b * slices + s is a batch row
+// and a 256-channel slice, g = 0 .. ceil(T / kTG) - 1 its kTG-token groups. Each warp takes
+// one contiguous span of it, the same length to one group, so the warps finish together
+// whatever B, D and T are. A span crosses pair boundaries where it must: the stretch of a
+// span inside one pair is a run, over which the window slides without a restart.
 struct Run {
-  int64_t b, c_base, cn, t0, t1;
+  int64_t b, c_base, cn, t0, t1;  // batch row, channels c_base .. c_base+cn-1, tokens t0 .. t1-1
+  int64_t next;                   // the group where the span's next run starts
 };
 
-// Run i, with the channel slice fastest so that neighbouring warps read neighbouring bytes
-// of the same tokens.
-__device__ __forceinline__ Run run_of(const UpdateParams &p, const PrefillParams &f, int64_t i,
-                                      int64_t slices, int64_t chunks) {
+// The run that starts at group q of a span ending at group q_end.
+__device__ __forceinline__ Run run_at(const UpdateParams &p, const PrefillParams &f, int64_t q,
+                                      int64_t q_end, int64_t slices, int64_t groups) {
   Run r;
-  const int64_t s = i % slices;
-  const int64_t rest = i / slices;
-  r.b = rest / chunks;
-  r.c_base = s * kRunCh;
+  const int64_t pair = q / groups;
+  const int64_t pair_end = (pair + 1) * groups;
+  r.next = q_end < pair_end ? q_end : pair_end;
+  r.b = pair / slices;
+  r.c_base = (pair - r.b * slices) * kRunCh;
   const int64_t rem = p.D - r.c_base;
   r.cn = rem < kRunCh ? rem : kRunCh;
-  r.t0 = (rest % chunks) * f.chunk;
-  r.t1 = r.t0 + f.chunk < f.T ? r.t0 + f.chunk : f.T;
+  r.t0 = (q - pair * groups) * kTG;
+  const int64_t t1 = (r.next - pair * groups) * kTG;
+  r.t1 = t1 < f.T ? t1 : f.T;
   return r;
 }
 
 // Lane 0's producer cursor: the next group's first x row, the tokens of its run from there,
-// the row bytes, the warp's run index m, the stage of the next load and the loads issued but
-// not yet consumed. It lives in shared memory, out of the registers the lanes need for their
-// windows and weights.
+// the row bytes, the group where the next run starts, the stage of the next load and the
+// loads issued but not yet consumed. It lives in shared memory, out of the registers the
+// lanes need for their windows and weights.
 struct Cursor {
   const uint16_t *src;
-  int64_t left, m;
+  int64_t left, next;
   uint32_t bytes;
   int st, inflight;
 };
 static_assert(kP * 8 + 8 + sizeof(Cursor) <= kHeadBytes, "warp header too small");
 
 template <int ACT>
-__global__ void __launch_bounds__(kPThreads, 1) k_prefill_bulk(UpdateParams p, PrefillParams f,
-                                                               int64_t chunks) {
+__global__ void __launch_bounds__(kPThreads, 1) k_prefill_bulk(UpdateParams p, PrefillParams f) {
   using namespace bulk;
   extern __shared__ __align__(128) unsigned char smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -297,25 +384,29 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_bulk(UpdateParams p, P
   Cursor *cur = reinterpret_cast<Cursor *>(wbase + 8 * ((kP + 1) & ~1));
   unsigned char *bufs = wbase + kHeadBytes;
 
+  // This warp's span [q0, q1) of the B * slices * groups groups.
   const int64_t slices = (p.D + kRunCh - 1) / kRunCh;
-  const int64_t runs = f.B * slices * chunks;
-  const int64_t first_run = (int64_t)blockIdx.x * kPWarps + warp;
-  const int64_t stride = (int64_t)gridDim.x * kPWarps;
-  const int64_t mine = runs > first_run ? (runs - first_run + stride - 1) / stride : 0;
-  if (mine == 0) return;
+  const int64_t groups = (f.T + kTG - 1) / kTG;
+  const int64_t total = f.B * slices * groups;
+  const int64_t nw = (int64_t)gridDim.x * kPWarps;
+  const int64_t w = (int64_t)blockIdx.x * kPWarps + warp;
+  const int64_t share = total / nw, extra = total % nw;
+  const int64_t q0 = w * share + (w < extra ? w : extra);
+  const int64_t q1 = q0 + share + (w < extra ? 1 : 0);
+  if (q0 >= q1) return;
 
-  // Lane 0: point the cursor at the start of the warp's m-th run.
-  auto start_run = [&](Cursor &c, int64_t m) {
-    const Run r = run_of(p, f, first_run + m * stride, slices, chunks);
+  // Lane 0: point the cursor at the run that starts at group q.
+  auto start_run = [&](Cursor &c, int64_t q) {
+    const Run r = run_at(p, f, q, q1, slices, groups);
     c.src = p.x + r.b * f.sxb + r.t0 * f.sxt + r.c_base;
     c.left = r.t1 - r.t0;
     c.bytes = (uint32_t)(r.cn * 2);
-    c.m = m;
+    c.next = r.next;
   };
   // Lane 0: load the cursor's group (up to kTG tokens) into its stage and advance.
   auto issue_next = [&]() {
     Cursor c = *cur;
-    if (c.m >= mine) return;
+    if (c.left == 0) return;  // the span is all issued
     const int nt = c.left < kTG ? (int)c.left : kTG;
     uint64_t *bar = &bars[c.st];
     unsigned char *buf = bufs + c.st * kStageBytes;
@@ -325,20 +416,14 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_bulk(UpdateParams p, P
     if (++c.st == kP) c.st = 0;
     c.left -= nt;
     c.src += nt * f.sxt;
-    if (c.left == 0) {
-      if (c.m + 1 < mine) {
-        start_run(c, c.m + 1);
-      } else {
-        c.m = mine;
-      }
-    }
+    if (c.left == 0 && c.next < q1) start_run(c, c.next);
     *cur = c;
   };
   if (lane == 0) {
     for (int k = 0; k < kP; ++k) mbar_init(&bars[k], 1);
     fence_mbar_init();
     Cursor c;
-    start_run(c, 0);
+    start_run(c, q0);
     c.st = 0;
     c.inflight = 0;
     *cur = c;
@@ -347,14 +432,15 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_bulk(UpdateParams p, P
   __syncwarp();
 
   const bool has_bias = p.bias != nullptr;
-  float wf[kW][8], bf[8], h0[8], h1[8], h2[8];
+  float2 wf[kW][4], bf[4], h0[4], h1[4], h2[4];
   int64_t w_base = -1;
   int st = 0;
   uint32_t phase = 0;
   bool failed = false;
-  for (int64_t m = 0; m < mine && !failed; ++m) {
+  for (int64_t q = q0; q < q1 && !failed;) {
     // A new run: weights (when the channels change) and the halo.
-    const Run r = run_of(p, f, first_run + m * stride, slices, chunks);
+    const Run r = run_at(p, f, q, q1, slices, groups);
+    q = r.next;
     const bool active = 8 * lane < r.cn;
     const int64_t c0 = r.c_base + 8 * lane;
     if (active) {
@@ -379,27 +465,17 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_bulk(UpdateParams p, P
         if (left >= kTG) {
 #pragma unroll
           for (int k = 0; k < kTG; ++k) {  // unrolled: the window slides by register renaming
-            float xk[8];
+            float2 xk[4];
             widen8(row[k * (kRowBytes / 16)], xk);
             st_stream(ob + k * f.sot, outputs8f<ACT>(wf, bf, has_bias, h0, h1, h2, xk));
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              h0[c] = h1[c];
-              h1[c] = h2[c];
-              h2[c] = xk[c];
-            }
+            slide(h0, h1, h2, xk);
           }
         } else {
           for (int k = 0; k < (int)left; ++k) {
-            float xk[8];
+            float2 xk[4];
             widen8(row[k * (kRowBytes / 16)], xk);
             st_stream(ob + k * f.sot, outputs8f<ACT>(wf, bf, has_bias, h0, h1, h2, xk));
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              h0[c] = h1[c];
-              h1[c] = h2[c];
-              h2[c] = xk[c];
-            }
+            slide(h0, h1, h2, xk);
           }
         }
         if (ends && left <= kTG) {
@@ -454,18 +530,11 @@ cudaError_t launch_prefill_bulk_act(const UpdateParams &p, PrefillParams f, cuda
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   const int64_t ctas = (int64_t)device_sm_count() * per_sm;
-  // Runs: split each (batch row, channel slice) pair's tokens so that there is about one run
-  // per warp; a run is a whole number of kTG-token groups.
-  const int64_t pairs = f.B * ((p.D + kRunCh - 1) / kRunCh);
-  int64_t chunks = ctas * kPWarps / pairs;
-  if (chunks < 1) chunks = 1;
-  int64_t chunk = (f.T + chunks - 1) / chunks;
-  chunk = (chunk + kTG - 1) / kTG * kTG;
-  chunks = (f.T + chunk - 1) / chunk;
-  f.chunk = chunk;
-  int64_t grid = (pairs * chunks + kPWarps - 1) / kPWarps;
+  // One CTA per SM (fewer when there are fewer groups than warps to share them).
+  const int64_t groups = f.B * ((p.D + kRunCh - 1) / kRunCh) * ((f.T + kTG - 1) / kTG);
+  int64_t grid = (groups + kPWarps - 1) / kPWarps;
   if (grid > ctas) grid = ctas;
-  k_prefill_bulk<ACT><<<(unsigned)grid, kPThreads, smem, stream>>>(p, f, chunks);
+  k_prefill_bulk<ACT><<<(unsigned)grid, kPThreads, smem, stream>>>(p, f);
   return cudaGetLastError();
 }
 

@@ -615,8 +615,9 @@ def test_multi_token(route, layout, ci):
     assert bf16_ulp_distance(got_out, want_out).max() <= 1, "outputs"
 
 
-def test_multi_large_batch():
-    """A large multi-token batch (N=1024, D=16384, T=4, ring state) on the vector kernel."""
+@pytest.mark.parametrize("route", ["auto", "vector"])
+def test_multi_large_batch(route):
+    """A large multi-token batch (N=1024, D=16384, T=4, ring state)."""
     import depthwise_causal_conv1d_gb300 as ccu
 
     case = dict(N=1024, D=16384, T=4, L=3, S=1024, ring=True, x_layout="tokens_major")
@@ -629,10 +630,40 @@ def test_multi_large_batch():
     st = to_dev_u16(state, DEV)
     out = ccu.causal_conv1d_update(x, st, to_dev_u16(weight, DEV), to_dev_u16(bias, DEV), "silu",
                                    conv_state_indices=torch.from_numpy(idx).to(DEV),
-                                   cache_seqlens=torch.from_numpy(seq).to(DEV))
+                                   cache_seqlens=torch.from_numpy(seq).to(DEV), route=route)
     torch.cuda.synchronize()
     from oracle_pins import bf16_ulp_distance
 
+    assert np.array_equal(from_dev_u16(st), st_ref)
+    assert bf16_ulp_distance(from_dev_u16(out.permute(0, 2, 1)).transpose(0, 2, 1), want_out).max() <= 1
+
+
+@pytest.mark.parametrize("route", ["scalar", "vector"])
+def test_multi_token_checked_bad_index(route):
+    """Checked multi-token call: an out-of-range slot raises CCU_DEVERR_RANGE and its row
+    behaves as padding (zero outputs, no state access); the other rows are exact."""
+    import depthwise_causal_conv1d_gb300 as ccu
+
+    case = dict(N=9, D=1032, T=4, L=3, S=12, ring=False, x_layout="tokens_major")
+    N, D, T, L, S = case["N"], case["D"], case["T"], case["L"], case["S"]
+    x_tok, weight, bias, state, idx, _ = _multi_inputs(case, 41)
+    bad = idx.copy()
+    bad[4] = S + 3
+    ref_idx = idx.copy()
+    ref_idx[4] = -1
+    st_ref = state.copy()
+    want_out = oracle.conv1d_update_multi(x_tok, (T * D, 1, D), st_ref, (D * L, L, 1), weight, bias,
+                                          "silu", ref_idx, None, N, D, T, S, L, 4)
+    st = to_dev_u16(state, DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = ccu.causal_conv1d_update(to_dev_u16(x_tok, DEV).permute(0, 2, 1), st, to_dev_u16(weight, DEV),
+                                   to_dev_u16(bias, DEV), "silu",
+                                   conv_state_indices=torch.from_numpy(bad).to(DEV), route=route,
+                                   status=status)
+    torch.cuda.synchronize()
+    from oracle_pins import bf16_ulp_distance
+
+    assert int(status.item()) & 1
     assert np.array_equal(from_dev_u16(st), st_ref)
     assert bf16_ulp_distance(from_dev_u16(out.permute(0, 2, 1)).transpose(0, 2, 1), want_out).max() <= 1
 
@@ -723,6 +754,36 @@ def test_prefill_bulk_more_runs_than_warps(T):
         want_y, want_fin = oracle.full_causal_conv(x_btd[b], weight, bias, "silu", init[b], L)
         assert bf16_ulp_distance(got_y[b], want_y.T).max() <= 1, b
         assert np.array_equal(got_fin[b], want_fin), b
+
+
+def test_prefill_host_resident_x_and_out():
+    """x and out in pinned host memory: AUTO runs the vector kernel on them in place (the
+    bulk kernel's copies need device memory, and a forced bulk route declines)."""
+    import depthwise_causal_conv1d_gb300 as ccu
+    from oracle_pins import bf16_ulp_distance
+
+    rng = np.random.default_rng(13)
+    B, T, D, L = 2, 600, 1024, 3
+    assert B * T * D >= 1 << 20  # device operands this size would take the bulk route
+    x_btd = synthetic.f64_to_bf16_bits(rng.standard_normal((B, T, D)))
+    weight = synthetic.f64_to_bf16_bits(rng.standard_normal((D, 4)) * 0.5)
+    bias = synthetic.f64_to_bf16_bits(rng.standard_normal(D) * 0.1)
+    h_x = torch.from_numpy(x_btd.view(np.int16)).pin_memory()
+    h_out = torch.full((B, T, D), -1, dtype=torch.int16).pin_memory()
+    w, b = to_dev_u16(weight, DEV), to_dev_u16(bias, DEV)
+    fin = torch.zeros((B, L, D), dtype=torch.int16, device=DEV)
+    stream = torch.cuda.current_stream().cuda_stream
+    args = (h_x.data_ptr(), T * D, 1, D, w.data_ptr(), b.data_ptr(), ccu.CCU_ACT_SILU, None, 0, 0, 0,
+            B, D, T, L, 4, h_out.data_ptr(), T * D, 1, D, fin.data_ptr(), L * D, 1, D)
+    assert ccu.ccu_causal_conv1d_fwd(*args, ccu.ROUTES["bulk"], stream) == ccu.CCU_ERR_NOT_IMPLEMENTED
+    assert ccu.ccu_causal_conv1d_fwd(*args, ccu.ROUTES["auto"], stream) == 0, ccu.ccu_conv1d_last_error()
+    torch.cuda.synchronize()
+    got = h_out.numpy().view(np.uint16)
+    got_fin = fin.cpu().numpy().view(np.uint16)
+    for bb in range(B):
+        want, want_fin = oracle.full_causal_conv(x_btd[bb], weight, bias, "silu", None, L)
+        assert bf16_ulp_distance(got[bb], want).max() <= 1
+        assert np.array_equal(got_fin[bb].T, want_fin)
 
 
 def test_prefill_hands_off_to_decode():
