@@ -638,6 +638,31 @@ def test_multi_large_batch(route):
     assert bf16_ulp_distance(from_dev_u16(out.permute(0, 2, 1)).transpose(0, 2, 1), want_out).max() <= 1
 
 
+@pytest.mark.parametrize("T", [1, 25])
+def test_multi_token_vector_extremes(T):
+    """The vector kernel at one token and at T = 25 (six groups of four tokens and a
+    remainder of one), N = 2 rows, ring state, intermediate states."""
+    import depthwise_causal_conv1d_gb300 as ccu
+    from oracle_pins import bf16_ulp_distance
+
+    case = dict(N=2, D=2048, T=T, L=3, S=3, ring=True, x_layout="tokens_major")
+    N, D, L, S = case["N"], case["D"], case["L"], case["S"]
+    x_tok, weight, bias, state, idx, seq = _multi_inputs(case, 60 + T)
+    st_ref = state.copy()
+    want_out, want_inter = oracle.conv1d_update_multi(x_tok, (T * D, 1, D), st_ref, (D * L, L, 1), weight,
+                                                      bias, "silu", idx, seq, N, D, T, S, L, 4, with_inter=True)
+    st = to_dev_u16(state, DEV)
+    inter = torch.zeros((N, T, D, L), dtype=torch.bfloat16, device=DEV)
+    args = dict(conv_state_indices=torch.from_numpy(idx).to(DEV), cache_seqlens=torch.from_numpy(seq).to(DEV))
+    out = ccu.causal_conv1d_update(to_dev_u16(x_tok, DEV).permute(0, 2, 1), st, to_dev_u16(weight, DEV),
+                                   to_dev_u16(bias, DEV), "silu", route="vector", intermediate_states=inter,
+                                   **args)
+    torch.cuda.synchronize()
+    assert np.array_equal(from_dev_u16(st), st_ref)
+    assert np.array_equal(from_dev_u16(inter), want_inter)
+    assert bf16_ulp_distance(from_dev_u16(out.permute(0, 2, 1)).transpose(0, 2, 1), want_out).max() <= 1
+
+
 @pytest.mark.parametrize("route", ["scalar", "vector"])
 def test_multi_token_checked_bad_index(route):
     """Checked multi-token call: an out-of-range slot raises CCU_DEVERR_RANGE and its row
