@@ -87,25 +87,25 @@ __device__ __forceinline__ float rcp_approx_ftz(float x) {
 }
 
 // The activation, a compile-time choice: identity kernels carry no SiLU code.
-// SiLU is a * sigmoid(a). With e = exp(-|a|) in (0, 1], sigmoid(a) = 1 / (1 + e) for
-// a >= 0 and e / (1 + e) for a < 0, so a * sigmoid(a) = (a >= 0 ? a : a * e) / (1 + e)
-// = max(a, a * e) / (1 + e), since e <= 1 makes a >= a * e exactly when a >= 0. No step
-// overflows for any finite a (a / (1 + exp(-a)) overflows to -0 below a ~ -88.7, where the
-// true value is still a representable float). The exponential is taken as
-// 2^(32 - |a| log2 e) = e * 2^32, a normal float for |a| < 109, and brought back with a
-// power-of-two multiply: exact while e is normal, and below 2^-126 an absolute error under
-// 1e-45, far below the BF16 subnormal step of ~9e-41 that a * e is rounded to (the
-// flushing approximation alone would zero e below a ~ -87.3, where a * e still rounds to a
-// nonzero BF16). Below a ~ -109 the true value rounds to -0 in BF16 as well. 1 + e lies in
-// [1, 2], where rcp.approx is accurate. The error is a few float ulps, far below the half
-// BF16 ulp (2^15 float ulps) the result keeps, so the rounded output stays within one BF16
-// ulp of the exact value. Eight arithmetic operations: the kernels that move 4 bytes per
-// element are issue-bound on the SiLU.
+// SiLU is a * sigmoid(a) with sigmoid(a) = 1 / (1 + exp(-a)). In float, exp(-a) overflows
+// below a ~ -88.7, where a * sigmoid(a) is still a representable float (a version that
+// returned -0 there failed the extreme-value parity test). So the exponential is taken
+// scaled down by 2^32,
+//   v = 2^(-a log2 e - 32) = exp(-a) 2^-32           finite down to a ~ -110.9,
+//   sigmoid(a) = 2^-32 / (v + 2^-32) = rcp(v + 2^-32) * 2^-32,
+// with ex2.approx and rcp.approx. For a > ~65, v flushes to zero and sigmoid is exactly 1, so
+// nothing overflows for any finite a. Below a ~ -87.3 the final multiply makes sigmoid a
+// float subnormal, with an absolute error under 1e-45, far below the ~9e-41 BF16 subnormal
+// step that a * sigmoid(a) is rounded to; below a ~ -103 it is 0, and a * sigmoid(a) rounds
+// to -0 in BF16 anyway. Elsewhere the error is a few float ulps, far below the half BF16 ulp
+// (2^15 float ulps) the result keeps, so the rounded output stays within one BF16 ulp of
+// the exact value. Six operations (four a channel in the paired form below): the kernels
+// that move 4 bytes per element are issue-bound on the SiLU.
 template <int ACT>
 __device__ __forceinline__ float activate(float a) {
   if constexpr (ACT == 1) {
-    const float e = ex2_approx_ftz(fmaf(fabsf(a), -1.4426950408889634f, 32.0f)) * 0x1p-32f;
-    return fmaxf(a, a * e) * rcp_approx_ftz(1.0f + e);
+    const float v = ex2_approx_ftz(fmaf(a, -1.4426950408889634f, -32.0f));
+    return a * (rcp_approx_ftz(v + 0x1p-32f) * 0x1p-32f);
   } else {
     return a;
   }
@@ -117,13 +117,13 @@ __device__ __forceinline__ float activate(float a) {
 template <int ACT>
 __device__ __forceinline__ float2 activate2(float2 a) {
   if constexpr (ACT == 1) {
-    const float2 es = make_float2(ex2_approx_ftz(fmaf(fabsf(a.x), -1.4426950408889634f, 32.0f)),
-                                  ex2_approx_ftz(fmaf(fabsf(a.y), -1.4426950408889634f, 32.0f)));
-    const float2 e = __fmul2_rn(es, make_float2(0x1p-32f, 0x1p-32f));
-    const float2 d = __fadd2_rn(e, make_float2(1.0f, 1.0f));
-    const float2 ae = __fmul2_rn(a, e);
-    return __fmul2_rn(make_float2(fmaxf(a.x, ae.x), fmaxf(a.y, ae.y)),
-                      make_float2(rcp_approx_ftz(d.x), rcp_approx_ftz(d.y)));
+    const float2 t = __ffma2_rn(a, make_float2(-1.4426950408889634f, -1.4426950408889634f),
+                                make_float2(-32.0f, -32.0f));
+    const float2 d = __fadd2_rn(make_float2(ex2_approx_ftz(t.x), ex2_approx_ftz(t.y)),
+                                make_float2(0x1p-32f, 0x1p-32f));
+    const float2 sig = __fmul2_rn(make_float2(rcp_approx_ftz(d.x), rcp_approx_ftz(d.y)),
+                                  make_float2(0x1p-32f, 0x1p-32f));
+    return __fmul2_rn(a, sig);
   } else {
     return a;
   }
