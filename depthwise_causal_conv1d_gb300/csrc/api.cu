@@ -110,13 +110,20 @@ ccu_status_t validate(const Args &a, bool *noop, Layout *layout) {
   return CCU_OK;
 }
 
-bool route_serves(int route, const Args &a, Layout /*layout*/) {
+// The bulk family is compiled for width 4 with L <= 8 (both layouts) and, in the compact
+// layout, for widths 2 and 3 with L <= 4 (the short states those widths are used with).
+constexpr int64_t kBulkNarrowMaxL = 4;
+
+bool route_serves(int route, const Args &a, Layout layout) {
   const bool vec8 = (a.D % 8 == 0) && (a.ld % 8 == 0);
   switch (route) {
     case CCU_ROUTE_SCALAR: return true;
     case CCU_ROUTE_VECTOR: return vec8 && a.L <= kVectorMaxL;
     case CCU_ROUTE_STAGED: return vec8 && a.L <= kStagedMaxL;
-    case CCU_ROUTE_BULK: return vec8 && a.L <= kVectorMaxL && a.W == kW;
+    case CCU_ROUTE_BULK:
+      if (!vec8) return false;
+      if (a.W == kW) return a.L <= kVectorMaxL;
+      return layout == Layout::Compact && a.L <= kBulkNarrowMaxL;
     default: return false;
   }
 }
@@ -133,7 +140,9 @@ ccu_status_t choose(int requested, const Args &a, Layout layout, int *chosen) {
     // Large batches with the compact state take the bulk kernel. The channel-last state is
     // already one 16-byte vector per plane and thread, and measured faster on the vector
     // kernel at every size (large batch: 160 vs 165 us linear, 146 vs 164 us ring).
-    if (a.N * a.D >= kBulkMinElements && layout == Layout::Compact &&
+    // A one-entry state (L = 1) moves 8 bytes per element: too little per 512-channel slice
+    // for the bulk pipeline (large batch, W = 2: 100.8 us bulk, 80.7 us vector).
+    if (a.N * a.D >= kBulkMinElements && layout == Layout::Compact && a.L >= 2 &&
         route_serves(CCU_ROUTE_BULK, a, layout)) {
       *chosen = CCU_ROUTE_BULK;
     } else if (route_serves(CCU_ROUTE_VECTOR, a, layout)) {

@@ -1,6 +1,6 @@
-// Bulk-copy kernel for large batches (compact state layout, width 4, L = 3..8, D % 8 == 0,
-// linear or ring-buffer state; the channel-last layout has its own bulk kernel in
-// k_bulk_planes.cu).
+// Bulk-copy kernel for large batches (compact state layout, D % 8 == 0, linear or
+// ring-buffer state; width 4 with L = 3..8, widths 2 and 3 with L = W-1..4; the channel-last
+// layout has its own bulk kernel in k_bulk_planes.cu, width 4).
 //
 // Every warp is an independent pipeline. Its work items are slices (row n, 256*G
 // consecutive channels); lane 0 moves whole slices between global and shared memory with
@@ -35,7 +35,7 @@ using namespace bulk;
 
 // Shared memory per warp: kBarrierBytes of mbarriers, then P stages of stage_bytes.
 // RING: conv_state is a ring buffer indexed by cache_seqlens (entry q replaced by x).
-template <int L, int ACT, int G, bool RING>
+template <int L, int W, int ACT, int G, bool RING>
 __global__ void __launch_bounds__(kThreads) k_update_bulk(UpdateParams p, int stages, int64_t stage_bytes) {
   constexpr int64_t kSlice = 256 * G;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -93,12 +93,7 @@ __global__ void __launch_bounds__(kThreads) k_update_bulk(UpdateParams p, int st
       for (int g = 0; g < G; ++g) {
         const int64_t c = sl.c_base + 8 * (lane + 32 * g);
         if (8 * (lane + 32 * g) < sl.cn) {
-          const uint16_t *wp = p.w + c * kW;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint4 t = ld_keep(wp + 8 * q);
-            wv[g][4 * q] = t.x; wv[g][4 * q + 1] = t.y; wv[g][4 * q + 2] = t.z; wv[g][4 * q + 3] = t.w;
-          }
+          load_weights_packed<W>(p.w, c, wv[g]);
           if (has_bias) {
             const uint4 t = ld_keep(p.bias + c);
             bv[g][0] = t.x; bv[g][1] = t.y; bv[g][2] = t.z; bv[g][3] = t.w;
@@ -137,9 +132,9 @@ __global__ void __launch_bounds__(kThreads) k_update_bulk(UpdateParams p, int st
       }
       uint4 outv;
       if constexpr (RING) {
-        outv = update8_compact_ring<L, kW, ACT>(xw, ow, wv[g], bv[g], has_bias, sl.q, nw);
+        outv = update8_compact_ring<L, W, ACT>(xw, ow, wv[g], bv[g], has_bias, sl.q, nw);
       } else {
-        outv = update8_compact<L, kW, ACT>(xw, ow, wv[g], bv[g], has_bias, nw);
+        outv = update8_compact<L, W, ACT>(xw, ow, wv[g], bv[g], has_bias, nw);
       }
 #pragma unroll
       for (int q = 0; q < L; ++q) ss[q] = make_uint4(nw[4 * q], nw[4 * q + 1], nw[4 * q + 2], nw[4 * q + 3]);
@@ -174,7 +169,7 @@ __global__ void __launch_bounds__(kThreads) k_update_bulk(UpdateParams p, int st
 }
 
 constexpr int kMaxDevices = 64;
-std::atomic<bool> g_opted_in[kMaxDevices][kVectorMaxL + 1][2][2];
+std::atomic<bool> g_opted_in[kMaxDevices][kVectorMaxL + 1][kW + 1][2][2];
 
 constexpr int kGroups = 2;  // 8-channel groups per lane: slices of 512 channels
 
@@ -183,7 +178,7 @@ int64_t stage_bytes_for(int64_t L) {
   return (b + 127) / 128 * 128;
 }
 
-template <int L, int ACT, bool RING>
+template <int L, int W, int ACT, bool RING>
 cudaError_t launch_LAR(const UpdateParams &p, cudaStream_t stream) {
   const int64_t sb = stage_bytes_for(L);
   // About 8 KB of stages per warp (two 4 KB stages at L = 3): 3 CTAs of 8 warps fit an SM.
@@ -194,15 +189,15 @@ cudaError_t launch_LAR(const UpdateParams &p, cudaStream_t stream) {
   const size_t smem = (size_t)kWarps * (kBarrierBytes + (size_t)P * sb);
   const int dev = current_device();
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!g_opted_in[dev][L][ACT][RING].load(std::memory_order_acquire)) {
-    cudaError_t e = cudaFuncSetAttribute(k_update_bulk<L, ACT, kGroups, RING>,
+  if (!g_opted_in[dev][L][W][ACT][RING].load(std::memory_order_acquire)) {
+    cudaError_t e = cudaFuncSetAttribute(k_update_bulk<L, W, ACT, kGroups, RING>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    g_opted_in[dev][L][ACT][RING].store(true, std::memory_order_release);
+    g_opted_in[dev][L][W][ACT][RING].store(true, std::memory_order_release);
   }
   int per_sm = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      &per_sm, k_update_bulk<L, ACT, kGroups, RING>, kThreads, smem);
+      &per_sm, k_update_bulk<L, W, ACT, kGroups, RING>, kThreads, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   const int64_t slices = (p.D + 256 * kGroups - 1) / (256 * kGroups);
@@ -214,24 +209,32 @@ cudaError_t launch_LAR(const UpdateParams &p, cudaStream_t stream) {
   if (warps > items) warps = items;
   int64_t grid = (warps + kWarps - 1) / kWarps;
   if (grid < 1) grid = 1;
-  k_update_bulk<L, ACT, kGroups, RING><<<(unsigned)grid, kThreads, smem, stream>>>(p, P, sb);
+  k_update_bulk<L, W, ACT, kGroups, RING><<<(unsigned)grid, kThreads, smem, stream>>>(p, P, sb);
   return cudaGetLastError();
 }
 
-template <int L, int ACT>
-cudaError_t launch_LA(const UpdateParams &p, cudaStream_t stream) {
-  return p.seqlens != nullptr ? launch_LAR<L, ACT, true>(p, stream) : launch_LAR<L, ACT, false>(p, stream);
+template <int L, int W, int ACT>
+cudaError_t launch_LWA(const UpdateParams &p, cudaStream_t stream) {
+  return p.seqlens != nullptr ? launch_LAR<L, W, ACT, true>(p, stream)
+                              : launch_LAR<L, W, ACT, false>(p, stream);
 }
 
 template <int ACT>
 cudaError_t launch_A(const UpdateParams &p, cudaStream_t stream) {
-  switch (p.L) {
-    case 3: return launch_LA<3, ACT>(p, stream);
-    case 4: return launch_LA<4, ACT>(p, stream);
-    case 5: return launch_LA<5, ACT>(p, stream);
-    case 6: return launch_LA<6, ACT>(p, stream);
-    case 7: return launch_LA<7, ACT>(p, stream);
-    case 8: return launch_LA<8, ACT>(p, stream);
+  switch (p.W * 16 + p.L) {
+    case 4 * 16 + 3: return launch_LWA<3, 4, ACT>(p, stream);
+    case 4 * 16 + 4: return launch_LWA<4, 4, ACT>(p, stream);
+    case 4 * 16 + 5: return launch_LWA<5, 4, ACT>(p, stream);
+    case 4 * 16 + 6: return launch_LWA<6, 4, ACT>(p, stream);
+    case 4 * 16 + 7: return launch_LWA<7, 4, ACT>(p, stream);
+    case 4 * 16 + 8: return launch_LWA<8, 4, ACT>(p, stream);
+    case 3 * 16 + 2: return launch_LWA<2, 3, ACT>(p, stream);
+    case 3 * 16 + 3: return launch_LWA<3, 3, ACT>(p, stream);
+    case 3 * 16 + 4: return launch_LWA<4, 3, ACT>(p, stream);
+    case 2 * 16 + 1: return launch_LWA<1, 2, ACT>(p, stream);
+    case 2 * 16 + 2: return launch_LWA<2, 2, ACT>(p, stream);
+    case 2 * 16 + 3: return launch_LWA<3, 2, ACT>(p, stream);
+    case 2 * 16 + 4: return launch_LWA<4, 2, ACT>(p, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -252,7 +252,7 @@ cudaError_t take_planes_error(int32_t *bits) {
 }
 
 cudaError_t launch_bulk_planes(const UpdateParams &p, int act, cudaStream_t stream) {
-  if (p.layout != (int)Layout::ChannelLast) return cudaErrorInvalidValue;
+  if (p.layout != (int)Layout::ChannelLast || p.W != kW) return cudaErrorInvalidValue;
   return act == 1 ? launch_A<1>(p, stream) : launch_A<0>(p, stream);
 }
 

@@ -83,7 +83,8 @@ typedef enum ccu_route {
                            (multi-token and prefill: width 4 only) */
   CCU_ROUTE_STAGED = 3, /* shared-memory staged tiles; D % 8 == 0, any L <= 256 */
   CCU_ROUTE_BULK = 4,   /* persistent CTAs, bulk async copies through shared memory;
-                           D % 8 == 0, L <= 8, width 4, both layouts */
+                           D % 8 == 0; width 4 with L <= 8 in both layouts, widths 2
+                           and 3 with L <= 4 in the compact layout */
   CCU_ROUTE_COUNT = 5
 } ccu_route_t;
 

@@ -151,8 +151,15 @@ def test_widths_2_and_3_are_served(ccu):
     assert select(ccu, W=2, L=1) == (0, 2)
     assert select(ccu, W=2, L=1, D=63) == (0, 1)
     assert select(ccu, W=3, L=12) == (0, 3)
-    assert select(ccu, W=3, L=3, N=4096, D=16384, S=4096) == (0, 2)  # bulk kernels: width 4
-    assert select(ccu, route=4, W=3, L=3)[0] == 2
+    # large compact batches take the bulk kernels, compiled for widths 2 and 3 up to L = 4
+    assert select(ccu, W=3, L=2, N=4096, D=16384, S=4096) == (0, 4)
+    assert select(ccu, W=2, L=2, N=4096, D=16384, S=4096) == (0, 4)
+    assert select(ccu, W=2, L=1, N=4096, D=16384, S=4096) == (0, 2)  # one-entry state: vector
+    assert select(ccu, W=3, L=5, N=4096, D=16384, S=4096) == (0, 2)
+    assert select(ccu, route=4, W=3, L=3) == (0, 4)
+    assert select(ccu, route=4, W=2, L=4) == (0, 4)
+    assert select(ccu, route=4, W=3, L=5)[0] == 2
+    assert select(ccu, route=4, W=3, L=2, stride_s=128, stride_d=1, stride_l=64)[0] == 2  # channel-last: width 4
     assert select(ccu, W=3, L=1)[0] == 1  # L < W - 1
 
 

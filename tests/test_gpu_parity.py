@@ -839,16 +839,18 @@ def test_prefill_hands_off_to_decode():
 
 # ----------------------------------------------------------------------------- widths 2 and 3
 
-WIDTH_CASES = [(W, L) for W in (2, 3) for L in sorted({W - 1, W, 5, 9})]
+WIDTH_CASES = [(W, L) for W in (2, 3) for L in sorted({W - 1, W, 4, 5, 9})]
 
 
 @pytest.mark.parametrize("ring", [False, True])
-@pytest.mark.parametrize("route", ["scalar", "vector", "staged"])
+@pytest.mark.parametrize("route", ["scalar", "vector", "staged", "bulk"])
 @pytest.mark.parametrize("layout", ["compact", "channel_last"])
 @pytest.mark.parametrize("W,L", WIDTH_CASES)
 def test_widths(W, L, layout, route, ring):
     if route == "vector" and L > 8:
         pytest.skip("vector kernels are compiled for L <= 8")
+    if route == "bulk" and (layout != "compact" or L > 4):
+        pytest.skip("bulk kernels serve widths 2 and 3 in the compact layout with L <= 4")
     wl = synthetic.variant(synthetic.WORKLOADS["paged_n256_d8192_l3_s1024_pad10_silu"], name="width",
                            N=9, D=264, ld=264, S=12, W=W, L=L, pad_frac=0.25)
     inp = synthetic.generate(wl, seed=W * 100 + L)
@@ -859,11 +861,12 @@ def test_widths(W, L, layout, route, ring):
         _check(inp, layout=layout, route=route, what=f"W={W} L={L} {route} {layout}")
 
 
-@pytest.mark.parametrize("W", [2, 3])
-def test_widths_large_batch_auto_route(W):
-    wl = synthetic.variant(synthetic.WORKLOADS[synthetic.BENCH_WORKLOAD], name="wide", N=512, S=512, W=W)
-    inp = synthetic.generate(wl, seed=W)
-    _check(inp, what=f"W={W} large")
+@pytest.mark.parametrize("W,L", [(2, 1), (2, 3), (3, 2), (3, 4)])
+def test_widths_large_batch_auto_route(W, L):
+    """Large compact batches at widths 2 and 3 take the bulk kernels (AUTO)."""
+    wl = synthetic.variant(synthetic.WORKLOADS[synthetic.BENCH_WORKLOAD], name="wide", N=512, S=512, W=W, L=L)
+    inp = synthetic.generate(wl, seed=W * 10 + L)
+    _check(inp, what=f"W={W} L={L} large")
 
 
 @pytest.mark.parametrize("W,L,T", [(2, 1, 3), (3, 2, 5), (3, 4, 2)])
