@@ -132,18 +132,24 @@ bool route_serves(int route, const Args &a, Layout layout) {
 // kernel's shorter start-up wins; above it the bulk-copy pipeline keeps more bytes in flight
 // (cold L2, D = 16384: tied at 64 rows, 12.3 vs 14.8 us at 128 rows, 24.6 vs 35.4 us at 512).
 constexpr int64_t kBulkMinElements = 1 << 20;
+constexpr int64_t kChannelLastBulkMaxElements = int64_t(3) << 24;
 
 ccu_status_t choose(int requested, const Args &a, Layout layout, int *chosen) {
   if (requested < 0 || requested >= CCU_ROUTE_COUNT)
     return fail(CCU_ERR_INVALID_ARGUMENT, "unknown route %d", requested);
   if (requested == CCU_ROUTE_AUTO) {
-    // Large batches with the compact state take the bulk kernel. The channel-last state is
-    // already one 16-byte vector per plane and thread, and measured faster on the vector
-    // kernel at every size (large batch: 160 vs 165 us linear, 146 vs 164 us ring).
-    // A one-entry state (L = 1) moves 8 bytes per element: too little per 512-channel slice
-    // for the bulk pipeline (large batch, W = 2: 100.8 us bulk, 80.7 us vector).
-    if (a.N * a.D >= kBulkMinElements && layout == Layout::Compact && a.L >= 2 &&
-        route_serves(CCU_ROUTE_BULK, a, layout)) {
+    // Batches from 2^20 elements take the bulk kernel, with two exceptions measured on the
+    // large batch (D = 16384, back to back). A one-entry state (L = 1) moves 8 bytes per
+    // element, too little per 512-channel slice for the bulk pipeline (W = 2: 100.8 us
+    // bulk, 80.7 us vector). With the channel-last state the bulk kernel leads from 128 to
+    // 2048 rows (1024 rows, ring: 44.8 vs 63.8 us), ties at 3072 and trails at 4096 rows
+    // (159.4 vs 163.7 us linear, 143.4 vs 156.9 us ring), so above 3 * 2^24 elements that
+    // layout stays on the vector kernel.
+    const int64_t elements = a.N * a.D;
+    const bool bulk_size = layout == Layout::Compact
+                               ? elements >= kBulkMinElements && a.L >= 2
+                               : elements >= kBulkMinElements && elements < kChannelLastBulkMaxElements;
+    if (bulk_size && route_serves(CCU_ROUTE_BULK, a, layout)) {
       *chosen = CCU_ROUTE_BULK;
     } else if (route_serves(CCU_ROUTE_VECTOR, a, layout)) {
       *chosen = CCU_ROUTE_VECTOR;

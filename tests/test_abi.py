@@ -188,6 +188,10 @@ ROUTE_CASES = [
     ("below the bulk threshold", dict(N=64, D=8192, S=64), "vector"),
     ("large batch channel-last", dict(N=4096, D=16384, S=4096, stride_s=3 * 16384, stride_d=1,
                                       stride_l=16384), "vector"),
+    ("mid batch channel-last", dict(N=1024, D=16384, S=1024, stride_s=3 * 16384, stride_d=1,
+                                    stride_l=16384), "bulk"),
+    ("small batch channel-last", dict(N=32, D=16384, S=32, stride_s=3 * 16384, stride_d=1,
+                                      stride_l=16384), "vector"),
     ("large batch L9", dict(N=4096, D=16384, S=4096, L=9), "staged"),
 ]
 
