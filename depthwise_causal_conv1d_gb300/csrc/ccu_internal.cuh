@@ -313,6 +313,63 @@ __device__ __forceinline__ void unpack8(const uint4 v, uint32_t (&e)[8]) {
 }
 
 // ---------------------------------------------------------------------------------------
+// Width-4 arithmetic on channel pairs (the prefill and the multi-token update): 8 channels
+// as 4 float pairs, the window sums and the SiLU through the paired FP32 instructions.
+
+// Widen 8 packed BF16 to 4 float pairs (channels 2i, 2i+1).
+__device__ __forceinline__ void widen8(const uint4 v, float2 (&f)[4]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) f[i] = make_float2(bf16_lo(w[i]), bf16_hi(w[i]));
+}
+
+// The width-4 weights of channels c0..c0+7 as float pairs: wf[j][i] = weight[c0 + 2i (+1), j].
+__device__ __forceinline__ void load_weights_f(const uint16_t *w, int64_t c0, float2 (&wf)[kW][4]) {
+  const uint16_t *wp = w + c0 * kW;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {  // 16 bytes = channels 2k, 2k+1, all four taps each
+    const uint4 t = ld_keep(wp + 8 * k);
+    wf[0][k] = make_float2(bf16_lo(t.x), bf16_lo(t.z));
+    wf[1][k] = make_float2(bf16_hi(t.x), bf16_hi(t.z));
+    wf[2][k] = make_float2(bf16_lo(t.y), bf16_lo(t.w));
+    wf[3][k] = make_float2(bf16_hi(t.y), bf16_hi(t.w));
+  }
+}
+
+// Outputs of 8 channels (4 pairs) for one token from the window a, b, c (oldest first) and
+// the token's inputs x. The accumulation order is the update's: ((0 + a*w0) + b*w1) + c*w2 +
+// x*w3, then the bias (each product of two BF16 values is exact in FP32); the paired FP32
+// instructions round each half exactly as the scalar ones.
+template <int ACT>
+__device__ __forceinline__ uint4 outputs8f(const float2 (&wf)[kW][4], const float2 (&bf)[4],
+                                           bool has_bias, const float2 (&a)[4], const float2 (&b)[4],
+                                           const float2 (&c)[4], const float2 (&x)[4]) {
+  uint32_t y[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 acc = __ffma2_rn(a[i], wf[0][i], make_float2(0.0f, 0.0f));
+    acc = __ffma2_rn(b[i], wf[1][i], acc);
+    acc = __ffma2_rn(c[i], wf[2][i], acc);
+    acc = __ffma2_rn(x[i], wf[3][i], acc);
+    if (has_bias) acc = __fadd2_rn(acc, bf[i]);
+    const float2 v = activate2<ACT>(acc);
+    y[i] = pack_bf16x2(v.x, v.y);
+  }
+  return make_uint4(y[0], y[1], y[2], y[3]);
+}
+
+// The window slides by one token: (h0, h1, h2) <- (h1, h2, x).
+__device__ __forceinline__ void slide(float2 (&h0)[4], float2 (&h1)[4], float2 (&h2)[4],
+                                      const float2 (&x)[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    h0[i] = h1[i];
+    h1[i] = h2[i];
+    h2[i] = x[i];
+  }
+}
+
+// ---------------------------------------------------------------------------------------
 // Kernel launchers (one per family). Each returns the cudaError_t of its launch.
 
 cudaError_t launch_scalar(const UpdateParams &p, int act, cudaStream_t stream);

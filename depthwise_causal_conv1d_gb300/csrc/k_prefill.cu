@@ -76,48 +76,6 @@ __global__ void __launch_bounds__(256) k_prefill_scalar(UpdateParams p, PrefillP
   }
 }
 
-// Widen 8 packed BF16 to 4 float pairs (channels 2i, 2i+1).
-__device__ __forceinline__ void widen8(const uint4 v, float2 (&f)[4]) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) f[i] = make_float2(bf16_lo(w[i]), bf16_hi(w[i]));
-}
-
-// The width-4 weights of channels c0..c0+7 as float pairs: wf[j][i] = weight[c0 + 2i (+1), j].
-__device__ __forceinline__ void load_weights_f(const UpdateParams &p, int64_t c0, float2 (&wf)[kW][4]) {
-  const uint16_t *wp = p.w + c0 * kW;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {  // 16 bytes = channels 2k, 2k+1, all four taps each
-    const uint4 t = ld_keep(wp + 8 * k);
-    wf[0][k] = make_float2(bf16_lo(t.x), bf16_lo(t.z));
-    wf[1][k] = make_float2(bf16_hi(t.x), bf16_hi(t.z));
-    wf[2][k] = make_float2(bf16_lo(t.y), bf16_lo(t.w));
-    wf[3][k] = make_float2(bf16_hi(t.y), bf16_hi(t.w));
-  }
-}
-
-// Outputs of 8 channels (4 pairs) for one token from the window a, b, c (oldest first) and
-// the token's inputs x. The accumulation order is the update's: ((0 + a*w0) + b*w1) + c*w2 +
-// x*w3, then the bias (each product of two BF16 values is exact in FP32); the paired FP32
-// instructions round each half exactly as the scalar ones.
-template <int ACT>
-__device__ __forceinline__ uint4 outputs8f(const float2 (&wf)[kW][4], const float2 (&bf)[4],
-                                           bool has_bias, const float2 (&a)[4], const float2 (&b)[4],
-                                           const float2 (&c)[4], const float2 (&x)[4]) {
-  uint32_t y[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float2 acc = __ffma2_rn(a[i], wf[0][i], make_float2(0.0f, 0.0f));
-    acc = __ffma2_rn(b[i], wf[1][i], acc);
-    acc = __ffma2_rn(c[i], wf[2][i], acc);
-    acc = __ffma2_rn(x[i], wf[3][i], acc);
-    if (has_bias) acc = __fadd2_rn(acc, bf[i]);
-    const float2 v = activate2<ACT>(acc);
-    y[i] = pack_bf16x2(v.x, v.y);
-  }
-  return make_uint4(y[0], y[1], y[2], y[3]);
-}
-
 // The window before token t0 for channels c0..c0+7: inputs t0-3, t0-2, t0-1 (from x, or the
 // initial state / zeros before the sequence).
 __device__ __forceinline__ void load_halo(const UpdateParams &p, const PrefillParams &f, int64_t b,
@@ -142,18 +100,7 @@ __device__ __forceinline__ void load_halo(const UpdateParams &p, const PrefillPa
   }
 }
 
-// The window slides by one token: (h0, h1, h2) <- (h1, h2, x).
-__device__ __forceinline__ void slide(float2 (&h0)[4], float2 (&h1)[4], float2 (&h2)[4],
-                                      const float2 (&x)[4]) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    h0[i] = h1[i];
-    h1[i] = h2[i];
-    h2[i] = x[i];
-  }
-}
-
-// Scalar-float forms of the helpers below, for the vector kernel (paired FP32 arithmetic
+// Scalar-float forms of the paired helpers in ccu_internal.cuh, for the vector kernel (paired FP32 arithmetic
 // made it spill at 128 registers).
 
 // Widen 8 packed BF16 to floats.
@@ -445,7 +392,7 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_bulk(UpdateParams p, P
     const int64_t c0 = r.c_base + 8 * lane;
     if (active) {
       if (r.c_base != w_base) {
-        load_weights_f(p, c0, wf);
+        load_weights_f(p.w, c0, wf);
         if (has_bias) widen8(ld_keep(p.bias + c0), bf);
       }
       load_halo(p, f, r.b, c0, r.t0, h0, h1, h2);
