@@ -321,6 +321,90 @@ def test_cuda_graph_replay_matches_eager():
     assert torch.equal(eager_state.view(torch.int16), st.view(torch.int16))
 
 
+def test_cuda_graph_prefill_multi_decode_sequence():
+    """One CUDA graph holding a serving sequence on one state: a bulk prefill that writes the
+    channel-last hand-off state, a multi-token update and a (bulk) decode step. Every replay
+    restarts from the prefill's state and equals the eager sequence bit for bit."""
+    import depthwise_causal_conv1d_gb300 as ccu
+
+    rng = np.random.default_rng(21)
+    B, T, D, L = 512, 16, 2048, 3
+    assert B * T * D >= 1 << 20 and B * D >= 1 << 20  # prefill and decode take the bulk kernels
+    x_pre = to_dev_u16(synthetic.f64_to_bf16_bits(rng.standard_normal((B, T, D))), DEV).permute(0, 2, 1)
+    x_multi = to_dev_u16(synthetic.f64_to_bf16_bits(rng.standard_normal((B, 4, D))), DEV).permute(0, 2, 1)
+    x_dec = to_dev_u16(synthetic.f64_to_bf16_bits(rng.standard_normal((B, D))), DEV)
+    w = to_dev_u16(synthetic.f64_to_bf16_bits(rng.standard_normal((D, 4)) * 0.5), DEV)
+    b = to_dev_u16(synthetic.f64_to_bf16_bits(rng.standard_normal(D) * 0.1), DEV)
+
+    def buffers():
+        return (torch.empty((B, L, D), dtype=torch.bfloat16, device=DEV).permute(0, 2, 1),
+                torch.empty_like(x_pre), torch.empty_like(x_multi), torch.empty_like(x_dec))
+
+    def sequence(fin, y0, y1, y2):
+        ccu.causal_conv1d_fwd(x_pre, w, b, "silu", final_states_out=fin, out=y0)
+        ccu.causal_conv1d_update(x_multi, fin, w, b, "silu", out=y1)
+        ccu.causal_conv1d_update(x_dec, fin, w, b, "silu", out=y2)
+
+    eager = buffers()
+    sequence(*eager)
+    torch.cuda.synchronize()
+
+    graphed = buffers()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # warm the exact signatures before capture
+        sequence(*graphed)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        sequence(*graphed)
+    for _ in range(3):
+        for t in graphed:
+            t.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for a, c in zip(eager, graphed):
+            assert torch.equal(a.contiguous().view(torch.int16), c.contiguous().view(torch.int16))
+
+
+def test_side_stream_prefill_and_multi_token():
+    """Prefill (bulk) and a multi-token update issued on a side stream while the default
+    stream is parked: complete and correct when the side stream alone is synchronized."""
+    import depthwise_causal_conv1d_gb300 as ccu
+    from oracle_pins import bf16_ulp_distance
+
+    rng = np.random.default_rng(23)
+    B, T, D, L, K = 4, 300, 1024, 3, 3
+    x_all = synthetic.f64_to_bf16_bits(rng.standard_normal((B, T + K, D)))
+    weight = synthetic.f64_to_bf16_bits(rng.standard_normal((D, 4)) * 0.5)
+    bias = synthetic.f64_to_bf16_bits(rng.standard_normal(D) * 0.1)
+    x_pre = to_dev_u16(np.ascontiguousarray(x_all[:, :T]), DEV).permute(0, 2, 1)
+    x_multi = to_dev_u16(np.ascontiguousarray(x_all[:, T:]), DEV).permute(0, 2, 1)
+    w, b = to_dev_u16(weight, DEV), to_dev_u16(bias, DEV)
+    fin = torch.empty((B, L, D), dtype=torch.bfloat16, device=DEV).permute(0, 2, 1)
+    y_pre, y_multi = torch.empty_like(x_pre), torch.empty_like(x_multi)
+    h_pre = torch.empty((B, T, D), dtype=torch.bfloat16, pin_memory=True)
+    h_multi = torch.empty((B, K, D), dtype=torch.bfloat16, pin_memory=True)
+    side = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    torch.cuda._sleep(200_000_000)  # parks the default stream for ~0.1 s (bounded spin)
+    with torch.cuda.stream(side):
+        ccu.causal_conv1d_fwd(x_pre, w, b, "silu", final_states_out=fin, out=y_pre, route="bulk")
+        ccu.causal_conv1d_update(x_multi, fin, w, b, "silu", out=y_multi)
+        h_pre.copy_(y_pre.permute(0, 2, 1), non_blocking=True)
+        h_multi.copy_(y_multi.permute(0, 2, 1), non_blocking=True)
+    side.synchronize()
+    default_busy = not torch.cuda.default_stream().query()
+    got = np.concatenate([h_pre.view(torch.int16).numpy().view(np.uint16),
+                          h_multi.view(torch.int16).numpy().view(np.uint16)], axis=1)
+    torch.cuda.synchronize()
+    assert default_busy, "the default stream finished first: the test did not park it"
+    for bb in range(B):
+        want, _ = oracle.full_causal_conv(x_all[bb], weight, bias, "silu", None, L)
+        assert bf16_ulp_distance(got[bb], want).max() <= 1, bb
+
+
 # ----------------------------------------------------------------------------- checked path
 
 @pytest.mark.parametrize("route", ["scalar", "vector", "staged", "bulk"])
