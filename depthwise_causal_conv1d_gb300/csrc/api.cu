@@ -420,17 +420,18 @@ ccu_status_t run_prefill(const PrefillArgs &a, int route, cudaStream_t stream) {
   f.fin = static_cast<uint16_t *>(const_cast<void *>(a.fin));
   f.sfb = a.sfb; f.sfd = a.sfd; f.sfl = a.sfl;
   // The bulk kernel's copies run between device memory and shared memory (as for the
-  // update, host-resident x or out go to the vector kernel).
-  const bool on_device = !is_host_memory(a.x) && !is_host_memory(a.out);
+  // update, host-resident x or out go to the vector kernel). The pointer query runs only
+  // when the bulk kernel is in question.
+  auto on_device = [&]() { return !is_host_memory(a.x) && !is_host_memory(a.out); };
   bool vector, bulk = false;
   if (route == CCU_ROUTE_AUTO) {
     vector = vec_ok;
-    bulk = vec_ok && on_device && a.B * a.D * a.T >= kPrefillBulkMinElements;
+    bulk = vec_ok && a.B * a.D * a.T >= kPrefillBulkMinElements && on_device();
   } else if (route == CCU_ROUTE_SCALAR) {
     vector = false;
   } else if (route == CCU_ROUTE_VECTOR && vec_ok) {
     vector = true;
-  } else if (route == CCU_ROUTE_BULK && vec_ok && on_device) {
+  } else if (route == CCU_ROUTE_BULK && vec_ok && on_device()) {
     vector = bulk = true;
   } else if (route >= 0 && route < CCU_ROUTE_COUNT) {
     return fail(CCU_ERR_NOT_IMPLEMENTED, "route '%s' does not serve these prefill arguments",
