@@ -29,6 +29,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -539,6 +540,63 @@ def per_workload_table(dev, stream, reps=50):
     return rows
 
 
+def n_curve(dev, stream, reps=100):
+    """µs per call against N·D: the large-batch decode settings (D=16384, L=3, SiLU, bias,
+    permuted slots with 5% padding) at N = 1, 8, 64, 256, 1024, 4096, route AUTO; warm
+    (back to back) and clean cold (a 2x-L2 buffer read before each call)."""
+    import torch
+
+    flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+    base = synthetic.WORKLOADS[synthetic.BENCH_WORKLOAD]
+    rows = {}
+    for n in (1, 8, 64, 256, 1024, 4096):
+        wl = synthetic.variant(base, N=n, S=n)
+        inp = synthetic.generate(wl)
+        res = Resident(inp, dev, stream)
+        nbytes = synthetic.algorithmic_bytes(wl, inp.indices)
+        for _ in range(5):
+            res.call()
+        torch.cuda.synchronize()
+        k = max(20, min(reps * 10, int(2e10 / max(nbytes, 1))))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(k):
+            res.call()
+        b.record(stream)
+        torch.cuda.synchronize()
+        warm_us = a.elapsed_time(b) * 1e3 / k
+        clean = []
+        for _ in range(30):
+            with torch.cuda.stream(stream):
+                flush.sum()
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            c0.record(stream)
+            res.call()
+            c1.record(stream)
+            clean.append((c0, c1))
+        torch.cuda.synchronize()
+        cold_us = statistics.median(c0.elapsed_time(c1) * 1e3 for c0, c1 in clean)
+        rows[f"N={n}"] = {"N_x_D": wl.N * wl.D, "bytes": nbytes, "route": res.route_name,
+                          "warm_us": round(warm_us, 3), "cold_clean_us": round(cold_us, 3),
+                          "cold_GBps": round(nbytes / (cold_us * 1e-6) / 1e9, 1),
+                          "cold_frac": round(nbytes / (cold_us * 1e-6) / 1e9 / PEAK_GBPS, 4)}
+        del res
+    del flush
+    return rows
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu), for the CPU baseline's record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.processor() or platform.machine()
+
+
 def multi_token_rows(dev, stream, reps=50, route=0, singles_too=True):
     """µs per call of the multi-token update, and of the same tokens as T single calls."""
     import torch
@@ -655,7 +713,7 @@ def cpu_baseline_sample(inp, target_s: float):
     return {"value": round(nbytes / t / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"first {rows} of {wl.N} rows (all {wl.D} channels, full state), "
                       f"median of 3 runs of {t:.2f} s each; {nbytes} algorithmic bytes per run",
-            "seconds_per_run": round(t, 3), "cores_available": os.cpu_count()}
+            "seconds_per_run": round(t, 3), "cores_available": os.cpu_count(), "cpu_model": cpu_model()}
 
 
 def _oracle_rows(oracle, lib, inp, rows):
@@ -737,6 +795,7 @@ def run_ours(args):
         line["clocks"] = sampler.summary(w0, w1)
         if rank == 0 and world == 1:
             line["per_workload"] = per_workload_table(dev, stream)
+            line["n_curve"] = n_curve(dev, stream)
             line["multi_token"] = multi_token_rows(dev, stream)
             line["prefill"] = prefill_rows(dev, stream)
         if rank == 0:
@@ -798,7 +857,7 @@ def run_reference(args):
         "config": config_of(wl, {"rows_per_step": rows}),
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"first {rows} of {wl.N} rows per step (all {wl.D} channels)",
-                         "cores_available": os.cpu_count()},
+                         "cores_available": os.cpu_count(), "cpu_model": cpu_model()},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
