@@ -52,7 +52,7 @@ UNIT = "GB/s"
 L2_BYTES = 129 * 1024 * 1024
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "update_bulk_large_n4096_d16384.txt")
 KERNEL_SOURCES = [os.path.join(ROOT, "depthwise_causal_conv1d_gb300", "csrc", f)
-                  for f in ("k_bulk.cu", "ccu_internal.cuh")]
+                  for f in ("k_bulk.cu", "ccu_bulk.cuh", "ccu_internal.cuh")]
 
 
 def parse_args():

@@ -95,7 +95,9 @@ struct Slice {
   int q;  // ring position of the oldest entry (ring-buffer state only)
 };
 
-template <int G>
+// LC: L known at compile time. The cache_seqlens load is issued together with the index
+// load, as in resolve_row.
+template <int G, int LC>
 __device__ __forceinline__ Slice slice_of(const UpdateParams &p, int64_t t, int64_t slices, bool report) {
   constexpr int64_t kSlice = 256 * G;
   Slice sl;
@@ -103,6 +105,7 @@ __device__ __forceinline__ Slice slice_of(const UpdateParams &p, int64_t t, int6
   sl.c_base = (t - sl.n * slices) * kSlice;
   const int64_t rem = p.D - sl.c_base;
   sl.cn = rem < kSlice ? rem : kSlice;
+  const int32_t v = p.seqlens != nullptr ? __ldg(p.seqlens + sl.n) : 0;
   if (p.idx == nullptr) {
     sl.s = sl.n;
   } else {
@@ -114,13 +117,12 @@ __device__ __forceinline__ Slice slice_of(const UpdateParams &p, int64_t t, int6
   }
   sl.q = 0;
   if (sl.s >= 0 && p.seqlens != nullptr) {
-    const int64_t v = __ldg(p.seqlens + sl.n);
     if (v < 0 && p.status != nullptr) {
       if (report) atomicOr(p.status, 1);  // CCU_DEVERR_RANGE
       sl.s = -1;
     } else {
-      const int64_t m = v % p.L;
-      sl.q = (int)(m < 0 ? m + p.L : m);
+      const int m = v % LC;
+      sl.q = m < 0 ? m + LC : m;
     }
   }
   return sl;

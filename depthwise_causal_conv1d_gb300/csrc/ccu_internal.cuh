@@ -200,17 +200,24 @@ struct RowSlot {
   int q;
 };
 
+// The cache_seqlens load is issued together with the index load (every row has an entry,
+// and it does not depend on the slot), so a ring row waits for one round of loads before
+// its state address is known, not two. LC: L known at compile time (0: use p.L).
+template <int LC = 0>
 __device__ __forceinline__ RowSlot resolve_row(const UpdateParams &p, int64_t n) {
   RowSlot r;
+  const int32_t v = p.seqlens != nullptr ? __ldg(p.seqlens + n) : 0;
   r.s = resolve_slot(p, n);
   r.q = 0;
   if (r.s >= 0 && p.seqlens != nullptr) {
-    const int64_t v = __ldg(p.seqlens + n);
     if (v < 0 && p.status != nullptr) {
       atomicOr(p.status, 1);  // CCU_DEVERR_RANGE
       r.s = -1;
+    } else if constexpr (LC > 0) {
+      const int m = v % LC;
+      r.q = m < 0 ? m + LC : m;
     } else {
-      int64_t m = v % p.L;
+      const int64_t m = (int64_t)v % p.L;
       r.q = (int)(m < 0 ? m + p.L : m);
     }
   }

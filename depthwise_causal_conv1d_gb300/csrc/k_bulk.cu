@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(kThreads) k_update_bulk(UpdateParams p, int st
 
   // Lane 0: put this warp's k-th slice into stage k % P.
   auto issue = [&](int64_t k) {
-    const Slice sl = slice_of<G>(p, first + k * stride, slices, true);
+    const Slice sl = slice_of<G, L>(p, first + k * stride, slices, true);
     uint64_t *bar = &bars[k % P];
     unsigned char *buf = bufs + (k % P) * stage_bytes;
     if (sl.s < 0) {
@@ -85,7 +85,7 @@ __global__ void __launch_bounds__(kThreads) k_update_bulk(UpdateParams p, int st
   for (; k < mine; ++k) {
     const int st = (int)(k % P);
     const uint32_t parity = (uint32_t)((k / P) & 1);
-    const Slice sl = slice_of<G>(p, first + k * stride, slices, false);
+    const Slice sl = slice_of<G, L>(p, first + k * stride, slices, false);
     unsigned char *buf = bufs + st * stage_bytes;
 
     if (sl.c_base != w_base) {  // weights of this slice, kept while it repeats

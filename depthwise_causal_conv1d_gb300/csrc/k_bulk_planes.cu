@@ -78,7 +78,7 @@ __global__ void __launch_bounds__(kThreads) k_update_bulk_planes(UpdateParams p,
   };
 
   auto issue = [&](int64_t k) {
-    const Slice sl = slice_of<kG>(p, first_item + k * stride, slices, true);
+    const Slice sl = slice_of<kG, L>(p, first_item + k * stride, slices, true);
     uint64_t *bar = &bars[k % P];
     unsigned char *buf = bufs + (k % P) * stage_bytes;
     if (sl.s < 0) {
@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(kThreads) k_update_bulk_planes(UpdateParams p,
   for (; k < mine; ++k) {
     const int st = (int)(k % P);
     const uint32_t parity = (uint32_t)((k / P) & 1);
-    const Slice sl = slice_of<kG>(p, first_item + k * stride, slices, false);
+    const Slice sl = slice_of<kG, L>(p, first_item + k * stride, slices, false);
     unsigned char *buf = bufs + st * stage_bytes;
 
     if (sl.c_base != w_base) {

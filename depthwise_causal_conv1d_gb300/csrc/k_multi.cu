@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(256) k_multi_vector(UpdateParams p, MultiParam
   }
 
   for (int64_t n = blockIdx.y; n < p.N; n += gridDim.y) {
-    const RowSlot row = resolve_row(p, n);
+    const RowSlot row = resolve_row<L>(p, n);
     if (row.s < 0) {
       for (int64_t t = 0; t < m.T; ++t)
         st_stream(p.out + n * m.son + t * m.sot + c0, make_uint4(0u, 0u, 0u, 0u));

@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(256) k_update_vector(UpdateParams p) {
   };
 
   auto load_row = [&](int64_t n, Row &r) {
-    r.slot = resolve_row(p, n);
+    r.slot = resolve_row<L>(p, n);
     if (r.slot.s < 0) return;
     const uint4 t = ld_stream(p.x + n * p.ld + c0);
     r.xw[0] = t.x; r.xw[1] = t.y; r.xw[2] = t.z; r.xw[3] = t.w;
