@@ -145,9 +145,14 @@ ccu_status_t choose(int requested, const Args &a, Layout layout, int *chosen) {
     // 2048 rows (1024 rows, ring: 44.8 vs 63.8 us), ties at 3072 and trails at 4096 rows
     // (159.4 vs 163.7 us linear, 143.4 vs 156.9 us ring), so above 3 * 2^24 elements that
     // layout stays on the vector kernel.
+    // Width 3 with L = 2 (a state of just the window) is the one compact case where the
+    // vector kernel, at three CTAs per SM, passes the bulk kernel on the full batch (4096
+    // rows: 119.0 vs 126.1 us; 1024 rows: 41.0 vs 36.8 us), so it stays on the vector kernel
+    // from 3 * 2^24 elements as the channel-last state does.
     const int64_t elements = a.N * a.D;
+    const bool window_only_w3 = a.W == 3 && a.L == 2 && elements >= kChannelLastBulkMaxElements;
     const bool bulk_size = layout == Layout::Compact
-                               ? elements >= kBulkMinElements && a.L >= 2
+                               ? elements >= kBulkMinElements && a.L >= 2 && !window_only_w3
                                : elements >= kBulkMinElements && elements < kChannelLastBulkMaxElements;
     if (bulk_size && route_serves(CCU_ROUTE_BULK, a, layout)) {
       *chosen = CCU_ROUTE_BULK;

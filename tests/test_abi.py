@@ -152,7 +152,9 @@ def test_widths_2_and_3_are_served(ccu):
     assert select(ccu, W=2, L=1, D=63) == (0, 1)
     assert select(ccu, W=3, L=12) == (0, 3)
     # large compact batches take the bulk kernels, compiled for widths 2 and 3 up to L = 4
-    assert select(ccu, W=3, L=2, N=4096, D=16384, S=4096) == (0, 4)
+    assert select(ccu, W=3, L=2, N=1024, D=16384, S=1024) == (0, 4)
+    assert select(ccu, W=3, L=2, N=4096, D=16384, S=4096) == (0, 2)  # window-only state, full batch
+    assert select(ccu, W=3, L=3, N=4096, D=16384, S=4096) == (0, 4)
     assert select(ccu, W=2, L=2, N=4096, D=16384, S=4096) == (0, 4)
     assert select(ccu, W=2, L=1, N=4096, D=16384, S=4096) == (0, 2)  # one-entry state: vector
     assert select(ccu, W=3, L=5, N=4096, D=16384, S=4096) == (0, 2)
