@@ -15,11 +15,9 @@ int device_sm_count();
 namespace {
 
 // W: filter width (2..4). RING: conv_state is a ring buffer indexed by cache_seqlens.
-// Width 3 asks for three CTAs per SM (at most 85 registers a thread): measured on the large
-// batch at L = 2, 118.6 us against 130.7 us at two; every other instantiation measured
-// slower with that cap and keeps the compiler's choice.
+// The body of the two kernels below.
 template <int L, int W, int ACT, int LAYOUT, bool RING>
-__global__ void __launch_bounds__(256, W == 3 ? 3 : 1) k_update_vector(UpdateParams p) {
+__device__ __forceinline__ void update_vector(const UpdateParams &p) {
   const int64_t groups = p.D >> 3;  // 8-channel groups per row (D % 8 == 0)
   const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (g >= groups) return;
@@ -144,20 +142,43 @@ __global__ void __launch_bounds__(256, W == 3 ? 3 : 1) k_update_vector(UpdatePar
   }
 }
 
+// Register budget left to the compiler (two CTAs per SM at the register counts it picks).
+template <int L, int W, int ACT, int LAYOUT, bool RING>
+__global__ void __launch_bounds__(256) k_update_vector(UpdateParams p) {
+  update_vector<L, W, ACT, LAYOUT, RING>(p);
+}
+
+// Width 3 at three CTAs per SM (at most 85 registers a thread): measured on the large batch at
+// L = 2, 118.6 us against 130.7 us with the compiler's budget; the other widths measured
+// slower with that cap.
+template <int L, int ACT, int LAYOUT, bool RING>
+__global__ void __launch_bounds__(256, 3) k_update_vector_w3(UpdateParams p) {
+  update_vector<L, 3, ACT, LAYOUT, RING>(p);
+}
+
+template <int L, int W, int ACT, int LAYOUT, bool RING>
+void launch_one(const UpdateParams &p, dim3 grid, dim3 block, cudaStream_t stream) {
+  if constexpr (W == 3) {
+    k_update_vector_w3<L, ACT, LAYOUT, RING><<<grid, block, 0, stream>>>(p);
+  } else {
+    k_update_vector<L, W, ACT, LAYOUT, RING><<<grid, block, 0, stream>>>(p);
+  }
+}
+
 template <int L, int W, int ACT>
 cudaError_t launch_LW(const UpdateParams &p, dim3 grid, dim3 block, cudaStream_t stream) {
   const bool ring = p.seqlens != nullptr;
   if (p.layout == (int)Layout::Compact) {
     if (ring) {
-      k_update_vector<L, W, ACT, (int)Layout::Compact, true><<<grid, block, 0, stream>>>(p);
+      launch_one<L, W, ACT, (int)Layout::Compact, true>(p, grid, block, stream);
     } else {
-      k_update_vector<L, W, ACT, (int)Layout::Compact, false><<<grid, block, 0, stream>>>(p);
+      launch_one<L, W, ACT, (int)Layout::Compact, false>(p, grid, block, stream);
     }
   } else {
     if (ring) {
-      k_update_vector<L, W, ACT, (int)Layout::ChannelLast, true><<<grid, block, 0, stream>>>(p);
+      launch_one<L, W, ACT, (int)Layout::ChannelLast, true>(p, grid, block, stream);
     } else {
-      k_update_vector<L, W, ACT, (int)Layout::ChannelLast, false><<<grid, block, 0, stream>>>(p);
+      launch_one<L, W, ACT, (int)Layout::ChannelLast, false>(p, grid, block, stream);
     }
   }
   return cudaGetLastError();
