@@ -55,13 +55,18 @@ KERNEL_SOURCES = [os.path.join(ROOT, "depthwise_causal_conv1d_gb300", "csrc", f)
                   for f in ("k_bulk.cu", "ccu_bulk.cuh", "ccu_internal.cuh")]
 
 
+ALL_DECODE_WORKLOADS = {**synthetic.WORKLOADS, **synthetic.RING_WORKLOADS, **synthetic.WIDTH_WORKLOADS}
+
+
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=synthetic.BENCH_WORKLOAD, choices=sorted(synthetic.WORKLOADS))
+    ap.add_argument("--workload", default=synthetic.BENCH_WORKLOAD, choices=sorted(ALL_DECODE_WORKLOADS),
+                    help="a decode workload; the ring-buffer and width variants are for profiling rows of "
+                         "the per-workload table")
     ap.add_argument("--rows", type=int, default=None,
                     help="run a smaller case of the same kernel: first ROWS rows (profiling)")
     ap.add_argument("--route", default="auto", choices=["auto", "scalar", "vector", "staged", "bulk"])
@@ -78,7 +83,7 @@ def parse_args():
 
 
 def workload_for(args) -> synthetic.Workload:
-    wl = synthetic.WORKLOADS[args.workload]
+    wl = ALL_DECODE_WORKLOADS[args.workload]
     if args.rows is not None and args.rows < wl.N:
         changes = dict(N=args.rows)
         if wl.indices.startswith("perm"):
@@ -226,9 +231,16 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(full_units: int):
+def ncu_traffic(full_units: int, wl=None, route_name="bulk"):
     """DRAM bytes per launch from the committed ncu summary, scaled to this launch's
-    (row, channel) units; None if the kernel source changed since the capture."""
+    (row, channel) units; None if the kernel source changed since the capture, or if this
+    run is not the captured kernel on the captured workload's kind of input."""
+    if wl is not None:
+        base = synthetic.WORKLOADS[synthetic.BENCH_WORKLOAD]
+        same_kind = (wl.D, wl.L, wl.W, wl.act, wl.layout, wl.ring) == (base.D, base.L, base.W, base.act,
+                                                                    base.layout, base.ring)
+        if not same_kind or route_name != "bulk":
+            return None, "no ncu capture for this workload and route"
     try:
         text = open(PROFILE_SUMMARY).read()
     except OSError:
@@ -754,7 +766,7 @@ def run_ours(args):
         peak, peak_src = float(peaks["hbm_gbs"]), "measured"
     except (OSError, KeyError, ValueError):
         peak, peak_src = 6800.0, "fallback"
-    traffic, traffic_note = ncu_traffic(wl.N * wl.D)
+    traffic, traffic_note = ncu_traffic(wl.N * wl.D, wl, res.route_name)
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
