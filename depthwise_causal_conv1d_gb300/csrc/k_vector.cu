@@ -132,12 +132,27 @@ __device__ __forceinline__ void update_vector(const UpdateParams &p) {
   const int64_t R = p.rows_per_cta;
   for (int64_t r0 = (int64_t)blockIdx.y * R; r0 < p.N; r0 += (int64_t)gridDim.y * R) {
     const int64_t r1 = r0 + R < p.N ? r0 + R : p.N;
-    for (int64_t n = r0; n < r1; n += 2) {
-      Row a, b;
-      load_row(n, a);
-      if (n + 1 < r1) load_row(n + 1, b);
-      store_row(n, a);
-      if (n + 1 < r1) store_row(n + 1, b);
+    if constexpr (kPlanes && RING) {
+      // The channel-last ring update holds 16 registers of loaded data per row and was
+      // bound by load latency with two rows in flight: four rows in flight took the large
+      // batch from 142.5 to 125.2 us (the other forms measured slower this way).
+      for (int64_t n = r0; n < r1; n += 4) {
+        Row rw[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (n + k < r1) load_row(n + k, rw[k]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (n + k < r1) store_row(n + k, rw[k]);
+      }
+    } else {
+      for (int64_t n = r0; n < r1; n += 2) {
+        Row a, b;
+        load_row(n, a);
+        if (n + 1 < r1) load_row(n + 1, b);
+        store_row(n, a);
+        if (n + 1 < r1) store_row(n + 1, b);
+      }
     }
   }
 }
@@ -224,6 +239,8 @@ cudaError_t launch_vector(const UpdateParams &p_in, int act, cudaStream_t stream
   const int64_t target_ctas = (int64_t)device_sm_count() * 32;
   int64_t R = (p.N * gx) / target_ctas;
   R = R < 1 ? 1 : (R > 8 ? 8 : R);
+  // The channel-last ring form walks its rows four at a time: whole groups of four.
+  if (p.layout == (int)Layout::ChannelLast && p.seqlens != nullptr) R = R < 4 ? 4 : (R + 3) / 4 * 4;
   int64_t gy = (p.N + R - 1) / R;
   if (gy > 65535) gy = 65535;  // the row loop strides over the rest
   p.rows_per_cta = (int)R;

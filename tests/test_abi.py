@@ -192,6 +192,8 @@ ROUTE_CASES = [
                                       stride_l=16384), "vector"),
     ("mid batch channel-last", dict(N=1024, D=16384, S=1024, stride_s=3 * 16384, stride_d=1,
                                     stride_l=16384), "bulk"),
+    ("mid batch channel-last ring", dict(N=1024, D=16384, S=1024, stride_s=3 * 16384, stride_d=1,
+                                         stride_l=16384, cache_seqlens=0x700000), "vector"),
     ("small batch channel-last", dict(N=32, D=16384, S=32, stride_s=3 * 16384, stride_d=1,
                                       stride_l=16384), "vector"),
     ("large batch L9", dict(N=4096, D=16384, S=4096, L=9), "staged"),
