@@ -235,10 +235,15 @@ cudaError_t launch_vector(const UpdateParams &p_in, int act, cudaStream_t stream
   if (groups < threads) threads = (int)((groups + 31) / 32 * 32);
   const int64_t gx = (groups + threads - 1) / threads;
   // Rows per CTA: enough CTAs for several waves on every SM, a few rows each so the
-  // weights loaded into registers are reused.
-  const int64_t target_ctas = (int64_t)device_sm_count() * 32;
+  // weights loaded into registers are reused and a thread has a pair of rows in flight.
+  // At least 4 rows once that still leaves a full wave of CTAs (two per SM): measured at
+  // D = 16384, 1024 rows took 63.6 us at one row per CTA and 47.2 us at four; 4096 rows
+  // take 164.4 us at six (the computed R), 170.0 at four and 242.4 at one.
+  const int64_t sms = device_sm_count();
+  const int64_t target_ctas = sms * 32;
   int64_t R = (p.N * gx) / target_ctas;
-  R = R < 1 ? 1 : (R > 8 ? 8 : R);
+  R = R > 8 ? 8 : R;
+  if (R < 4) R = p.N * gx >= 4 * 2 * sms ? 4 : 1;
   // The channel-last ring form walks its rows four at a time: whole groups of four.
   if (p.layout == (int)Layout::ChannelLast && p.seqlens != nullptr) R = R < 4 ? 4 : (R + 3) / 4 * 4;
   int64_t gy = (p.N + R - 1) / R;
