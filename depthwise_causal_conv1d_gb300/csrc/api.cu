@@ -130,34 +130,31 @@ bool route_serves(int route, const Args &a, Layout layout) {
 
 // Below this many (row, channel) elements a call is launch-bound and the plain vector
 // kernel's shorter start-up wins; above it the bulk-copy pipeline keeps more bytes in flight
-// (cold L2, D = 16384: tied at 64 rows, 12.3 vs 14.8 us at 128 rows, 24.6 vs 35.4 us at 512).
+// (compact state, cold L2, D = 16384: tied at 64 rows, 12.3 vs 14.8 us at 128 rows, 24.6 vs
+// 27.5 us at 512).
 constexpr int64_t kBulkMinElements = 1 << 20;
-constexpr int64_t kChannelLastBulkMaxElements = int64_t(3) << 24;
+constexpr int64_t kWindowOnlyW3VectorElements = int64_t(3) << 24;
 
 ccu_status_t choose(int requested, const Args &a, Layout layout, int *chosen) {
   if (requested < 0 || requested >= CCU_ROUTE_COUNT)
     return fail(CCU_ERR_INVALID_ARGUMENT, "unknown route %d", requested);
   if (requested == CCU_ROUTE_AUTO) {
-    // Batches from 2^20 elements take the bulk kernel, with two exceptions measured on the
-    // large batch (D = 16384, back to back). A one-entry state (L = 1) moves 8 bytes per
-    // element, too little per 512-channel slice for the bulk pipeline (W = 2: 100.8 us
-    // bulk, 80.7 us vector). With the channel-last state the bulk kernel leads from 128 to
-    // 2048 rows (1024 rows, ring: 44.8 vs 63.8 us), ties at 3072 and trails at 4096 rows
-    // (159.4 vs 163.7 us linear, 143.4 vs 156.9 us ring), so above 3 * 2^24 elements that
-    // layout stays on the vector kernel.
-    // Width 3 with L = 2 (a state of just the window) is the one compact case where the
-    // vector kernel, at three CTAs per SM, passes the bulk kernel on the full batch (4096
-    // rows: 119.0 vs 126.1 us; 1024 rows: 41.0 vs 36.8 us), so it stays on the vector kernel
-    // from 3 * 2^24 elements as the channel-last state does.
+    // Compact batches from 2^20 elements take the bulk kernel, with two exceptions measured
+    // on the large batch (D = 16384, back to back). A one-entry state (L = 1) moves 8 bytes
+    // per element, too little per 512-channel slice for the bulk pipeline (W = 2: 100.8 us
+    // bulk, 80.7 us vector). Width 3 with L = 2 (a state of just the window) is the one
+    // compact case where the vector kernel, at three CTAs per SM, passes the bulk kernel on
+    // the full batch (4096 rows: 119.0 vs 126.1 us; 1024 rows: 41.0 vs 36.8 us), so it stays
+    // on the vector kernel from 3 * 2^24 elements.
+    // The channel-last state stays on the vector kernel at every size. Ring: with four rows
+    // in flight per thread it leads the bulk kernel from 128 to 4096 rows (1024 rows: 37.0 vs
+    // 42.1 us; 4096 rows: 125.5 vs 156.9 us). Linear: at four to eight rows per CTA it leads
+    // the plane-bulk kernel from 64 to 2048 rows (1024 rows: 45.3 vs 47.2 us) and at 4096 rows
+    // (159.9 vs 164.7 us), and trails it by 1.5 % at 3072 rows.
     const int64_t elements = a.N * a.D;
-    const bool window_only_w3 = a.W == 3 && a.L == 2 && elements >= kChannelLastBulkMaxElements;
-    // The channel-last ring update (four rows in flight per thread on the vector kernel)
-    // leads the bulk kernel at every size measured, 128 to 4096 rows (1024 rows: 37.0 vs
-    // 42.1 us; 4096 rows: 125.5 vs 156.9 us), so it never takes the bulk kernel.
-    const bool bulk_size = layout == Layout::Compact
-                               ? elements >= kBulkMinElements && a.L >= 2 && !window_only_w3
-                               : elements >= kBulkMinElements && elements < kChannelLastBulkMaxElements &&
-                                     a.cache_seqlens == nullptr;
+    const bool window_only_w3 = a.W == 3 && a.L == 2 && elements >= kWindowOnlyW3VectorElements;
+    const bool bulk_size =
+        layout == Layout::Compact && elements >= kBulkMinElements && a.L >= 2 && !window_only_w3;
     if (bulk_size && route_serves(CCU_ROUTE_BULK, a, layout)) {
       *chosen = CCU_ROUTE_BULK;
     } else if (route_serves(CCU_ROUTE_VECTOR, a, layout)) {

@@ -191,7 +191,7 @@ ROUTE_CASES = [
     ("large batch channel-last", dict(N=4096, D=16384, S=4096, stride_s=3 * 16384, stride_d=1,
                                       stride_l=16384), "vector"),
     ("mid batch channel-last", dict(N=1024, D=16384, S=1024, stride_s=3 * 16384, stride_d=1,
-                                    stride_l=16384), "bulk"),
+                                    stride_l=16384), "vector"),
     ("mid batch channel-last ring", dict(N=1024, D=16384, S=1024, stride_s=3 * 16384, stride_d=1,
                                          stride_l=16384, cache_seqlens=0x700000), "vector"),
     ("small batch channel-last", dict(N=32, D=16384, S=32, stride_s=3 * 16384, stride_d=1,
