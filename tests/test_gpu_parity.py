@@ -999,3 +999,78 @@ def test_widths_prefill(W):
         y, f = oracle.full_causal_conv(x_btd[b], weight, bias, "silu", init[b], L)
         assert bf16_ulp_distance(from_dev_u16(out[b]), y.T).max() <= 1
         assert np.array_equal(from_dev_u16(fin[b]), f)
+
+
+# ----------------------------------------------------------------------------- timed workloads
+
+# The ring-buffer, width, multi-token and prefill workloads that the benchmark times, on
+# exactly its seeded inputs and entry points, at full size, against the oracle.
+
+@pytest.mark.parametrize("name", list(synthetic.RING_WORKLOADS) + list(synthetic.WIDTH_WORKLOADS))
+def test_timed_decode_variants_full_size(name):
+    wl = {**synthetic.RING_WORKLOADS, **synthetic.WIDTH_WORKLOADS}[name]
+    inp = synthetic.generate(wl)
+    want_out, want_state = oracle_ref(inp, wl.layout, cache_seqlens=inp.cache_seqlens)
+    got_out, got_state, _, ok = run_gpu(inp, wl.layout, "auto", cache_seqlens=inp.cache_seqlens)
+    assert ok, f"{name}: a guard band was overwritten"
+    assert_parity(inp, got_out, got_state, want_out, want_state, name)
+
+
+@pytest.mark.parametrize("name", list(synthetic.MULTI_WORKLOADS))
+def test_timed_multi_token_full_size(name):
+    import depthwise_causal_conv1d_gb300 as ccu
+    from oracle_pins import bf16_ulp_distance
+
+    wl = synthetic.MULTI_WORKLOADS[name]
+    inp = synthetic.generate(wl)
+    N, D, T, L, S = wl.N, wl.D, wl.T, wl.L, wl.S
+    want_state = inp.conv_state.copy()
+    want_out = oracle.conv1d_update_multi(inp.x, (T * D, 1, D), want_state, (D * L, L, 1), inp.weight,
+                                          inp.bias, wl.act, inp.indices, None, N, D, T, S, L, wl.W)
+    x = to_dev_u16(inp.x, DEV)  # [N, T, D] memory
+    st = to_dev_u16(inp.conv_state, DEV)
+    w = to_dev_u16(inp.weight, DEV)
+    b = to_dev_u16(inp.bias, DEV) if inp.bias is not None else None
+    idx = torch.from_numpy(inp.indices).to(DEV) if inp.indices is not None else None
+    out = torch.empty((N, T, D), dtype=torch.bfloat16, device=DEV)
+    act = ccu.CCU_ACT_SILU if wl.act == "silu" else ccu.CCU_ACT_IDENTITY
+    stream = torch.cuda.current_stream()
+    rc = ccu.lib.ccu_conv1d_update_multi(
+        x.data_ptr(), T * D, 1, D, st.data_ptr(), D * L, L, 1, w.data_ptr(),
+        None if b is None else b.data_ptr(), act, None if idx is None else idx.data_ptr(), None, N, D, T, S, L, wl.W, out.data_ptr(), T * D, 1, D, None, None,
+        ccu.ROUTES["auto"], stream.cuda_stream)
+    assert rc == 0, ccu.ccu_conv1d_last_error()
+    torch.cuda.synchronize()
+    assert np.array_equal(from_dev_u16(st), want_state)
+    got = from_dev_u16(out).transpose(0, 2, 1)  # [N, D, T], the oracle's order
+    limit = 0 if wl.act == "identity" else 1
+    assert bf16_ulp_distance(got, want_out).max() <= limit
+
+
+@pytest.mark.parametrize("name", list(synthetic.PREFILL_WORKLOADS))
+def test_timed_prefill_full_size(name):
+    import depthwise_causal_conv1d_gb300 as ccu
+    from oracle_pins import bf16_ulp_distance
+
+    spec = synthetic.PREFILL_WORKLOADS[name]
+    x_btd, weight, bias = synthetic.generate_prefill(spec)
+    B, T, D, L, W = spec["B"], spec["T"], spec["D"], spec["L"], spec["W"]
+    x = to_dev_u16(x_btd, DEV).permute(0, 2, 1)  # [B, D, T] view of token-major memory
+    w = to_dev_u16(weight, DEV)
+    b = to_dev_u16(bias, DEV) if bias is not None else None
+    out = torch.empty_like(x)
+    fin = torch.empty((B, L, D), dtype=torch.bfloat16, device=DEV).permute(0, 2, 1)
+    act = ccu.CCU_ACT_SILU if spec["act"] == "silu" else ccu.CCU_ACT_IDENTITY
+    rc = ccu.lib.ccu_causal_conv1d_fwd(
+        x.data_ptr(), *x.stride(), w.data_ptr(), None if b is None else b.data_ptr(), act,
+        None, 0, 0, 0, B, D, T, L, W, out.data_ptr(), *out.stride(), fin.data_ptr(), *fin.stride(),
+        ccu.ROUTES["auto"], torch.cuda.current_stream().cuda_stream)
+    assert rc == 0, ccu.ccu_conv1d_last_error()
+    torch.cuda.synchronize()
+    got_y = from_dev_u16(out.permute(0, 2, 1))  # [B, T, D]
+    got_fin = from_dev_u16(fin)  # [B, D, L]
+    limit = 0 if spec["act"] == "identity" else 1
+    for bb in range(B):
+        want_y, want_fin = oracle.full_causal_conv(x_btd[bb], weight, bias, spec["act"], None, L)
+        assert np.array_equal(got_fin[bb], want_fin), f"sequence {bb}: final state differs"
+        assert bf16_ulp_distance(got_y[bb], want_y).max() <= limit, f"sequence {bb}: output"
