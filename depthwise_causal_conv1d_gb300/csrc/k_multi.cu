@@ -185,9 +185,10 @@ __global__ void __launch_bounds__(256, 2) k_multi_vector(UpdateParams p, MultiPa
         uint32_t nw[4 * L];
         uint4 outv;
         if constexpr (RING) {
-          outv = update8_compact_ring<L, kW, ACT>(xw, r.ow, wv, bv, has_bias, (int)((r.slot.q + t) % L), nw);
+          outv = update8_compact_ring<L, kW, ACT, true>(xw, r.ow, wv, bv, has_bias,
+                                                        (int)((r.slot.q + t) % L), nw);
         } else {
-          outv = update8_compact<L, kW, ACT>(xw, r.ow, wv, bv, has_bias, nw);
+          outv = update8_compact<L, kW, ACT, true>(xw, r.ow, wv, bv, has_bias, nw);
         }
         st_stream(orow + t * m.sot, outv);
 #pragma unroll
