@@ -37,6 +37,7 @@ using namespace bulk;
 // RING: conv_state is a ring buffer indexed by cache_seqlens (entry q replaced by x).
 template <int L, int W, int ACT, int G, bool RING>
 __global__ void __launch_bounds__(kThreads) k_update_bulk(UpdateParams p, int stages, int64_t stage_bytes) {
+  grid_dependency_boundary();
   constexpr int64_t kSlice = 256 * G;
   extern __shared__ __align__(128) unsigned char smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -209,8 +210,8 @@ cudaError_t launch_LAR(const UpdateParams &p, cudaStream_t stream) {
   if (warps > items) warps = items;
   int64_t grid = (warps + kWarps - 1) / kWarps;
   if (grid < 1) grid = 1;
-  k_update_bulk<L, W, ACT, kGroups, RING><<<(unsigned)grid, kThreads, smem, stream>>>(p, P, sb);
-  return cudaGetLastError();
+  return launch_overlapped(k_update_bulk<L, W, ACT, kGroups, RING>, dim3((unsigned)grid), dim3(kThreads),
+                           smem, stream, p, P, sb);
 }
 
 template <int L, int W, int ACT>

@@ -45,6 +45,7 @@ __host__ __device__ constexpr int plane_buffers() {
 template <int L, int ACT, bool RING>
 __global__ void __launch_bounds__(kThreads) k_update_bulk_planes(UpdateParams p, int stages,
                                                                  int64_t stage_bytes) {
+  grid_dependency_boundary();
   constexpr int NB = plane_buffers<L, RING>();
   // First plane held in buffer 0 for the linear state (0 when L == 3, else 1).
   constexpr int first = (L == kW - 1) ? 0 : 1;
@@ -220,8 +221,8 @@ cudaError_t launch_LAR(const UpdateParams &p, cudaStream_t stream) {
   if (warps > items) warps = items;
   int64_t grid = (warps + kWarps - 1) / kWarps;
   if (grid < 1) grid = 1;
-  k_update_bulk_planes<L, ACT, RING><<<(unsigned)grid, kThreads, smem, stream>>>(p, P, sb);
-  return cudaGetLastError();
+  return launch_overlapped(k_update_bulk_planes<L, ACT, RING>, dim3((unsigned)grid), dim3(kThreads), smem,
+                           stream, p, P, sb);
 }
 
 template <int L, int ACT>

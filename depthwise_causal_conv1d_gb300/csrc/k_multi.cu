@@ -21,6 +21,7 @@ namespace {
 // One thread per (row, channel), any x / out strides, any L: the correctness anchor.
 template <int ACT>
 __global__ void __launch_bounds__(256) k_multi_scalar(UpdateParams p, MultiParams m) {
+  grid_dependency_boundary();
   const int64_t total = p.N * p.D;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -116,6 +117,7 @@ __device__ __forceinline__ void compact_to_planes(const uint32_t (&cw)[4 * L], u
 // per SM, and loses).
 template <int L, int ACT, int LAYOUT, bool RING>
 __global__ void __launch_bounds__(256, 2) k_multi_vector(UpdateParams p, MultiParams m) {
+  grid_dependency_boundary();
   const int64_t groups = p.D >> 3;
   const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (g >= groups) return;
@@ -230,14 +232,13 @@ template <int L, int ACT>
 cudaError_t launch_vec_L(const UpdateParams &p, const MultiParams &m, dim3 grid, dim3 block,
                          cudaStream_t stream) {
   const bool ring = p.seqlens != nullptr;
-  if (p.layout == (int)Layout::Compact) {
-    if (ring) k_multi_vector<L, ACT, (int)Layout::Compact, true><<<grid, block, 0, stream>>>(p, m);
-    else k_multi_vector<L, ACT, (int)Layout::Compact, false><<<grid, block, 0, stream>>>(p, m);
-  } else {
-    if (ring) k_multi_vector<L, ACT, (int)Layout::ChannelLast, true><<<grid, block, 0, stream>>>(p, m);
-    else k_multi_vector<L, ACT, (int)Layout::ChannelLast, false><<<grid, block, 0, stream>>>(p, m);
+  constexpr int kC = (int)Layout::Compact, kCL = (int)Layout::ChannelLast;
+  if (p.layout == kC) {
+    return ring ? launch_overlapped(k_multi_vector<L, ACT, kC, true>, grid, block, 0, stream, p, m)
+                : launch_overlapped(k_multi_vector<L, ACT, kC, false>, grid, block, 0, stream, p, m);
   }
-  return cudaGetLastError();
+  return ring ? launch_overlapped(k_multi_vector<L, ACT, kCL, true>, grid, block, 0, stream, p, m)
+              : launch_overlapped(k_multi_vector<L, ACT, kCL, false>, grid, block, 0, stream, p, m);
 }
 
 template <int ACT>
@@ -263,12 +264,9 @@ cudaError_t launch_multi_scalar(const UpdateParams &p, const MultiParams &m, int
   const int64_t cap = (int64_t)device_sm_count() * 16;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  if (act == 1) {
-    k_multi_scalar<1><<<(unsigned)blocks, threads, 0, stream>>>(p, m);
-  } else {
-    k_multi_scalar<0><<<(unsigned)blocks, threads, 0, stream>>>(p, m);
-  }
-  return cudaGetLastError();
+  const dim3 grid((unsigned)blocks), block(threads);
+  return act == 1 ? launch_overlapped(k_multi_scalar<1>, grid, block, 0, stream, p, m)
+                  : launch_overlapped(k_multi_scalar<0>, grid, block, 0, stream, p, m);
 }
 
 cudaError_t launch_multi_vector(const UpdateParams &p, const MultiParams &m, int act,

@@ -45,6 +45,7 @@ __device__ __forceinline__ void write_final(const UpdateParams &p, const Prefill
 // One thread per (batch row, channel, token chunk); any strides.
 template <int ACT>
 __global__ void __launch_bounds__(256) k_prefill_scalar(UpdateParams p, PrefillParams f) {
+  grid_dependency_boundary();
   const int64_t chunks = (f.T + f.chunk - 1) / f.chunk;
   const int64_t total = f.B * p.D * chunks;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
@@ -181,6 +182,7 @@ __device__ __forceinline__ void load_halo_s(const UpdateParams &p, const Prefill
 // float windows, 105 us with the loads one group ahead).
 template <int ACT>
 __global__ void __launch_bounds__(256) k_prefill_vector(UpdateParams p, PrefillParams f) {
+  grid_dependency_boundary();
   const int64_t groups = p.D >> 3;
   const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (g >= groups) return;
@@ -323,6 +325,7 @@ static_assert(kP * 8 + 8 + sizeof(Cursor) <= kHeadBytes, "warp header too small"
 
 template <int ACT>
 __global__ void __launch_bounds__(kPThreads, 1) k_prefill_bulk(UpdateParams p, PrefillParams f) {
+  grid_dependency_boundary();
   using namespace bulk;
   extern __shared__ __align__(128) unsigned char smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -481,8 +484,7 @@ cudaError_t launch_prefill_bulk_act(const UpdateParams &p, PrefillParams f, cuda
   const int64_t groups = f.B * ((p.D + kRunCh - 1) / kRunCh) * ((f.T + kTG - 1) / kTG);
   int64_t grid = (groups + kPWarps - 1) / kPWarps;
   if (grid > ctas) grid = ctas;
-  k_prefill_bulk<ACT><<<(unsigned)grid, kPThreads, smem, stream>>>(p, f);
-  return cudaGetLastError();
+  return launch_overlapped(k_prefill_bulk<ACT>, dim3((unsigned)grid), dim3(kPThreads), smem, stream, p, f);
 }
 
 }  // namespace
@@ -497,11 +499,8 @@ cudaError_t launch_prefill(const UpdateParams &p, const PrefillParams &f, int ac
     const int64_t gy = (f.T + f.chunk - 1) / f.chunk;
     if (gy > 65535 || f.B > 65535) return cudaErrorInvalidConfiguration;
     const dim3 grid((unsigned)gx, (unsigned)gy, (unsigned)f.B);
-    if (act == 1) {
-      k_prefill_vector<1><<<grid, threads, 0, stream>>>(p, f);
-    } else {
-      k_prefill_vector<0><<<grid, threads, 0, stream>>>(p, f);
-    }
+    return act == 1 ? launch_overlapped(k_prefill_vector<1>, grid, dim3(threads), 0, stream, p, f)
+                    : launch_overlapped(k_prefill_vector<0>, grid, dim3(threads), 0, stream, p, f);
   } else {
     const int threads = 256;
     const int64_t chunks = (f.T + f.chunk - 1) / f.chunk;
@@ -509,13 +508,10 @@ cudaError_t launch_prefill(const UpdateParams &p, const PrefillParams &f, int ac
     const int64_t cap = (int64_t)device_sm_count() * 16;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    if (act == 1) {
-      k_prefill_scalar<1><<<(unsigned)blocks, threads, 0, stream>>>(p, f);
-    } else {
-      k_prefill_scalar<0><<<(unsigned)blocks, threads, 0, stream>>>(p, f);
-    }
+    const dim3 grid((unsigned)blocks), block(threads);
+    return act == 1 ? launch_overlapped(k_prefill_scalar<1>, grid, block, 0, stream, p, f)
+                    : launch_overlapped(k_prefill_scalar<0>, grid, block, 0, stream, p, f);
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_prefill_bulk(const UpdateParams &p, const PrefillParams &f, int act,

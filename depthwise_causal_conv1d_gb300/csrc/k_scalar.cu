@@ -15,6 +15,7 @@ namespace {
 // entries and x, computes the output, then shifts its own channel's state in place.
 template <int ACT>
 __global__ void __launch_bounds__(256) k_update_scalar(UpdateParams p) {
+  grid_dependency_boundary();
   const int64_t total = p.N * p.D;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
@@ -55,6 +56,7 @@ __global__ void __launch_bounds__(256) k_update_scalar(UpdateParams p) {
 // bit in *status. No trap, no wait.
 __global__ void __launch_bounds__(256) k_check_indices(const int32_t *idx, int64_t N, int64_t S,
                                                        uint32_t *bitmap, int32_t *status) {
+  grid_dependency_boundary();
   for (int64_t n = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; n < N;
        n += (int64_t)gridDim.x * blockDim.x) {
     const int64_t s = idx[n];
@@ -80,20 +82,15 @@ int64_t grid_for(int64_t work, int threads) {
 cudaError_t launch_scalar(const UpdateParams &p, int act, cudaStream_t stream) {
   const int threads = 256;
   const dim3 grid((unsigned)grid_for(p.N * p.D, threads));
-  if (act == 1) {
-    k_update_scalar<1><<<grid, threads, 0, stream>>>(p);
-  } else {
-    k_update_scalar<0><<<grid, threads, 0, stream>>>(p);
-  }
-  return cudaGetLastError();
+  return act == 1 ? launch_overlapped(k_update_scalar<1>, grid, dim3(threads), 0, stream, p)
+                  : launch_overlapped(k_update_scalar<0>, grid, dim3(threads), 0, stream, p);
 }
 
 cudaError_t launch_check_indices(const int32_t *idx, int64_t N, int64_t S, uint32_t *bitmap,
                                  int32_t *status, cudaStream_t stream) {
   const int threads = 256;
   const dim3 grid((unsigned)grid_for(N, threads));
-  k_check_indices<<<grid, threads, 0, stream>>>(idx, N, S, bitmap, status);
-  return cudaGetLastError();
+  return launch_overlapped(k_check_indices, grid, dim3(threads), 0, stream, idx, N, S, bitmap, status);
 }
 
 }  // namespace ccu

@@ -75,6 +75,7 @@ __device__ __forceinline__ uint4 outputs8(const uint32_t (&h)[3][8], const uint3
 // Compact layout. Dynamic shared memory: 8*T*L BF16 for the slab, then 8*T BF16 for x.
 template <int ACT>
 __global__ void __launch_bounds__(256) k_update_staged_compact(UpdateParams p) {
+  grid_dependency_boundary();
   extern __shared__ uint4 smem[];
   const int T = blockDim.x;
   const int tid = threadIdx.x;
@@ -160,6 +161,7 @@ __global__ void __launch_bounds__(256) k_update_staged_compact(UpdateParams p) {
 // in flight before their stores.
 template <int ACT>
 __global__ void __launch_bounds__(256) k_update_staged_chlast(UpdateParams p) {
+  grid_dependency_boundary();
   const int64_t groups = p.D >> 3;
   const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (g >= groups) return;
@@ -238,8 +240,8 @@ cudaError_t launch_compact(const UpdateParams &p, cudaStream_t stream) {
   if (gy < 1) gy = 1;
   if (gy > p.N) gy = p.N;
   if (gy > 65535) gy = 65535;
-  k_update_staged_compact<ACT><<<dim3((unsigned)gx, (unsigned)gy), T, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_overlapped(k_update_staged_compact<ACT>, dim3((unsigned)gx, (unsigned)gy), dim3(T), smem,
+                           stream, p);
 }
 
 template <int ACT>
@@ -252,8 +254,8 @@ cudaError_t launch_chlast(const UpdateParams &p, cudaStream_t stream) {
   if (gy < 1) gy = 1;
   if (gy > p.N) gy = p.N;
   if (gy > 65535) gy = 65535;
-  k_update_staged_chlast<ACT><<<dim3((unsigned)gx, (unsigned)gy), T, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_overlapped(k_update_staged_chlast<ACT>, dim3((unsigned)gx, (unsigned)gy), dim3(T), 0,
+                           stream, p);
 }
 
 }  // namespace

@@ -160,6 +160,7 @@ __device__ __forceinline__ void update_vector(const UpdateParams &p) {
 // Register budget left to the compiler (two CTAs per SM at the register counts it picks).
 template <int L, int W, int ACT, int LAYOUT, bool RING>
 __global__ void __launch_bounds__(256) k_update_vector(UpdateParams p) {
+  grid_dependency_boundary();
   update_vector<L, W, ACT, LAYOUT, RING>(p);
 }
 
@@ -168,15 +169,16 @@ __global__ void __launch_bounds__(256) k_update_vector(UpdateParams p) {
 // slower with that cap.
 template <int L, int ACT, int LAYOUT, bool RING>
 __global__ void __launch_bounds__(256, 3) k_update_vector_w3(UpdateParams p) {
+  grid_dependency_boundary();
   update_vector<L, 3, ACT, LAYOUT, RING>(p);
 }
 
 template <int L, int W, int ACT, int LAYOUT, bool RING>
-void launch_one(const UpdateParams &p, dim3 grid, dim3 block, cudaStream_t stream) {
+cudaError_t launch_one(const UpdateParams &p, dim3 grid, dim3 block, cudaStream_t stream) {
   if constexpr (W == 3) {
-    k_update_vector_w3<L, ACT, LAYOUT, RING><<<grid, block, 0, stream>>>(p);
+    return launch_overlapped(k_update_vector_w3<L, ACT, LAYOUT, RING>, grid, block, 0, stream, p);
   } else {
-    k_update_vector<L, W, ACT, LAYOUT, RING><<<grid, block, 0, stream>>>(p);
+    return launch_overlapped(k_update_vector<L, W, ACT, LAYOUT, RING>, grid, block, 0, stream, p);
   }
 }
 
@@ -184,19 +186,11 @@ template <int L, int W, int ACT>
 cudaError_t launch_LW(const UpdateParams &p, dim3 grid, dim3 block, cudaStream_t stream) {
   const bool ring = p.seqlens != nullptr;
   if (p.layout == (int)Layout::Compact) {
-    if (ring) {
-      launch_one<L, W, ACT, (int)Layout::Compact, true>(p, grid, block, stream);
-    } else {
-      launch_one<L, W, ACT, (int)Layout::Compact, false>(p, grid, block, stream);
-    }
-  } else {
-    if (ring) {
-      launch_one<L, W, ACT, (int)Layout::ChannelLast, true>(p, grid, block, stream);
-    } else {
-      launch_one<L, W, ACT, (int)Layout::ChannelLast, false>(p, grid, block, stream);
-    }
+    return ring ? launch_one<L, W, ACT, (int)Layout::Compact, true>(p, grid, block, stream)
+                : launch_one<L, W, ACT, (int)Layout::Compact, false>(p, grid, block, stream);
   }
-  return cudaGetLastError();
+  return ring ? launch_one<L, W, ACT, (int)Layout::ChannelLast, true>(p, grid, block, stream)
+              : launch_one<L, W, ACT, (int)Layout::ChannelLast, false>(p, grid, block, stream);
 }
 
 // L from W - 1 (the shortest state the contract allows) up to kVectorMaxL.
