@@ -34,6 +34,13 @@
  *    errors are reported as CCU_ERR_CUDA; errors of the asynchronous execution surface
  *    at the caller's next synchronization.
  *  - `stream` is a cudaStream_t; NULL is the legacy default stream.
+ *  - Kernels are launched with programmatic stream serialization (programmatic dependent
+ *    launch), and each one waits for all earlier work on `stream` to complete
+ *    (griddepcontrol.wait) before it touches memory, so the order is that of a plain
+ *    launch: only the launch and start-up of consecutive calls overlap. Work the caller
+ *    enqueues after a call sees its results, as usual, unless the caller launches its own
+ *    kernel with programmatic dependent launch: such a kernel must wait itself
+ *    (griddepcontrol.wait / cudaGridDependencySynchronize) before reading them.
  *  - BF16 tensors are passed as `const void*` / `void*` to 16-bit storage.
  *  - Every argument check happens before any launch; a declined call changes nothing.
  *  - Sizes are elements, not bytes. Strides are elements.
