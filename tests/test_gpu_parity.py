@@ -261,6 +261,11 @@ def test_side_stream_with_default_stream_parked():
     host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     host_state = torch.empty(st.shape, dtype=st.dtype, pin_memory=True)
     side = torch.cuda.Stream()
+    # A process's first call of a kernel loads its module and sets its attributes, which may
+    # synchronize the device: make that call (on copies) before the default stream is parked.
+    warm_out, warm_st = torch.empty_like(out), st.clone()
+    with torch.cuda.stream(side):
+        ccu.causal_conv1d_update(x, warm_st, w, b, "silu", conv_state_indices=idx, out=warm_out)
     torch.cuda.synchronize()
     # nothing below allocates device or pinned memory, which could synchronize the device
     torch.cuda._sleep(200_000_000)  # parks the default stream for ~0.1 s (bounded spin)
@@ -387,6 +392,11 @@ def test_side_stream_prefill_and_multi_token():
     h_pre = torch.empty((B, T, D), dtype=torch.bfloat16, pin_memory=True)
     h_multi = torch.empty((B, K, D), dtype=torch.bfloat16, pin_memory=True)
     side = torch.cuda.Stream()
+    # first calls of these kernels (module load, attributes) before the default stream is parked
+    fin_w, y_pre_w, y_multi_w = torch.empty_like(fin), torch.empty_like(y_pre), torch.empty_like(y_multi)
+    with torch.cuda.stream(side):
+        ccu.causal_conv1d_fwd(x_pre, w, b, "silu", final_states_out=fin_w, out=y_pre_w, route="bulk")
+        ccu.causal_conv1d_update(x_multi, fin_w, w, b, "silu", out=y_multi_w)
     torch.cuda.synchronize()
     torch.cuda._sleep(200_000_000)  # parks the default stream for ~0.1 s (bounded spin)
     with torch.cuda.stream(side):
@@ -1074,3 +1084,55 @@ def test_timed_prefill_full_size(name):
         want_y, want_fin = oracle.full_causal_conv(x_btd[bb], weight, bias, spec["act"], None, L)
         assert np.array_equal(got_fin[bb], want_fin), f"sequence {bb}: final state differs"
         assert bf16_ulp_distance(got_y[bb], want_y).max() <= limit, f"sequence {bb}: output"
+
+
+@pytest.mark.parametrize("route", ["vector", "bulk"])
+def test_stream_order_with_foreign_kernels(route):
+    """Calls interleaved on one stream with torch kernels that write x and a state slot
+    before each call and read its output after it: every call sees the writes made before
+    it and its output is complete for the read after it (the kernels are launched as
+    programmatic dependents and wait for prior work before touching memory)."""
+    import depthwise_causal_conv1d_gb300 as ccu
+    from oracle_pins import bf16_ulp_distance
+
+    wl = synthetic.variant(synthetic.WORKLOADS["paged_n256_d8192_l3_s1024_pad10_silu"], name="order",
+                           N=256, D=8192, S=300, indices="distinct_pad", pad_frac=0.1)
+    inp = synthetic.generate(wl, seed=31)
+    rng = np.random.default_rng(32)
+    steps = 6
+    xs = [synthetic.f64_to_bf16_bits(rng.standard_normal((wl.N, wl.D))) for _ in range(steps)]
+    s0 = int(inp.indices[np.flatnonzero(inp.indices >= 0)[0]])
+    patch = synthetic.f64_to_bf16_bits(rng.standard_normal((wl.D, wl.L)))
+    # oracle: the same sequence on the host
+    state = inp.conv_state.copy()
+    want = []
+    for k in range(steps):
+        if k % 2:
+            state[s0] = patch
+        want.append(oracle.conv1d_update(xs[k], wl.D, state, (wl.D * wl.L, wl.L, 1), inp.weight, inp.bias,
+                                         wl.act, inp.indices, wl.N, wl.D, wl.S, wl.L, wl.W))
+    # device: torch writes and reads around every call, all on one side stream
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        x_src = [to_dev_u16(a, DEV) for a in xs]
+        patch_d = to_dev_u16(patch, DEV)
+        x = torch.empty((wl.N, wl.D), dtype=torch.bfloat16, device=DEV)
+        st = to_dev_u16(inp.conv_state, DEV)
+        w = to_dev_u16(inp.weight, DEV)
+        b = to_dev_u16(inp.bias, DEV)
+        idx = torch.from_numpy(inp.indices).to(DEV)
+        out = torch.empty((wl.N, wl.D), dtype=torch.bfloat16, device=DEV)
+        got = [torch.empty_like(out) for _ in range(steps)]
+        stream.synchronize()
+        for k in range(steps):
+            x.copy_(x_src[k])
+            if k % 2:
+                st[s0].copy_(patch_d)
+            ccu.causal_conv1d_update(x, st, w, b, wl.act, conv_state_indices=idx, out=out, route=route)
+            got[k].copy_(out)
+    stream.synchronize()
+    final_state = from_dev_u16(st)
+    for k in range(steps):
+        dist = bf16_ulp_distance(from_dev_u16(got[k]), want[k])
+        assert dist.max() <= 1, f"step {k}: output off by {dist.max()} ulp"
+    assert np.array_equal(final_state, state)
