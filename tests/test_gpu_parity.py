@@ -1136,3 +1136,115 @@ def test_stream_order_with_foreign_kernels(route):
         dist = bf16_ulp_distance(from_dev_u16(got[k]), want[k])
         assert dist.max() <= 1, f"step {k}: output off by {dist.max()} ulp"
     assert np.array_equal(final_state, state)
+
+
+# ----------------------------------------------------------------------------- 64-bit offsets
+
+BIG_D, BIG_L = 16384, 3
+BIG_S = (1 << 31) // (BIG_D * BIG_L) + 48  # state of ~2.15e9 elements: the last slots lie past 2^31
+
+
+def _big_state(layout):
+    """A 4.3 GB BF16 state filled on the device (N(0,1)); returns (memory, logical [S, D, L])."""
+    torch.manual_seed(7)
+    if layout == "compact":
+        mem = torch.randn((BIG_S, BIG_D, BIG_L), dtype=torch.bfloat16, device=DEV)
+        return mem, mem
+    mem = torch.randn((BIG_S, BIG_L, BIG_D), dtype=torch.bfloat16, device=DEV)
+    return mem, mem.permute(0, 2, 1)
+
+
+def _big_slots():
+    """Slots past element 2^31, the one that straddles it, small ones, and padding rows."""
+    first_past = (1 << 31) // (BIG_D * BIG_L) + 1
+    slots = [BIG_S - 1, BIG_S - 2, first_past, first_past - 1, first_past + 7, 0, 5, 1000, -1, BIG_S - 30, -1, 12345]
+    return np.array(slots, dtype=np.int32)
+
+
+@pytest.mark.parametrize("layout", ["compact", "channel_last"])
+@pytest.mark.parametrize("route", ["scalar", "vector", "staged", "bulk", "multi"])
+def test_state_offsets_past_int32(layout, route):
+    """Slots whose state starts past element 2^31 of a 4.3 GB state, on every route. The
+    oracle runs on the touched slots only (a row's update reads and writes its own slot
+    alone); untouched neighbours must keep their bytes."""
+    import depthwise_causal_conv1d_gb300 as ccu
+    from oracle_pins import bf16_ulp_distance
+
+    D, L, W = BIG_D, BIG_L, 4
+    mem, st = _big_state(layout)
+    idx_np = _big_slots()
+    N = len(idx_np)
+    T = 3 if route == "multi" else 1
+    rng = np.random.default_rng(8)
+    x_np = synthetic.f64_to_bf16_bits(rng.standard_normal((N, T, D)))
+    w_np = synthetic.f64_to_bf16_bits(rng.standard_normal((D, W)) * 0.5)
+    b_np = synthetic.f64_to_bf16_bits(rng.standard_normal(D) * 0.1)
+    touched = idx_np[idx_np >= 0]
+    t_dev = torch.from_numpy(touched.astype(np.int64)).to(DEV)
+    mini = from_dev_u16(st[t_dev])  # [k, D, L] logical, before
+    neighbours = np.array([s for s in {0, 1, 4, 6, 999, 1001, int(touched.max()) - 2} if s not in set(touched)],
+                          dtype=np.int64)
+    nb_dev = torch.from_numpy(neighbours).to(DEV)
+    nb_before = from_dev_u16(st[nb_dev])
+    remap = {int(s): i for i, s in enumerate(touched)}
+    idx_mini = np.array([remap[int(s)] if s >= 0 else -1 for s in idx_np], dtype=np.int32)
+    w, b = to_dev_u16(w_np, DEV), to_dev_u16(b_np, DEV)
+    idx = torch.from_numpy(idx_np).to(DEV)
+    if route == "multi":
+        want_out = oracle.conv1d_update_multi(x_np, (T * D, 1, D), mini, (D * L, L, 1), w_np, b_np, "silu",
+                                              idx_mini, None, N, D, T, len(touched), L, W)
+        x = to_dev_u16(x_np, DEV).permute(0, 2, 1)  # [N, D, T] view of [N, T, D] memory
+        out = ccu.causal_conv1d_update(x, st, w, b, "silu", conv_state_indices=idx)
+        got_out = from_dev_u16(out)
+    else:
+        x2 = np.ascontiguousarray(x_np[:, 0, :])
+        want_out = oracle.conv1d_update(x2, D, mini, (D * L, L, 1), w_np, b_np, "silu", idx_mini, N, D,
+                                        len(touched), L, W)
+        out = torch.empty((N, D), dtype=torch.bfloat16, device=DEV)
+        ccu.causal_conv1d_update(to_dev_u16(x2, DEV), st, w, b, "silu", conv_state_indices=idx, out=out,
+                                 route=route)
+        got_out = from_dev_u16(out)
+    torch.cuda.synchronize()
+    got_mini = from_dev_u16(st[t_dev])
+    nb_after = from_dev_u16(st[nb_dev])
+    del mem, st
+    torch.cuda.empty_cache()
+    assert np.array_equal(got_mini, mini), "touched slots' state differs from the oracle"
+    assert np.array_equal(nb_after, nb_before), "an untouched slot changed"
+    assert bf16_ulp_distance(got_out, want_out).max() <= 1
+
+
+@pytest.mark.parametrize("route", ["scalar", "vector", "bulk"])
+def test_prefill_offsets_past_int32(route):
+    """A prefill whose x and out hold more than 2^31 elements (B=1, D=16384, T=131104,
+    token-major): the first and last tokens' outputs and the final state against the
+    oracle (the last window starts from the three tokens before it)."""
+    import depthwise_causal_conv1d_gb300 as ccu
+    from oracle_pins import bf16_ulp_distance
+
+    D, L, W, T, K = 16384, 3, 4, 131104, 40
+    assert T * D > (1 << 31)
+    torch.manual_seed(9)
+    x_mem = torch.randn((1, T, D), dtype=torch.bfloat16, device=DEV)
+    x = x_mem.permute(0, 2, 1)
+    rng = np.random.default_rng(10)
+    w_np = synthetic.f64_to_bf16_bits(rng.standard_normal((D, W)) * 0.5)
+    b_np = synthetic.f64_to_bf16_bits(rng.standard_normal(D) * 0.1)
+    out = torch.empty_like(x)
+    fin = torch.empty((1, L, D), dtype=torch.bfloat16, device=DEV).permute(0, 2, 1)
+    ccu.causal_conv1d_fwd(x, to_dev_u16(w_np, DEV), to_dev_u16(b_np, DEV), "silu", final_states_out=fin,
+                          out=out, route=route)
+    torch.cuda.synchronize()
+    head_x = from_dev_u16(x_mem[0, :K])
+    tail_x = from_dev_u16(x_mem[0, T - K - L:])
+    head_y = from_dev_u16(out.permute(0, 2, 1)[0, :K])
+    tail_y = from_dev_u16(out.permute(0, 2, 1)[0, T - K:])
+    got_fin = from_dev_u16(fin[0])
+    del x_mem, x, out
+    torch.cuda.empty_cache()
+    want_head, _ = oracle.full_causal_conv(head_x, w_np, b_np, "silu", None, L)
+    init = np.ascontiguousarray(tail_x[:L].T)  # [D, L]: the three tokens before the window
+    want_tail, want_fin = oracle.full_causal_conv(tail_x[L:], w_np, b_np, "silu", init, L)
+    assert bf16_ulp_distance(head_y, want_head).max() <= 1
+    assert bf16_ulp_distance(tail_y, want_tail).max() <= 1
+    assert np.array_equal(got_fin, want_fin)
