@@ -224,3 +224,22 @@ def test_check_indices_declines(ccu):
     assert ccu.ccu_conv1d_check_indices(None, 4, 4, 0x900000, 0x800000, None) == 1
     assert ccu.ccu_conv1d_check_indices(IDX + 1, 4, 4, 0x900000, 0x800000, None) == 1
     assert ccu.ccu_conv1d_check_indices(IDX, -1, 4, 0x900000, 0x800000, None) == 1
+
+
+def test_every_kernel_waits_for_prior_grids_first():
+    """Kernels are launched as programmatic dependents: each must run
+    grid_dependency_boundary() before anything else, and every launch must go through
+    launch_overlapped (no triple-chevron launch that would skip the attribute)."""
+    import pathlib
+
+    csrc = pathlib.Path(ROOT) / "depthwise_causal_conv1d_gb300" / "csrc"
+    kernels = 0
+    for path in sorted(csrc.glob("*.cu")):
+        src = path.read_text()
+        assert "<<<" not in src, f"{path.name}: launch outside launch_overlapped"
+        for m in re.finditer(r"__global__ void[^{;]*\{", src):
+            body = src[m.end():].lstrip()
+            assert body.startswith("grid_dependency_boundary();"), \
+                f"{path.name}: kernel at offset {m.start()} does not wait for prior grids first"
+            kernels += 1
+    assert kernels >= 13
