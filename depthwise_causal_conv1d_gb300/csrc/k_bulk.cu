@@ -182,9 +182,11 @@ int64_t stage_bytes_for(int64_t L) {
 template <int L, int W, int ACT, bool RING>
 cudaError_t launch_LAR(const UpdateParams &p, cudaStream_t stream) {
   const int64_t sb = stage_bytes_for(L);
-  // About 8 KB of stages per warp (two 4 KB stages at L = 3): 3 CTAs of 8 warps fit an SM.
-  // Measured on the large batch: slices of 512 channels with two stages beat 256-channel
-  // slices with four (larger bulk copies) and deeper rings with fewer resident warps.
+  // About 8 KB of stages per warp (two 4 KB stages at L = 3), 66 KB a CTA; the registers
+  // (99 a thread at L = 3) keep 2 CTAs of 8 warps resident per SM. Measured on the large
+  // batch: slices of 512 channels with two stages beat 256-channel slices with four (larger
+  // bulk copies); more in flight (three stages, or 3 CTAs per SM under a register cap) and
+  // less (one CTA per SM) were both slower at full size.
   int P = (int)(8 * 1024 / sb);
   P = P < 2 ? 2 : (P > kMaxStages ? kMaxStages : P);
   const size_t smem = (size_t)kWarps * (kBarrierBytes + (size_t)P * sb);
