@@ -217,6 +217,14 @@ def _check_tensor(name, t, dtype, torch):
         raise ValueError(f"{name} requires grad: the update is inference-only (autograd unsupported)")
 
 
+def _same_device(ref, named, ref_name="x"):
+    """Every tensor of a call on the device of ``ref`` (the kernels get raw pointers)."""
+    for name, t in named:
+        if t is not None and t.device != ref.device:
+            raise ValueError(f"{name} is on {t.device} but {ref_name} is on {ref.device}: "
+                             "all tensors of a call must be on one device")
+
+
 def causal_conv1d_update(x, conv_state, weight, bias=None, activation=None, *, cache_seqlens=None,
                          conv_state_indices=None, out=None, route: str = "auto", status=None,
                          intermediate_states=None):
@@ -283,13 +291,17 @@ def causal_conv1d_update(x, conv_state, weight, bias=None, activation=None, *, c
         raise ValueError(f"route must be one of {sorted(ROUTES)}")
     if status is not None:
         _check_tensor("status", status, torch.int32, torch)
+    _same_device(x, (("conv_state", conv_state), ("weight", weight), ("bias", bias),
+                     ("conv_state_indices", conv_state_indices), ("cache_seqlens", cache_seqlens),
+                     ("out", out), ("status", status)))
     ld = x.stride(0) if N > 1 else D  # a single row's stride is never used
     ss, sd, sl = conv_state.stride()
-    stream = torch.cuda.current_stream(x.device).cuda_stream
-    st = lib.ccu_conv1d_update_ex(
-        _ptr(x), ld, _ptr(conv_state), ss, sd, sl, _ptr(weight), _ptr(bias),
-        _ACTIVATIONS[activation], _ptr(conv_state_indices), _ptr(cache_seqlens), N, D, S, L, W, _ptr(out),
-        _ptr(status), ROUTES[route], stream)
+    with torch.cuda.device(x.device):  # the library launches on the current device
+        stream = torch.cuda.current_stream(x.device).cuda_stream
+        st = lib.ccu_conv1d_update_ex(
+            _ptr(x), ld, _ptr(conv_state), ss, sd, sl, _ptr(weight), _ptr(bias),
+            _ACTIVATIONS[activation], _ptr(conv_state_indices), _ptr(cache_seqlens), N, D, S, L, W,
+            _ptr(out), _ptr(status), ROUTES[route], stream)
     raise_for_status(st)
     return out
 
@@ -332,11 +344,15 @@ def _update_multi(x, conv_state, weight, bias, activation, cache_seqlens, conv_s
         _check_tensor("status", status, torch.int32, torch)
     if route not in ROUTES:
         raise ValueError(f"route must be one of {sorted(ROUTES)}")
-    stream = torch.cuda.current_stream(x.device).cuda_stream
-    st = lib.ccu_conv1d_update_multi(
-        _ptr(x), *x.stride(), _ptr(conv_state), *conv_state.stride(), _ptr(weight), _ptr(bias),
-        _ACTIVATIONS[activation], _ptr(conv_state_indices), _ptr(cache_seqlens), N, D, T, S, L, W,
-        _ptr(out), *out.stride(), _ptr(intermediate_states), _ptr(status), ROUTES[route], stream)
+    _same_device(x, (("conv_state", conv_state), ("weight", weight), ("bias", bias),
+                     ("conv_state_indices", conv_state_indices), ("cache_seqlens", cache_seqlens),
+                     ("out", out), ("intermediate_states", intermediate_states), ("status", status)))
+    with torch.cuda.device(x.device):  # the library launches on the current device
+        stream = torch.cuda.current_stream(x.device).cuda_stream
+        st = lib.ccu_conv1d_update_multi(
+            _ptr(x), *x.stride(), _ptr(conv_state), *conv_state.stride(), _ptr(weight), _ptr(bias),
+            _ACTIVATIONS[activation], _ptr(conv_state_indices), _ptr(cache_seqlens), N, D, T, S, L, W,
+            _ptr(out), *out.stride(), _ptr(intermediate_states), _ptr(status), ROUTES[route], stream)
     raise_for_status(st)
     return out
 
@@ -393,12 +409,16 @@ def causal_conv1d_fwd(x, weight, bias=None, activation=None, *, initial_states=N
             raise ValueError("out must be [B, D, T]")
     if route not in ROUTES:
         raise ValueError(f"route must be one of {sorted(ROUTES)}")
+    _same_device(x, (("weight", weight), ("bias", bias), ("initial_states", initial_states),
+                     ("final_states_out", fin), ("out", out)))
     ist = initial_states.stride() if initial_states is not None else (0, 0, 0)
     fst = fin.stride() if fin is not None else (0, 0, 0)
-    stream = torch.cuda.current_stream(x.device).cuda_stream
-    st = lib.ccu_causal_conv1d_fwd(
-        _ptr(x), *x.stride(), _ptr(weight), _ptr(bias), _ACTIVATIONS[activation], _ptr(initial_states),
-        *ist, B, D, T, L, W, _ptr(out), *out.stride(), _ptr(fin), *fst, ROUTES[route], stream)
+    with torch.cuda.device(x.device):  # the library launches on the current device
+        stream = torch.cuda.current_stream(x.device).cuda_stream
+        st = lib.ccu_causal_conv1d_fwd(
+            _ptr(x), *x.stride(), _ptr(weight), _ptr(bias), _ACTIVATIONS[activation],
+            _ptr(initial_states), *ist, B, D, T, L, W, _ptr(out), *out.stride(), _ptr(fin), *fst,
+            ROUTES[route], stream)
     raise_for_status(st)
     return (out, fin) if fin is not None else out
 
@@ -418,8 +438,10 @@ def check_indices(conv_state_indices, S: int, status=None, scratch=None):
     nbytes = ccu_conv1d_check_indices_scratch_bytes(S)
     if scratch is None:
         scratch = torch.empty((max(nbytes // 4, 1),), dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream(dev).cuda_stream
-    st = lib.ccu_conv1d_check_indices(_ptr(conv_state_indices), conv_state_indices.numel(), S,
-                                      _ptr(scratch), _ptr(status), stream)
+    _same_device(conv_state_indices, (("status", status), ("scratch", scratch)), "conv_state_indices")
+    with torch.cuda.device(dev):  # the library launches on the current device
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        st = lib.ccu_conv1d_check_indices(_ptr(conv_state_indices), conv_state_indices.numel(), S,
+                                          _ptr(scratch), _ptr(status), stream)
     raise_for_status(st)
     return status
