@@ -243,3 +243,23 @@ def test_every_kernel_waits_for_prior_grids_first():
                 f"{path.name}: kernel at offset {m.start()} does not wait for prior grids first"
             kernels += 1
     assert kernels >= 13
+
+
+def test_auto_route_thresholds(ccu):
+    """The AUTO route at the measured thresholds: compact batches take the bulk kernel from
+    2^20 (row, channel) elements; width 3 with a window-only state (L = 2) returns to the
+    vector kernel from 3 * 2^24; the channel-last state never takes the bulk kernel; a
+    one-entry state (L = 1) never does either."""
+    D = 16384
+    below, at = (1 << 20) // D - 1, (1 << 20) // D  # 63 and 64 rows
+    assert select(ccu, N=below, S=below, D=D) == (0, 2)
+    assert select(ccu, N=at, S=at, D=D) == (0, 4)
+    w3_below, w3_at = (3 << 24) // D - 1, (3 << 24) // D  # 3071 and 3072 rows
+    assert select(ccu, N=w3_below, S=w3_below, D=D, W=3, L=2) == (0, 4)
+    assert select(ccu, N=w3_at, S=w3_at, D=D, W=3, L=2) == (0, 2)
+    assert select(ccu, N=w3_at, S=w3_at, D=D, W=3, L=3) == (0, 4)  # L = 3 stays on bulk
+    cl = dict(stride_s=3 * D, stride_d=1, stride_l=D)
+    for n in (at, 1024, w3_below, 4096):
+        assert select(ccu, N=n, S=n, D=D, **cl) == (0, 2), n
+        assert select(ccu, N=n, S=n, D=D, cache_seqlens=0x700000, **cl) == (0, 2), n
+    assert select(ccu, N=4096, S=4096, D=D, W=2, L=1) == (0, 2)
