@@ -670,13 +670,18 @@ def _multi_inputs(case, seed):
 @pytest.mark.parametrize("layout", ["compact", "channel_last"])
 @pytest.mark.parametrize("ci", range(len(MULTI)))
 def test_multi_token(route, layout, ci):
+    case = MULTI[ci]
+    if route == "vector" and (case["D"] % 8 or case["L"] > 8 or case["x_layout"] != "tokens_major"):
+        pytest.skip("the vector kernel needs channel-contiguous 16-byte token rows and L <= 8")
+    _check_multi(case, route, layout, 300 + ci)
+
+
+def _check_multi(case, route, layout, seed):
+    """One multi-token call against the oracle: outputs, intermediate states, final state."""
     import depthwise_causal_conv1d_gb300 as ccu
 
-    case = MULTI[ci]
     N, D, T, L, S = case["N"], case["D"], case["T"], case["L"], case["S"]
-    if route == "vector" and (D % 8 or L > 8 or case["x_layout"] != "tokens_major"):
-        pytest.skip("the vector kernel needs channel-contiguous 16-byte token rows and L <= 8")
-    x_tok, weight, bias, state, idx, seq = _multi_inputs(case, 300 + ci)
+    x_tok, weight, bias, state, idx, seq = _multi_inputs(case, seed)
     # oracle on its own copies
     st_ref = state.copy() if layout == "compact" else synthetic.to_channel_last(state)
     strides = (D * L, L, 1) if layout == "compact" else (L * D, 1, D)
@@ -1248,3 +1253,19 @@ def test_prefill_offsets_past_int32(route):
     assert bf16_ulp_distance(head_y, want_head).max() <= 1
     assert bf16_ulp_distance(tail_y, want_tail).max() <= 1
     assert np.array_equal(got_fin, want_fin)
+
+
+# The vector multi-token kernel at the state lengths the cases above reach only on the
+# scalar route (L = 5 to 7 with D % 8 == 0), linear and ring, both layouts.
+MULTI_LONG = [
+    dict(N=5, D=264, T=4, L=5, S=7, ring=False, x_layout="tokens_major"),
+    dict(N=4, D=136, T=6, L=6, S=6, ring=True, x_layout="tokens_major"),
+    dict(N=6, D=520, T=3, L=7, S=9, ring=False, x_layout="tokens_major"),
+    dict(N=3, D=72, T=9, L=7, S=5, ring=True, x_layout="tokens_major"),
+]
+
+
+@pytest.mark.parametrize("layout", ["compact", "channel_last"])
+@pytest.mark.parametrize("ci", range(len(MULTI_LONG)))
+def test_multi_token_vector_long_states(layout, ci):
+    _check_multi(MULTI_LONG[ci], "vector", layout, 400 + ci)
