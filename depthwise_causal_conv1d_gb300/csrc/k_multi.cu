@@ -116,9 +116,8 @@ __device__ __forceinline__ void compact_to_planes(const uint32_t (&cw)[4 * L], u
 // cap keeps (without the cap the kernel takes 170 registers, one CTA per SM, and loses).
 // The SiLU runs on channel pairs (the arithmetic is not hidden here: 86.0 -> 84.1 us), at
 // 72 spilled bytes.
-template <int L, int ACT, int LAYOUT, bool RING>
-__global__ void __launch_bounds__(256, 2) k_multi_vector(UpdateParams p, MultiParams m) {
-  grid_dependency_boundary();
+template <int L, int ACT, int LAYOUT, bool RING, int ROWS>
+__device__ __forceinline__ void multi_vector_body(const UpdateParams &p, const MultiParams &m) {
   const int64_t groups = p.D >> 3;
   const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (g >= groups) return;
@@ -219,14 +218,37 @@ __global__ void __launch_bounds__(256, 2) k_multi_vector(UpdateParams p, MultiPa
     }
   };
   // Two rows' loads (state and the first four tokens) in flight before either is computed.
-  for (int64_t n = blockIdx.y; n < p.N; n += 2 * (int64_t)gridDim.y) {
-    const int64_t n2 = n + gridDim.y;
-    MRow a, b;
-    load_row(n, a);
-    if (n2 < p.N) load_row(n2, b);
-    process_row(a);
-    if (n2 < p.N) process_row(b);
+  if constexpr (ROWS == 2) {
+    for (int64_t n = blockIdx.y; n < p.N; n += 2 * (int64_t)gridDim.y) {
+      const int64_t n2 = n + gridDim.y;
+      MRow a, b;
+      load_row(n, a);
+      if (n2 < p.N) load_row(n2, b);
+      process_row(a);
+      if (n2 < p.N) process_row(b);
+    }
+  } else {
+    for (int64_t n = blockIdx.y; n < p.N; n += gridDim.y) {
+      MRow a;
+      load_row(n, a);
+      process_row(a);
+    }
   }
+}
+
+// Up to L = 6: two rows in flight under a 128-register cap (two CTAs per SM).
+template <int L, int ACT, int LAYOUT, bool RING>
+__global__ void __launch_bounds__(256, 2) k_multi_vector(UpdateParams p, MultiParams m) {
+  grid_dependency_boundary();
+  multi_vector_body<L, ACT, LAYOUT, RING, 2>(p, m);
+}
+
+// L = 7 and 8: one row in flight and the compiler's register budget (the two-row form
+// spills 300-600 bytes there under the cap).
+template <int L, int ACT, int LAYOUT, bool RING>
+__global__ void __launch_bounds__(256) k_multi_vector_long(UpdateParams p, MultiParams m) {
+  grid_dependency_boundary();
+  multi_vector_body<L, ACT, LAYOUT, RING, 1>(p, m);
 }
 
 template <int L, int ACT>
@@ -234,12 +256,21 @@ cudaError_t launch_vec_L(const UpdateParams &p, const MultiParams &m, dim3 grid,
                          cudaStream_t stream) {
   const bool ring = p.seqlens != nullptr;
   constexpr int kC = (int)Layout::Compact, kCL = (int)Layout::ChannelLast;
-  if (p.layout == kC) {
-    return ring ? launch_overlapped(k_multi_vector<L, ACT, kC, true>, grid, block, 0, stream, p, m)
-                : launch_overlapped(k_multi_vector<L, ACT, kC, false>, grid, block, 0, stream, p, m);
+  if constexpr (L >= 7) {
+    if (p.layout == kC) {
+      return ring ? launch_overlapped(k_multi_vector_long<L, ACT, kC, true>, grid, block, 0, stream, p, m)
+                  : launch_overlapped(k_multi_vector_long<L, ACT, kC, false>, grid, block, 0, stream, p, m);
+    }
+    return ring ? launch_overlapped(k_multi_vector_long<L, ACT, kCL, true>, grid, block, 0, stream, p, m)
+                : launch_overlapped(k_multi_vector_long<L, ACT, kCL, false>, grid, block, 0, stream, p, m);
+  } else {
+    if (p.layout == kC) {
+      return ring ? launch_overlapped(k_multi_vector<L, ACT, kC, true>, grid, block, 0, stream, p, m)
+                  : launch_overlapped(k_multi_vector<L, ACT, kC, false>, grid, block, 0, stream, p, m);
+    }
+    return ring ? launch_overlapped(k_multi_vector<L, ACT, kCL, true>, grid, block, 0, stream, p, m)
+                : launch_overlapped(k_multi_vector<L, ACT, kCL, false>, grid, block, 0, stream, p, m);
   }
-  return ring ? launch_overlapped(k_multi_vector<L, ACT, kCL, true>, grid, block, 0, stream, p, m)
-              : launch_overlapped(k_multi_vector<L, ACT, kCL, false>, grid, block, 0, stream, p, m);
 }
 
 template <int ACT>
