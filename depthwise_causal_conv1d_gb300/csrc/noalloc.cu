@@ -10,8 +10,12 @@
 //
 // The array is a file-scope __device__ variable: every GPU on which the library's device
 // code is loaded holds its 128 KB until the process exits. In host code its name is only
-// a host-side stand-in, so the device address is looked up with cudaGetSymbolAddress,
-// once per device, with that device current, and cached.
+// a host-side stand-in, so the device address is looked up with cudaGetSymbolAddress with
+// the device current. The lookup is repeated on every call whose stream is not being
+// captured: after a cudaDeviceReset (or a release of the primary context) the device code
+// is loaded again and the array may sit at another address. While a stream is being
+// captured the address found by the last uncaptured call on the device is used instead,
+// since the lookup may load device code, which a capture does not allow.
 #include <mutex>
 
 #include "ccu_conv1d.h"
@@ -34,19 +38,22 @@ ccu_status_t noalloc_fail(ccu_status_t st, const char *msg) {
   return st;
 }
 
-// The bitmap's device address on the current device (set up on first use per device).
-cudaError_t bitmap_on_current_device(uint32_t **out) {
+// The bitmap's device address on the current device: looked up again unless `capturing`,
+// in which case the address of the last uncaptured lookup on this device is returned
+// (cudaErrorStreamCaptureUnsupported if there was none).
+cudaError_t bitmap_on_current_device(bool capturing, uint32_t **out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (g_bitmap_addr[dev] == nullptr) {
+  if (!capturing) {
     void *addr = nullptr;
     e = cudaGetSymbolAddress(&addr, g_noalloc_bitmap);
     if (e != cudaSuccess) return e;
     g_bitmap_addr[dev] = static_cast<uint32_t *>(addr);
   }
+  if (g_bitmap_addr[dev] == nullptr) return cudaErrorStreamCaptureUnsupported;
   *out = g_bitmap_addr[dev];
   return cudaSuccess;
 }
@@ -69,11 +76,16 @@ ccu_status_t ccu_conv1d_check_indices_noalloc(const int32_t *indices, int64_t N,
   if (reinterpret_cast<uintptr_t>(indices) % 4 != 0 ||
       reinterpret_cast<uintptr_t>(status_dev) % 4 != 0)
     return noalloc_fail(CCU_ERR_INVALID_ARGUMENT, "indices and status_dev must be 4-byte aligned");
-  uint32_t *bitmap = nullptr;
-  cudaError_t e = bitmap_on_current_device(&bitmap);
-  if (e != cudaSuccess)
-    return noalloc_fail(CCU_ERR_CUDA, "could not resolve the built-in bitmap on this device");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &cap);
+  if (e != cudaSuccess) return noalloc_fail(CCU_ERR_CUDA, cudaGetErrorString(e));
+  uint32_t *bitmap = nullptr;
+  e = bitmap_on_current_device(cap != cudaStreamCaptureStatusNone, &bitmap);
+  if (e != cudaSuccess)
+    return noalloc_fail(CCU_ERR_CUDA,
+                        "could not resolve the built-in bitmap on this device (while a stream is "
+                        "captured, an earlier uncaptured call on the device is needed)");
   // The array keeps the previous call's bits: clear the words this call uses.
   const size_t bytes = (size_t)((S + 31) / 32) * sizeof(uint32_t);
   if (bytes > 0) e = cudaMemsetAsync(bitmap, 0, bytes, s);
