@@ -80,6 +80,19 @@ __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 
+// bulk_wait_read<N> for a run-time N in [0, kMaxStages - 2].
+__device__ __forceinline__ void bulk_wait_read_n(int n) {
+  switch (n) {
+    case 0: bulk_wait_read<0>(); break;
+    case 1: bulk_wait_read<1>(); break;
+    case 2: bulk_wait_read<2>(); break;
+    case 3: bulk_wait_read<3>(); break;
+    case 4: bulk_wait_read<4>(); break;
+    case 5: bulk_wait_read<5>(); break;
+    default: bulk_wait_read<6>(); break;
+  }
+}
+
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }

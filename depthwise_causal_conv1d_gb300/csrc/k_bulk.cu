@@ -19,6 +19,7 @@
 // block) and the conv_state_indices paragraph; compact state layout from its "Semantic
 // tensor contract".
 #include <atomic>
+#include <mutex>
 
 #include "ccu_bulk.cuh"
 
@@ -28,6 +29,14 @@ int device_sm_count();
 int current_device();
 
 __device__ int32_t g_async_error = 0;  // CCU_DEVERR_* bits raised by a kernel with no status word
+__device__ int32_t g_async_error_taken = 0;  // the value the last exchange read
+
+// Reads and clears the error word in one atomic step (a kernel that raises a bit
+// meanwhile leaves it for the next exchange).
+__global__ void k_exchange_async_error() {
+  grid_dependency_boundary();
+  g_async_error_taken = atomicExch(&g_async_error, 0);
+}
 
 namespace {
 
@@ -35,13 +44,20 @@ using namespace bulk;
 
 // Shared memory per warp: kBarrierBytes of mbarriers, then P stages of stage_bytes.
 // RING: conv_state is a ring buffer indexed by cache_seqlens (entry q replaced by x).
+// Two refill schedules, chosen by `ahead`:
+//   ahead == 0: the stage of slice k - 1 is refilled (with slice k - 1 + P) after slice k has
+//     been computed and stored; P slices are loaded before the loop.
+//   1 <= ahead <= P - 1: slice k + ahead is issued at the top of iteration k, before the wait
+//     on slice k, so a load is in flight while the warp waits and while it computes; ahead
+//     slices are loaded before the loop.
 template <int L, int W, int ACT, int G, bool RING>
-__global__ void __launch_bounds__(kThreads) k_update_bulk(UpdateParams p, int stages, int64_t stage_bytes) {
+__global__ void __launch_bounds__(kThreads) k_update_bulk(UpdateParams p, int stages, int ahead,
+                                                          int64_t stage_bytes) {
   grid_dependency_boundary();
   constexpr int64_t kSlice = 256 * G;
   extern __shared__ __align__(128) unsigned char smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int P = stages;
+  const int P = stages, A = ahead;
   unsigned char *wbase = smem + (int64_t)warp * (kBarrierBytes + P * stage_bytes);
   uint64_t *bars = reinterpret_cast<uint64_t *>(wbase);
   unsigned char *bufs = wbase + kBarrierBytes;
@@ -73,7 +89,8 @@ __global__ void __launch_bounds__(kThreads) k_update_bulk(UpdateParams p, int st
     }
   };
 
-  const int64_t prologue = mine < P ? mine : P;
+  const int64_t pre = A > 0 ? A : P;
+  const int64_t prologue = mine < pre ? mine : pre;
   if (lane == 0)
     for (int64_t k = 0; k < prologue; ++k) issue(k);
 
@@ -86,6 +103,12 @@ __global__ void __launch_bounds__(kThreads) k_update_bulk(UpdateParams p, int st
   for (; k < mine; ++k) {
     const int st = (int)(k % P);
     const uint32_t parity = (uint32_t)((k / P) & 1);
+    if (A > 0 && lane == 0 && k + A < mine) {
+      // Stage (k + A) % P last held slice k + A - P, whose stores were committed in iteration
+      // k + A - P: P - A - 1 groups before the newest. Wait until they have read it.
+      bulk_wait_read_n(P - A - 1);
+      issue(k + A);
+    }
     const Slice sl = slice_of<G, L>(p, first + k * stride, slices, false);
     unsigned char *buf = bufs + st * stage_bytes;
 
@@ -150,9 +173,9 @@ __global__ void __launch_bounds__(kThreads) k_update_bulk(UpdateParams p, int st
         bulk_store(p.state + sl.s * (p.D * L) + sl.c_base * L, buf + 2 * kSlice,
                    (uint32_t)(sl.cn * L * 2));
       }
-      bulk_commit();
+      bulk_commit();  // one group per iteration, empty for a padding slice
       // Refill the previous stage once its stores have read their shared memory.
-      if (k >= 1 && k - 1 + P < mine) {
+      if (A == 0 && k >= 1 && k - 1 + P < mine) {
         bulk_wait_read<1>();
         issue(k - 1 + P);
       }
@@ -161,9 +184,12 @@ __global__ void __launch_bounds__(kThreads) k_update_bulk(UpdateParams p, int st
   }
 
   if (failed && lane == 0) {
-    // Record the error, then let this warp's own loads land before shared memory goes away.
+    // Record the error, then let this warp's own loads land before shared memory goes away:
+    // slices k .. issued - 1 were issued and not consumed (ahead == 0: the P slices of the
+    // prologue and one refill per iteration from k = 1 on, so up to slice max(k, 1) + P - 2).
     atomicOr(p.status != nullptr ? p.status : &g_async_error, kDevErrTimeout);
-    const int64_t issued = (k - 1 + P < mine) ? k - 1 + P : mine;
+    const int64_t last = A > 0 ? k + A + 1 : (k > 0 ? k - 1 : 0) + P;
+    const int64_t issued = last < mine ? last : mine;
     for (int64_t q = k; q < issued; ++q) mbar_wait(&bars[q % P], (uint32_t)((q / P) & 1));
   }
   if (lane == 0) bulk_wait_all();  // stores complete before the warp retires
@@ -179,16 +205,24 @@ int64_t stage_bytes_for(int64_t L) {
   return (b + 127) / 128 * 128;
 }
 
+// Stage bytes a warp may hold (see launch_LAR).
+constexpr int64_t kWarpStageBudget = 8 * 1024;
+
 template <int L, int W, int ACT, bool RING>
 cudaError_t launch_LAR(const UpdateParams &p, cudaStream_t stream) {
   const int64_t sb = stage_bytes_for(L);
   // About 8 KB of stages per warp (two 4 KB stages at L = 3), 66 KB a CTA; the registers
   // (99 a thread at L = 3) keep 2 CTAs of 8 warps resident per SM. Measured on the large
   // batch: slices of 512 channels with two stages beat 256-channel slices with four (larger
-  // bulk copies); more in flight (three stages, or 3 CTAs per SM under a register cap) and
-  // less (one CTA per SM) were both slower at full size.
-  int P = (int)(8 * 1024 / sb);
+  // bulk copies); one CTA per SM was slower.
+  int P = (int)(kWarpStageBudget / sb);
   P = P < 2 ? 2 : (P > kMaxStages ? kMaxStages : P);
+  // Refill schedule, measured at N=4096, D=16384 (us, refilled after compute / issued one
+  // ahead): linear L = 3 160.2 / 168.8 (and 169.7 with two ahead at three stages), L = 4
+  // 199.6 / 213.7, L = 5 247.3 / 248.1, L = 6 289.2 / 288.2, L = 7 309.3 / 325.8, L = 8
+  // 656.7 / 570.4; the ring state at L = 3 166.9 / 161.5. At L = 8 a lane's state is 128
+  // bytes, so the lanes of a quarter-warp read and write the same shared-memory banks.
+  const int A = (RING || L == 8) ? 1 : 0;
   const size_t smem = (size_t)kWarps * (kBarrierBytes + (size_t)P * sb);
   const int dev = current_device();
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
@@ -213,7 +247,7 @@ cudaError_t launch_LAR(const UpdateParams &p, cudaStream_t stream) {
   int64_t grid = (warps + kWarps - 1) / kWarps;
   if (grid < 1) grid = 1;
   return launch_overlapped(k_update_bulk<L, W, ACT, kGroups, RING>, dim3((unsigned)grid), dim3(kThreads),
-                           smem, stream, p, P, sb);
+                           smem, stream, p, P, A, sb);
 }
 
 template <int L, int W, int ACT>
@@ -245,12 +279,21 @@ cudaError_t launch_A(const UpdateParams &p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t take_async_error(int32_t *bits) {
-  int32_t zero = 0, planes = 0, prefill = 0;
-  cudaError_t e = cudaMemcpyFromSymbol(bits, g_async_error, sizeof(int32_t));
-  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_async_error, &zero, sizeof(int32_t));
+  // One caller at a time, after every kernel issued so far has finished. Each word is read
+  // and cleared by one atomic exchange on the device, so a bit raised by a kernel that runs
+  // meanwhile (on a stream that does not synchronize with the legacy default stream) is
+  // kept for the next call rather than lost between a read and a clear.
+  static std::mutex serial;
+  std::lock_guard<std::mutex> lock(serial);
+  int32_t mine = 0, planes = 0, prefill = 0;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) {
+    e = launch_overlapped(k_exchange_async_error, dim3(1), dim3(1), 0, (cudaStream_t)0);
+  }
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&mine, g_async_error_taken, sizeof(int32_t));
   if (e == cudaSuccess) e = take_planes_error(&planes);
   if (e == cudaSuccess) e = take_prefill_error(&prefill);
-  if (e == cudaSuccess) *bits |= planes | prefill;
+  if (e == cudaSuccess) *bits = mine | planes | prefill;
   return e;
 }
 

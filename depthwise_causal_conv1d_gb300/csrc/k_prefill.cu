@@ -273,6 +273,14 @@ __global__ void __launch_bounds__(256) k_prefill_vector(UpdateParams p, PrefillP
 // CCU_DEVERR_TIMEOUT, waits (bounded) for its own copies and returns.
 
 __device__ int32_t g_prefill_error = 0;  // CCU_DEVERR_* bits raised by the bulk prefill
+__device__ int32_t g_prefill_error_taken = 0;  // the value the last exchange read
+
+// Reads and clears the error word in one atomic step (a kernel that raises a bit
+// meanwhile leaves it for the next exchange).
+__global__ void k_exchange_prefill_error() {
+  grid_dependency_boundary();
+  g_prefill_error_taken = atomicExch(&g_prefill_error, 0);
+}
 
 constexpr int kPThreads = 384;                 // 12 warps per CTA, up to 170 registers each
 constexpr int kPWarps = kPThreads / 32;
@@ -520,9 +528,10 @@ cudaError_t launch_prefill_bulk(const UpdateParams &p, const PrefillParams &f, i
 }
 
 cudaError_t take_prefill_error(int32_t *bits) {
-  int32_t zero = 0;
-  cudaError_t e = cudaMemcpyFromSymbol(bits, g_prefill_error, sizeof(int32_t));
-  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_prefill_error, &zero, sizeof(int32_t));
+  // read and clear in one atomic step on the device (the legacy default stream orders
+  // the copy after the exchange)
+  cudaError_t e = launch_overlapped(k_exchange_prefill_error, dim3(1), dim3(1), 0, (cudaStream_t)0);
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(bits, g_prefill_error_taken, sizeof(int32_t));
   return e;
 }
 

@@ -326,9 +326,12 @@ CCU_API ccu_status_t ccu_conv1d_check_indices(const int32_t *indices, int64_t N,
  *   status_dev  device int32 word; CCU_DEVERR_RANGE / CCU_DEVERR_DUPLICATE are ORed in,
  *               never cleared.
  *
- * The first call on each device looks up the array's device address (a runtime symbol
- * lookup, which can load the library's device code onto that device) and caches it; make
- * that first call on a device before any stream capture on it. All calls in the process
+ * Each call whose stream is not being captured looks up the array's device address (a
+ * runtime symbol lookup, which can load the library's device code onto that device), so
+ * the address stays right after a cudaDeviceReset. A call on a stream that is being
+ * captured cannot do that lookup and uses the address of the last uncaptured call on the
+ * same device: make the first call on a device, and the first after a reset of it, outside
+ * any stream capture (otherwise the call fails with CCU_ERR_CUDA). All calls in the process
  * share the one array per device, and it keeps the previous call's contents until the
  * next call clears it: calls that overlap on the GPU (on different streams, or from
  * different threads without ordering) race on it and can report false duplicates or miss
@@ -349,7 +352,10 @@ CCU_API int64_t ccu_conv1d_check_indices_scratch_bytes(int64_t S);
  * of the prefill) never wait without
  * limit; if a wait gives up they OR CCU_DEVERR_TIMEOUT into the caller's status word when
  * there is one (checked entry points), and otherwise into this per-process, per-device
- * word. This call SYNCHRONIZES the current device (it copies the word to the host).
+ * word. This call SYNCHRONIZES the current device (it waits for all work issued so far,
+ * then reads and clears the word in one atomic step and copies it to the host; a bit
+ * raised by a kernel issued later is kept for the next call). Calls from several host
+ * threads are serialized.
  *
  *   bits  host int32 out-parameter: the CCU_DEVERR_* bits raised since the last call.
  */
