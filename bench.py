@@ -50,9 +50,15 @@ except (OSError, KeyError, ValueError):
     PEAK_GBPS = 6800.0  # fallback figure when the measured peaks are absent
 UNIT = "GB/s"
 L2_BYTES = 129 * 1024 * 1024
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "update_bulk_large_n4096_d16384.txt")
-KERNEL_SOURCES = [os.path.join(ROOT, "depthwise_causal_conv1d_gb300", "csrc", f)
-                  for f in ("k_bulk.cu", "ccu_bulk.cuh", "ccu_internal.cuh")]
+_CSRC = os.path.join(ROOT, "depthwise_causal_conv1d_gb300", "csrc")
+# Per kernel family: the committed ncu summary of its DRAM traffic on the large-batch
+# workload, and the sources whose hash that capture was taken with.
+PROFILE_SUMMARIES = {
+    "vector": (os.path.join(ROOT, "profiles", "update_vector_large_n4096_d16384.txt"),
+               [os.path.join(_CSRC, f) for f in ("k_vector.cu", "ccu_internal.cuh")]),
+    "bulk": (os.path.join(ROOT, "profiles", "update_bulk_large_n4096_d16384.txt"),
+             [os.path.join(_CSRC, f) for f in ("k_bulk.cu", "ccu_bulk.cuh", "ccu_internal.cuh")]),
+}
 
 
 ALL_DECODE_WORKLOADS = {**synthetic.WORKLOADS, **synthetic.RING_WORKLOADS, **synthetic.WIDTH_WORKLOADS}
@@ -223,31 +229,33 @@ def gpu_id_for(dev_index: int) -> str:
 
 # --------------------------------------------------------------------------- profile summary
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(route_name="vector") -> str:
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
+    for p in PROFILE_SUMMARIES[route_name][1]:
         with open(p, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(full_units: int, wl=None, route_name="bulk"):
-    """DRAM bytes per launch from the committed ncu summary, scaled to this launch's
-    (row, channel) units; None if the kernel source changed since the capture, or if this
-    run is not the captured kernel on the captured workload's kind of input."""
+def ncu_traffic(full_units: int, wl=None, route_name="vector"):
+    """DRAM bytes per launch from the committed ncu summary of this kernel family, scaled to
+    this launch's (row, channel) units; None if the kernel source changed since the capture,
+    or if this run is not the captured kernel on the captured workload's kind of input."""
+    if route_name not in PROFILE_SUMMARIES:
+        return None, "no ncu capture for this route"
     if wl is not None:
         base = synthetic.WORKLOADS[synthetic.BENCH_WORKLOAD]
         same_kind = (wl.D, wl.L, wl.W, wl.act, wl.layout, wl.ring) == (base.D, base.L, base.W, base.act,
                                                                     base.layout, base.ring)
-        if not same_kind or route_name != "bulk":
-            return None, "no ncu capture for this workload and route"
+        if not same_kind:
+            return None, "no ncu capture for this workload"
     try:
-        text = open(PROFILE_SUMMARY).read()
+        text = open(PROFILE_SUMMARIES[route_name][0]).read()
     except OSError:
         return None, "no ncu summary"
     kv = dict(ln.split("=", 1) for ln in text.splitlines() if "=" in ln and not ln.startswith("#"))
     try:
-        if kv.get("kernel_source_sha256_16") != kernel_source_hash():
+        if kv.get("kernel_source_sha256_16") != kernel_source_hash(route_name):
             return None, "kernel changed since the ncu capture"
         traffic = float(kv["dram_bytes_per_launch"])
         units = float(kv["units_per_launch"])
@@ -284,6 +292,7 @@ class Resident:
         self.w = to_dev(inp.weight, dev)
         self.b = to_dev(inp.bias, dev) if inp.bias is not None else None
         self.idx = torch.from_numpy(inp.indices).to(dev) if inp.indices is not None else None
+        self.idx_host = inp.indices
         self.seq = (torch.from_numpy(inp.cache_seqlens).to(dev) if inp.cache_seqlens is not None
                     else None)
         self.out = torch.empty((wl.N, wl.D), dtype=torch.bfloat16, device=dev)
@@ -305,6 +314,20 @@ class Resident:
         st = self.ccu.lib.ccu_conv1d_update_ex(*self.args)
         if st != 0:
             self.ccu.raise_for_status(st)
+
+    def rotating_args(self, k):
+        """Argument tuples of k calls, each on its own device copies of x, conv_state and out
+        (weights, bias, indices and cache_seqlens are shared: they are read, not written)."""
+        import torch
+
+        self.copies = [(self.x_full.clone(), self.state.clone(), torch.empty_like(self.out)) for _ in range(k)]
+        torch.cuda.synchronize()  # the copies are made on the current stream; the calls run on another
+        out = []
+        for xf, st, o in self.copies:
+            a = list(self.args)
+            a[0], a[2], a[16] = xf.data_ptr(), st.data_ptr(), o.data_ptr()
+            out.append(tuple(a))
+        return out
 
 
 def time_device_resident(res: Resident, steps: int, warmup: int, world: int, dev):
@@ -492,15 +515,47 @@ def time_e2e_zero_copy(res: Resident, inp, steps: int, warmup: int, world: int, 
     return total, bytes_in, bytes_out
 
 
-def per_workload_table(dev, stream, reps=50):
-    """µs per call for every workload: eager (warm), CUDA-graph replay, and cold L2.
-
-    cold: a 2x-L2 buffer is written before each call (L2 left full of dirty lines, which
-    the call then also writes back); cold_clean: the buffer is read instead.
-    """
+def cold_rotating_us(res, stream, passes=3):
+    """µs per call with nothing of the call's own data in L2: K back-to-back calls, each on its
+    own copies of x, conv_state and out, the K copies together at least 3x the L2 (each
+    copy was last touched K - 1 calls earlier); two CUDA events around each pass of K
+    calls, the median pass divided by K. One call between two events cannot resolve a few
+    microseconds (the events tick in ~2 µs steps on this GPU)."""
     import torch
 
-    flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
+    wl = res.wl
+    touched = synthetic.algorithmic_bytes(wl, res.idx_host)
+    k = max(4, -(-3 * L2_BYTES // max(touched, 1)))
+    args = res.rotating_args(k)
+    lib = res.ccu.lib
+
+    def one_pass():
+        for a in args:
+            st = lib.ccu_conv1d_update_ex(*a)
+            if st != 0:
+                res.ccu.raise_for_status(st)
+
+    one_pass()
+    torch.cuda.synchronize()
+    per = []
+    for _ in range(passes):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        one_pass()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        per.append(e0.elapsed_time(e1) * 1e3 / k)
+    res.copies = None
+    return statistics.median(per), k
+
+
+def per_workload_table(dev, stream, reps=50):
+    """µs per call for every decode workload: eager (back to back on the same buffers, so a
+    workload smaller than L2 is served from it), CUDA-graph replay, and cold (back-to-back
+    calls on rotating copies larger than L2 together, see cold_rotating_us). The roofline
+    fraction of a workload that fits in L2 comes from its cold time."""
+    import torch
+
     rows = {}
     for name, wl in {**synthetic.WORKLOADS, **synthetic.RING_WORKLOADS,
                      **synthetic.WIDTH_WORKLOADS}.items():
@@ -518,31 +573,7 @@ def per_workload_table(dev, stream, reps=50):
         b.record(stream)
         torch.cuda.synchronize()
         eager_us = a.elapsed_time(b) * 1e3 / reps
-        # cold: flush L2 before every call, time the call alone
-        cold = []
-        for _ in range(reps):
-            with torch.cuda.stream(stream):
-                flush.fill_(1)
-            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            c0.record(stream)
-            res.call()
-            c1.record(stream)
-            cold.append((c0, c1))
-        torch.cuda.synchronize()
-        cold_us = statistics.median(c0.elapsed_time(c1) * 1e3 for c0, c1 in cold)
-        # clean cold: L2 filled by reading a buffer twice its size, so the call does not also
-        # pay for writing back the flush's dirty lines
-        clean = []
-        for _ in range(reps):
-            with torch.cuda.stream(stream):
-                flush.sum()
-            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            c0.record(stream)
-            res.call()
-            c1.record(stream)
-            clean.append((c0, c1))
-        torch.cuda.synchronize()
-        clean_us = statistics.median(c0.elapsed_time(c1) * 1e3 for c0, c1 in clean)
+        cold_us, k = cold_rotating_us(res, stream)
         # CUDA graph: 100 calls captured, replayed 20 times
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
@@ -561,21 +592,20 @@ def per_workload_table(dev, stream, reps=50):
         rows[name] = {"N_x_D": wl.N * wl.D, "bytes": nbytes, "route": res.route_name,
                       "state": f"{'ring' if wl.ring else 'linear'} {wl.layout}", "W": wl.W, "L": wl.L,
                       "eager_us": round(eager_us, 3), "graph_us": round(graph_us, 3),
-                      "cold_us": round(cold_us, 3), "cold_clean_us": round(clean_us, 3),
+                      "cold_us": round(cold_us, 3), "cold_copies": k,
                       "cold_GBps": round(nbytes / (cold_us * 1e-6) / 1e9, 1),
+                      "cold_frac": round(nbytes / (cold_us * 1e-6) / 1e9 / PEAK_GBPS, 4),
                       "warm_frac": round(nbytes / (eager_us * 1e-6) / 1e9 / PEAK_GBPS, 4)}
         del g, res
-    del flush
     return rows
 
 
 def n_curve(dev, stream, reps=100):
     """µs per call against N·D: the large-batch decode settings (D=16384, L=3, SiLU, bias,
     permuted slots with 5% padding) at N = 1, 8, 64, 256, 1024, 4096, route AUTO; warm
-    (back to back) and clean cold (a 2x-L2 buffer read before each call)."""
+    (back to back on the same buffers) and cold (rotating copies, see cold_rotating_us)."""
     import torch
 
-    flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.int32, device=dev)
     base = synthetic.WORKLOADS[synthetic.BENCH_WORKLOAD]
     rows = {}
     for n in (1, 8, 64, 256, 1024, 4096):
@@ -594,23 +624,56 @@ def n_curve(dev, stream, reps=100):
         b.record(stream)
         torch.cuda.synchronize()
         warm_us = a.elapsed_time(b) * 1e3 / k
-        clean = []
-        for _ in range(30):
-            with torch.cuda.stream(stream):
-                flush.sum()
-            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            c0.record(stream)
-            res.call()
-            c1.record(stream)
-            clean.append((c0, c1))
-        torch.cuda.synchronize()
-        cold_us = statistics.median(c0.elapsed_time(c1) * 1e3 for c0, c1 in clean)
+        cold_us, copies = cold_rotating_us(res, stream)
         rows[f"N={n}"] = {"N_x_D": wl.N * wl.D, "bytes": nbytes, "route": res.route_name,
-                          "warm_us": round(warm_us, 3), "cold_clean_us": round(cold_us, 3),
+                          "warm_us": round(warm_us, 3), "cold_us": round(cold_us, 3), "cold_copies": copies,
                           "cold_GBps": round(nbytes / (cold_us * 1e-6) / 1e9, 1),
                           "cold_frac": round(nbytes / (cold_us * 1e-6) / 1e9 / PEAK_GBPS, 4)}
         del res
-    del flush
+    return rows
+
+
+def checked_cost_rows(dev, stream, reps=100):
+    """µs per call, back to back, of the update unchecked, range-checked
+    (ccu_conv1d_update_checked) and range- and duplicate-checked in the same launch
+    (ccu_conv1d_update_checked_ex with its slot scratch cleared by the call), on the paged
+    (N=256, D=8192, S=1024) and the large-batch workloads, AUTO route."""
+    import torch
+
+    rows = {}
+    for name in ("paged_n256_d8192_l3_s1024_pad10_silu", synthetic.BENCH_WORKLOAD):
+        wl = synthetic.WORKLOADS[name]
+        inp = synthetic.generate(wl)
+        res = Resident(inp, dev, stream)
+        lib = res.ccu.lib
+        status = torch.zeros((1,), dtype=torch.int32, device=dev)
+        scratch = torch.zeros((wl.S,), dtype=torch.int32, device=dev)
+        a = list(res.args)
+        a[18] = 0  # AUTO
+        plain = tuple(a)
+        a[17] = status.data_ptr()
+        checked = tuple(a)
+        ex = tuple(a[:18]) + (scratch.data_ptr(),) + tuple(a[18:])
+        calls = {"unchecked": lambda: lib.ccu_conv1d_update_ex(*plain),
+                 "range_checked": lambda: lib.ccu_conv1d_update_ex(*checked),
+                 "range_and_duplicate_checked": lambda: lib.ccu_conv1d_update_checked_ex(*ex)}
+        row = {"N_x_D": wl.N * wl.D, "route": res.route_name}
+        for label, fn in calls.items():
+            for _ in range(5):
+                st = fn()
+                if st != 0:
+                    res.ccu.raise_for_status(st)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            row[f"{label}_us"] = round(e0.elapsed_time(e1) * 1e3 / reps, 3)
+        row["status"] = int(status.item())
+        rows[name] = row
+        del res
     return rows
 
 
@@ -835,6 +898,7 @@ def run_ours(args):
             line["n_curve"] = n_curve(dev, stream)
             line["multi_token"] = multi_token_rows(dev, stream)
             line["prefill"] = prefill_rows(dev, stream)
+            line["checked_cost"] = checked_cost_rows(dev, stream)
         if rank == 0:
             line["cpu_baseline"] = cpu_baseline_sample(inp, args.cpu_seconds)
     if rank == 0:
@@ -891,9 +955,10 @@ def run_reference(args):
         "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; the pages publish no dataset)",
-        "config": config_of(wl, {"rows_per_step": rows}),
+        "config": config_of(wl),
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": f"first {rows} of {wl.N} rows per step (all {wl.D} channels)",
+                         "rows_per_step": rows,
                          "cores_available": os.cpu_count(), "cpu_model": cpu_model()},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,

@@ -58,6 +58,9 @@ def _load() -> ctypes.CDLL:
     lib.ccu_conv1d_update.argtypes = upd + [vp]
     lib.ccu_conv1d_update_checked.argtypes = upd + [vp, vp]
     lib.ccu_conv1d_update_ex.argtypes = upd + [vp, i32, vp]
+    lib.ccu_conv1d_update_checked_ex.argtypes = upd + [vp, vp, i32, vp]
+    lib.ccu_conv1d_slot_scratch_bytes.argtypes = [i64]
+    lib.ccu_conv1d_slot_scratch_bytes.restype = i64
     lib.ccu_conv1d_select_route.argtypes = upd + [i32, ctypes.POINTER(i32)]
     lib.ccu_conv1d_update_multi.argtypes = [vp, i64, i64, i64, vp, i64, i64, i64, vp, vp, ctypes.c_int,
                                             vp, vp, i64, i64, i64, i64, i64, i64, vp, i64, i64, i64,
@@ -68,7 +71,7 @@ def _load() -> ctypes.CDLL:
                                           i32, vp]
     lib.ccu_causal_conv1d_fwd.restype = ctypes.c_int
     for f in ("ccu_conv1d_update", "ccu_conv1d_update_checked", "ccu_conv1d_update_ex",
-              "ccu_conv1d_select_route", "ccu_conv1d_check_indices"):
+              "ccu_conv1d_update_checked_ex", "ccu_conv1d_select_route", "ccu_conv1d_check_indices"):
         getattr(lib, f).restype = ctypes.c_int
     lib.ccu_conv1d_check_indices.argtypes = [vp, i64, i64, vp, vp, vp]
     lib.ccu_conv1d_check_indices_noalloc.argtypes = [vp, i64, i64, vp, vp]
@@ -111,6 +114,18 @@ def ccu_conv1d_update_ex(x, ld, conv_state, stride_s, stride_d, stride_l, weight
     return lib.ccu_conv1d_update_ex(x, ld, conv_state, stride_s, stride_d, stride_l, weight, bias,
                                     act, indices, cache_seqlens, N, D, S, L, W, out, status_dev,
                                     route, stream)
+
+
+def ccu_conv1d_update_checked_ex(x, ld, conv_state, stride_s, stride_d, stride_l, weight, bias, act,
+                                 indices, cache_seqlens, N, D, S, L, W, out, status_dev, slot_scratch,
+                                 route, stream) -> int:
+    return lib.ccu_conv1d_update_checked_ex(x, ld, conv_state, stride_s, stride_d, stride_l, weight,
+                                            bias, act, indices, cache_seqlens, N, D, S, L, W, out,
+                                            status_dev, slot_scratch, route, stream)
+
+
+def ccu_conv1d_slot_scratch_bytes(S) -> int:
+    return lib.ccu_conv1d_slot_scratch_bytes(S)
 
 
 def ccu_conv1d_update_multi(x, x_stride_n, x_stride_d, x_stride_t, conv_state, stride_s, stride_d,
@@ -227,7 +242,7 @@ def _same_device(ref, named, ref_name="x"):
 
 def causal_conv1d_update(x, conv_state, weight, bias=None, activation=None, *, cache_seqlens=None,
                          conv_state_indices=None, out=None, route: str = "auto", status=None,
-                         intermediate_states=None):
+                         intermediate_states=None, slot_scratch=None):
     """One decode step: mutate ``conv_state`` in place and return the BF16 output ``[N, D]``.
 
     Follows the cuDNN page "Causal Conv1d Decode Update" ("Python API" and "Semantic
@@ -237,8 +252,10 @@ def causal_conv1d_update(x, conv_state, weight, bias=None, activation=None, *, c
     ``conv_state_indices`` int32 ``[N]`` (``-1`` = padding row) or None; ``cache_seqlens``
     None (linear state) or int32 ``[N]``: the state is then a ring buffer whose oldest entry
     is at ``cache_seqlens[n] % L`` and only that entry is overwritten. ``out`` (optional, preallocated ``[N, D]`` BF16), ``route`` (kernel
-    family) and ``status`` (int32 device word: turns on the device range check) are
-    extensions of this binding. Runs on the current CUDA stream.
+    family), ``status`` (int32 device word: turns on the device range check) and
+    ``slot_scratch`` (int32 ``[S]`` device tensor, with ``status``: also detects repeated
+    slots in the same launch, see ccu_conv1d_update_checked_ex) are extensions of this
+    binding. Runs on the current CUDA stream.
 
     A 3-D ``x`` ``[N, D, T]`` (any strides) is the multi-token update: T tokens per row,
     output ``[N, D, T]`` laid out like ``x``; ``intermediate_states`` (optional BF16
@@ -250,6 +267,8 @@ def causal_conv1d_update(x, conv_state, weight, bias=None, activation=None, *, c
         raise ValueError(f"activation must be one of None, 'identity', 'silu', 'swish'; got {activation!r}")
     _check_tensor("x", x, torch.bfloat16, torch)
     if x.dim() == 3:
+        if slot_scratch is not None:
+            raise ValueError("slot_scratch serves the single-token update")
         return _update_multi(x, conv_state, weight, bias, activation, cache_seqlens,
                              conv_state_indices, out, route, status, intermediate_states, torch)
     if x.dim() != 2:
@@ -291,17 +310,29 @@ def causal_conv1d_update(x, conv_state, weight, bias=None, activation=None, *, c
         raise ValueError(f"route must be one of {sorted(ROUTES)}")
     if status is not None:
         _check_tensor("status", status, torch.int32, torch)
+    if slot_scratch is not None:
+        if status is None:
+            raise ValueError("slot_scratch needs a status word")
+        _check_tensor("slot_scratch", slot_scratch, torch.int32, torch)
+        if slot_scratch.numel() < S or not slot_scratch.is_contiguous():
+            raise ValueError("slot_scratch must be a contiguous int32 tensor of at least S elements")
     _same_device(x, (("conv_state", conv_state), ("weight", weight), ("bias", bias),
                      ("conv_state_indices", conv_state_indices), ("cache_seqlens", cache_seqlens),
-                     ("out", out), ("status", status)))
+                     ("out", out), ("status", status), ("slot_scratch", slot_scratch)))
     ld = x.stride(0) if N > 1 else D  # a single row's stride is never used
     ss, sd, sl = conv_state.stride()
     with torch.cuda.device(x.device):  # the library launches on the current device
         stream = torch.cuda.current_stream(x.device).cuda_stream
-        st = lib.ccu_conv1d_update_ex(
-            _ptr(x), ld, _ptr(conv_state), ss, sd, sl, _ptr(weight), _ptr(bias),
-            _ACTIVATIONS[activation], _ptr(conv_state_indices), _ptr(cache_seqlens), N, D, S, L, W,
-            _ptr(out), _ptr(status), ROUTES[route], stream)
+        if slot_scratch is not None:
+            st = lib.ccu_conv1d_update_checked_ex(
+                _ptr(x), ld, _ptr(conv_state), ss, sd, sl, _ptr(weight), _ptr(bias),
+                _ACTIVATIONS[activation], _ptr(conv_state_indices), _ptr(cache_seqlens), N, D, S, L, W,
+                _ptr(out), _ptr(status), _ptr(slot_scratch), ROUTES[route], stream)
+        else:
+            st = lib.ccu_conv1d_update_ex(
+                _ptr(x), ld, _ptr(conv_state), ss, sd, sl, _ptr(weight), _ptr(bias),
+                _ACTIVATIONS[activation], _ptr(conv_state_indices), _ptr(cache_seqlens), N, D, S, L, W,
+                _ptr(out), _ptr(status), ROUTES[route], stream)
     raise_for_status(st)
     return out
 

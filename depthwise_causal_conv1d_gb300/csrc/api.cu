@@ -50,6 +50,7 @@ struct Args {
   int64_t N, D, S, L, W;
   const void *out;
   const int32_t *status;
+  int32_t *owner = nullptr;  // slot-owner scratch [S]: the duplicate check (checked mode only)
 };
 
 // Every check of the contract. On CCU_OK, *noop says whether there is nothing to launch
@@ -70,6 +71,14 @@ ccu_status_t validate(const Args &a, bool *noop, Layout *layout) {
                 (long long)a.W);
   if (a.status != nullptr && !aligned(a.status, 4))
     return fail(CCU_ERR_INVALID_ARGUMENT, "status word must be 4-byte aligned");
+  if (a.owner != nullptr) {
+    if (a.status == nullptr)
+      return fail(CCU_ERR_INVALID_ARGUMENT, "the duplicate check needs a status word");
+    if (!aligned(a.owner, 4))
+      return fail(CCU_ERR_INVALID_ARGUMENT, "slot_scratch must be 4-byte aligned");
+    if (a.N >= INT32_MAX)
+      return fail(CCU_ERR_NOT_IMPLEMENTED, "the duplicate check serves N < 2^31 - 1 rows");
+  }
   if (a.N == 0 || a.D == 0) {
     *noop = true;  // nothing to read or write, whatever the strides
     return CCU_OK;
@@ -134,27 +143,34 @@ bool route_serves(int route, const Args &a, Layout layout) {
 // 27.5 us at 512).
 constexpr int64_t kBulkMinElements = 1 << 20;
 constexpr int64_t kWindowOnlyW3VectorElements = int64_t(3) << 24;
+// Above this many elements the lean vector kernel leads at L = 3, 5 and 6.
+constexpr int64_t kLeanVectorElements = int64_t(1) << 23;
 
 ccu_status_t choose(int requested, const Args &a, Layout layout, int *chosen) {
   if (requested < 0 || requested >= CCU_ROUTE_COUNT)
     return fail(CCU_ERR_INVALID_ARGUMENT, "unknown route %d", requested);
   if (requested == CCU_ROUTE_AUTO) {
-    // Compact batches from 2^20 elements take the bulk kernel, with two exceptions measured
-    // on the large batch (D = 16384, back to back). A one-entry state (L = 1) moves 8 bytes
-    // per element, too little per 512-channel slice for the bulk pipeline (W = 2: 100.8 us
-    // bulk, 80.7 us vector). Width 3 with L = 2 (a state of just the window) is the one
-    // compact case where the vector kernel, at three CTAs per SM, passes the bulk kernel on
-    // the full batch (4096 rows: 119.0 vs 126.1 us; 1024 rows: 41.0 vs 36.8 us), so it stays
-    // on the vector kernel from 3 * 2^24 elements.
-    // The channel-last state stays on the vector kernel at every size. Ring: with four rows
-    // in flight per thread it leads the bulk kernel from 128 to 4096 rows (1024 rows: 37.0 vs
-    // 42.1 us; 4096 rows: 125.5 vs 156.9 us). Linear: at four to eight rows per CTA it leads
-    // the plane-bulk kernel from 64 to 2048 rows (1024 rows: 45.3 vs 47.2 us) and at 4096 rows
-    // (159.9 vs 164.7 us), and trails it by 1.5 % at 3072 rows.
+    // The bulk kernel serves the linear compact state from 2^20 elements where it measured
+    // ahead of the vector kernel (D = 16384, back to back, us, bulk / vector):
+    //  - L = 3 up to 2^23 elements (N = 384: 16.2 / 17.5, N = 512: 19.9 / 20.6; but N = 256:
+    //    12.6 / 12.0), beyond it the vector kernel (N = 640: 27.0 / 25.7, N = 1024: 45.3 / 42.7,
+    //    N = 4096: 160.1 / 155.5); L = 5 and 6 likewise (N = 4096: 247.3 / 237.8 and 289.2 /
+    //    286.7);
+    //  - L = 4 and L = 7 at every size (N = 4096: 199.6 / 201.0 and 310.2 / 362.9);
+    //  - not L = 8 (N = 4096: 570.4 / 530.7; a lane's 128-byte state makes the bulk kernel's
+    //    shared-memory accesses bank-conflicted), nor L = 1, which moves 8 bytes per element,
+    //    too little per 512-channel slice (W = 2: 100.8 / 80.7);
+    //  - width 3 with L = 2 (a state of just the window) below 3 * 2^24 elements (4096 rows:
+    //    119.0 / 116.5 vector; 1024 rows: 36.8 bulk / 41.0).
+    // The ring state stays on the vector kernel at every size (compact, N = 4096: 161.5 /
+    // 158.6; N = 1024: 45.3 / 43.7; N = 256: 13.8 / 13.3), and so does the channel-last state
+    // (linear: N = 4096, 162.3 plane-bulk / 154.3; ring: the vector kernel leads from 128 rows).
     const int64_t elements = a.N * a.D;
+    const bool ring = a.cache_seqlens != nullptr;
     const bool window_only_w3 = a.W == 3 && a.L == 2 && elements >= kWindowOnlyW3VectorElements;
-    const bool bulk_size =
-        layout == Layout::Compact && elements >= kBulkMinElements && a.L >= 2 && !window_only_w3;
+    const bool lean_leads = (a.L == 3 || a.L == 5 || a.L == 6) && elements > kLeanVectorElements;
+    const bool bulk_size = layout == Layout::Compact && !ring && elements >= kBulkMinElements && a.L >= 2 &&
+                           a.L != 8 && !window_only_w3 && !lean_leads;
     if (bulk_size && route_serves(CCU_ROUTE_BULK, a, layout)) {
       *chosen = CCU_ROUTE_BULK;
     } else if (route_serves(CCU_ROUTE_VECTOR, a, layout)) {
@@ -211,6 +227,8 @@ ccu_status_t run(const Args &a, int route, cudaStream_t stream) {
   p.seqlens = a.cache_seqlens;
   p.out = static_cast<uint16_t *>(const_cast<void *>(a.out));
   p.status = const_cast<int32_t *>(a.status);
+  // Without indices row n uses slot n: no two rows can share a slot.
+  p.owner = a.idx != nullptr ? a.owner : nullptr;
   p.N = a.N;
   p.D = a.D;
   p.S = a.S;
@@ -222,7 +240,11 @@ ccu_status_t run(const Args &a, int route, cudaStream_t stream) {
   p.layout = (int)layout;
   p.rows_per_cta = 1;
 
-  cudaError_t e = cudaErrorInvalidValue;
+  cudaError_t e = cudaSuccess;
+  if (p.owner != nullptr && a.S > 0) e = cudaMemsetAsync(p.owner, 0, (size_t)a.S * sizeof(int32_t), stream);
+  if (e != cudaSuccess)
+    return fail(CCU_ERR_CUDA, "clearing slot_scratch failed: %s", cudaGetErrorString(e));
+  e = cudaErrorInvalidValue;
   switch (chosen) {
     case CCU_ROUTE_SCALAR: e = launch_scalar(p, a.act, stream); break;
     case CCU_ROUTE_VECTOR: e = launch_vector(p, a.act, stream); break;
@@ -299,9 +321,13 @@ ccu_status_t validate_multi(const MultiArgs &m, bool *noop, Layout *layout) {
 }
 
 // The vector multi-token kernel moves 8 channels of one token as one 16-byte vector.
+constexpr int64_t kMultiNarrowMaxL = 4;
+
 bool multi_vector_serves(const MultiArgs &m) {
   const Args &a = m.a;
-  return a.D % 8 == 0 && a.L <= kVectorMaxL && a.W == kW && m.sxd == 1 && m.sod == 1 &&
+  // width 4 up to L = 8; widths 2 and 3 up to L = 4
+  const bool served_l = a.W == kW ? a.L <= kVectorMaxL : a.L <= kMultiNarrowMaxL;
+  return a.D % 8 == 0 && served_l && m.sxd == 1 && m.sod == 1 &&
          m.sxn % 8 == 0 && m.sxt % 8 == 0 && m.son % 8 == 0 && m.sot % 8 == 0;
 }
 
@@ -322,7 +348,7 @@ ccu_status_t run_multi(const MultiArgs &m, int route, cudaStream_t stream) {
     return fail(CCU_ERR_INVALID_ARGUMENT, "unknown route %d", route);
   }
   const Args &a = m.a;
-  UpdateParams p;
+  UpdateParams p = {};
   p.x = static_cast<const uint16_t *>(a.x);
   p.ld = 0;
   p.state = static_cast<uint16_t *>(const_cast<void *>(a.state));
@@ -522,6 +548,25 @@ ccu_status_t ccu_conv1d_update_checked(const void *x, int64_t ld, void *conv_sta
                               indices, cache_seqlens, N, D, S, L, W, out, status_dev,
                               CCU_ROUTE_AUTO, stream);
 }
+
+ccu_status_t ccu_conv1d_update_checked_ex(const void *x, int64_t ld, void *conv_state,
+                                          int64_t stride_s, int64_t stride_d, int64_t stride_l,
+                                          const void *weight, const void *bias, ccu_act_t act,
+                                          const int32_t *indices, const int32_t *cache_seqlens,
+                                          int64_t N, int64_t D, int64_t S, int64_t L, int64_t W,
+                                          void *out, int32_t *status_dev, int32_t *slot_scratch,
+                                          int32_t route, ccu_stream_t stream) {
+  if (status_dev == nullptr)
+    return ccu::fail(CCU_ERR_INVALID_ARGUMENT, "status_dev must not be NULL");
+  if (slot_scratch == nullptr && indices != nullptr && N > 0 && D > 0 && S > 0)
+    return ccu::fail(CCU_ERR_INVALID_ARGUMENT, "slot_scratch must not be NULL");
+  Args a{x,    ld,      conv_state, stride_s,      stride_d, stride_l, weight, bias,
+         (int)act, indices, cache_seqlens, N, D, S, L, W, out, status_dev};
+  a.owner = slot_scratch;
+  return ccu::run(a, route, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int64_t ccu_conv1d_slot_scratch_bytes(int64_t S) { return S > 0 ? S * (int64_t)sizeof(int32_t) : 0; }
 
 ccu_status_t ccu_conv1d_select_route(const void *x, int64_t ld, const void *conv_state,
                                      int64_t stride_s, int64_t stride_d, int64_t stride_l,

@@ -127,6 +127,11 @@ __device__ __forceinline__ Slice slice_of(const UpdateParams &p, int64_t t, int6
       if (report) atomicOr(p.status, 1);  // CCU_DEVERR_RANGE
       sl.s = -1;
     }
+    // Duplicate check (every slice of the row gets the same answer; see claim_slot).
+    if (p.owner != nullptr && sl.s >= 0 && !claim_slot(p.owner, sl.s, sl.n)) {
+      if (report) atomicOr(p.status, 2);  // CCU_DEVERR_DUPLICATE
+      sl.s = -1;
+    }
   }
   sl.q = 0;
   if (sl.s >= 0 && p.seqlens != nullptr) {

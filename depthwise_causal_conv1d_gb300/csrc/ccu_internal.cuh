@@ -27,6 +27,7 @@ struct UpdateParams {
   const int32_t *seqlens; // [N] cache_seqlens (ring-buffer state) or nullptr (linear state)
   uint16_t *out;          // [N, D]
   int32_t *status;        // nullptr: unchecked; else device error word (range check on)
+  int32_t *owner;         // nullptr, or [S] slot owners (checked mode: duplicate check on)
   int64_t N, D, S, L, W;  // W: filter width (2, 3 or 4)
   int64_t ss, sd, sl;     // element strides of the state (used by the scalar kernel)
   int layout;             // Layout
@@ -173,14 +174,39 @@ cudaError_t launch_overlapped(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-// Slot of row n, or -1 for "no state access" (a padding row, or in checked mode a slot
-// out of range, which also raises CCU_DEVERR_RANGE in *status).
+// Duplicate check: row n claims slot s in owner[] (zeroed before the launch), which then
+// holds n + 1 for good. Every thread, CTA and slice working on row n may call this; all of
+// them get the same answer: true if row n owns the slot (it claimed it first), false if
+// another row did. The owner word is read from L2 first, so only the first claims of a slot
+// are atomic operations.
+__device__ __forceinline__ bool claim_slot(int32_t *owner, int64_t s, int64_t n) {
+  const int32_t me = (int32_t)(n + 1);
+  int32_t v = __ldcg(owner + s);
+  if (v == 0) {
+    v = atomicCAS(owner + s, 0, me);
+    if (v == 0) return true;
+  }
+  return v == me;
+}
+
+// Slot of row n, or -1 for "no state access" (a padding row; in checked mode also a slot
+// out of range, which raises CCU_DEVERR_RANGE in *status, and with the duplicate check a
+// slot another row has claimed, which raises CCU_DEVERR_DUPLICATE). DEDUP = false leaves
+// the duplicate check out of the code (kernels whose entry points never turn it on: the
+// multi-token update, whose two-row form spilled 164 instead of 72 bytes with it).
+template <bool DEDUP = true>
 __device__ __forceinline__ int64_t resolve_slot(const UpdateParams &p, int64_t n) {
   if (p.idx == nullptr) return n;
   int64_t s = __ldg(p.idx + n);
   if (p.status != nullptr && (s < -1 || s >= p.S)) {
     atomicOr(p.status, 1);  // CCU_DEVERR_RANGE
     return -1;
+  }
+  if constexpr (DEDUP) {
+    if (p.owner != nullptr && s >= 0 && !claim_slot(p.owner, s, n)) {
+      atomicOr(p.status, 2);  // CCU_DEVERR_DUPLICATE
+      return -1;
+    }
   }
   return s;
 }
@@ -251,11 +277,11 @@ struct RowSlot {
 // The cache_seqlens load is issued together with the index load (every row has an entry,
 // and it does not depend on the slot), so a ring row waits for one round of loads before
 // its state address is known, not two. LC: L known at compile time (0: use p.L).
-template <int LC = 0>
+template <int LC = 0, bool DEDUP = true>
 __device__ __forceinline__ RowSlot resolve_row(const UpdateParams &p, int64_t n) {
   RowSlot r;
   const int32_t v = p.seqlens != nullptr ? __ldg(p.seqlens + n) : 0;
-  r.s = resolve_slot(p, n);
+  r.s = resolve_slot<DEDUP>(p, n);
   r.q = 0;
   if (r.s >= 0 && p.seqlens != nullptr) {
     if (v < 0 && p.status != nullptr) {

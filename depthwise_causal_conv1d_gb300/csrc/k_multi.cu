@@ -27,7 +27,7 @@ __global__ void __launch_bounds__(256) k_multi_scalar(UpdateParams p, MultiParam
        i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t n = i / p.D;
     const int64_t d = i - n * p.D;
-    const RowSlot r = resolve_row(p, n);
+    const RowSlot r = resolve_row<0, false>(p, n);
     if (r.s < 0) {
       for (int64_t t = 0; t < m.T; ++t) p.out[n * m.son + d * m.sod + t * m.sot] = 0;
       continue;
@@ -116,14 +116,14 @@ __device__ __forceinline__ void compact_to_planes(const uint32_t (&cw)[4 * L], u
 // cap keeps (without the cap the kernel takes 170 registers, one CTA per SM, and loses).
 // The SiLU runs on channel pairs (the arithmetic is not hidden here: 86.0 -> 84.1 us), at
 // 72 spilled bytes.
-template <int L, int ACT, int LAYOUT, bool RING, int ROWS>
+template <int L, int W, int ACT, int LAYOUT, bool RING, int ROWS>
 __device__ __forceinline__ void multi_vector_body(const UpdateParams &p, const MultiParams &m) {
   const int64_t groups = p.D >> 3;
   const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (g >= groups) return;
   const int64_t c0 = g << 3;
   uint32_t wv[16];
-  load_weights_packed<kW>(p.w, c0, wv);
+  load_weights_packed<W>(p.w, c0, wv);
   const bool has_bias = p.bias != nullptr;
   uint32_t bv[4] = {0u, 0u, 0u, 0u};
   if (has_bias) {
@@ -139,7 +139,7 @@ __device__ __forceinline__ void multi_vector_body(const UpdateParams &p, const M
   };
   auto load_row = [&](int64_t n, MRow &r) {
     r.n = n;
-    r.slot = resolve_row<L>(p, n);
+    r.slot = resolve_row<L, false>(p, n);
     if (r.slot.s < 0) return;
     if constexpr (LAYOUT == (int)Layout::Compact) {
       const uint16_t *sp = p.state + r.slot.s * (p.D * L) + c0 * L;
@@ -187,10 +187,10 @@ __device__ __forceinline__ void multi_vector_body(const UpdateParams &p, const M
         uint32_t nw[4 * L];
         uint4 outv;
         if constexpr (RING) {
-          outv = update8_compact_ring<L, kW, ACT, true>(xw, r.ow, wv, bv, has_bias,
+          outv = update8_compact_ring<L, W, ACT, true>(xw, r.ow, wv, bv, has_bias,
                                                         (int)((r.slot.q + t) % L), nw);
         } else {
-          outv = update8_compact<L, kW, ACT, true>(xw, r.ow, wv, bv, has_bias, nw);
+          outv = update8_compact<L, W, ACT, true>(xw, r.ow, wv, bv, has_bias, nw);
         }
         st_stream(orow + t * m.sot, outv);
 #pragma unroll
@@ -237,52 +237,63 @@ __device__ __forceinline__ void multi_vector_body(const UpdateParams &p, const M
 }
 
 // Up to L = 6: two rows in flight under a 128-register cap (two CTAs per SM).
-template <int L, int ACT, int LAYOUT, bool RING>
+template <int L, int W, int ACT, int LAYOUT, bool RING>
 __global__ void __launch_bounds__(256, 2) k_multi_vector(UpdateParams p, MultiParams m) {
   grid_dependency_boundary();
-  multi_vector_body<L, ACT, LAYOUT, RING, 2>(p, m);
+  multi_vector_body<L, W, ACT, LAYOUT, RING, 2>(p, m);
 }
 
 // L = 7 and 8: one row in flight and the compiler's register budget (the two-row form
-// spills 300-600 bytes there under the cap).
-template <int L, int ACT, int LAYOUT, bool RING>
+// spills 300-600 bytes there under the cap; N=1024, D=16384, T=4: L = 7 148.3 against
+// 192.8 us, L = 8 144.7 against 206.9 us).
+template <int L, int W, int ACT, int LAYOUT, bool RING>
 __global__ void __launch_bounds__(256) k_multi_vector_long(UpdateParams p, MultiParams m) {
   grid_dependency_boundary();
-  multi_vector_body<L, ACT, LAYOUT, RING, 1>(p, m);
+  multi_vector_body<L, W, ACT, LAYOUT, RING, 1>(p, m);
 }
 
-template <int L, int ACT>
+template <int L, int W, int ACT, int LAYOUT, bool RING>
+cudaError_t launch_vec_one(const UpdateParams &p, const MultiParams &m, dim3 grid, dim3 block,
+                           cudaStream_t stream) {
+  if constexpr (L >= 7) {
+    return launch_overlapped(k_multi_vector_long<L, W, ACT, LAYOUT, RING>, grid, block, 0, stream, p, m);
+  } else {
+    return launch_overlapped(k_multi_vector<L, W, ACT, LAYOUT, RING>, grid, block, 0, stream, p, m);
+  }
+}
+
+template <int L, int W, int ACT>
 cudaError_t launch_vec_L(const UpdateParams &p, const MultiParams &m, dim3 grid, dim3 block,
                          cudaStream_t stream) {
   const bool ring = p.seqlens != nullptr;
   constexpr int kC = (int)Layout::Compact, kCL = (int)Layout::ChannelLast;
-  if constexpr (L >= 7) {
-    if (p.layout == kC) {
-      return ring ? launch_overlapped(k_multi_vector_long<L, ACT, kC, true>, grid, block, 0, stream, p, m)
-                  : launch_overlapped(k_multi_vector_long<L, ACT, kC, false>, grid, block, 0, stream, p, m);
-    }
-    return ring ? launch_overlapped(k_multi_vector_long<L, ACT, kCL, true>, grid, block, 0, stream, p, m)
-                : launch_overlapped(k_multi_vector_long<L, ACT, kCL, false>, grid, block, 0, stream, p, m);
-  } else {
-    if (p.layout == kC) {
-      return ring ? launch_overlapped(k_multi_vector<L, ACT, kC, true>, grid, block, 0, stream, p, m)
-                  : launch_overlapped(k_multi_vector<L, ACT, kC, false>, grid, block, 0, stream, p, m);
-    }
-    return ring ? launch_overlapped(k_multi_vector<L, ACT, kCL, true>, grid, block, 0, stream, p, m)
-                : launch_overlapped(k_multi_vector<L, ACT, kCL, false>, grid, block, 0, stream, p, m);
+  if (p.layout == kC) {
+    return ring ? launch_vec_one<L, W, ACT, kC, true>(p, m, grid, block, stream)
+                : launch_vec_one<L, W, ACT, kC, false>(p, m, grid, block, stream);
   }
+  return ring ? launch_vec_one<L, W, ACT, kCL, true>(p, m, grid, block, stream)
+              : launch_vec_one<L, W, ACT, kCL, false>(p, m, grid, block, stream);
 }
 
+// Width 4 with L = 3..8; widths 2 and 3 with L = W - 1..4 (the short states they are used
+// with; longer states run on the scalar kernel).
 template <int ACT>
 cudaError_t launch_vec_A(const UpdateParams &p, const MultiParams &m, dim3 grid, dim3 block,
                          cudaStream_t stream) {
-  switch (p.L) {
-    case 3: return launch_vec_L<3, ACT>(p, m, grid, block, stream);
-    case 4: return launch_vec_L<4, ACT>(p, m, grid, block, stream);
-    case 5: return launch_vec_L<5, ACT>(p, m, grid, block, stream);
-    case 6: return launch_vec_L<6, ACT>(p, m, grid, block, stream);
-    case 7: return launch_vec_L<7, ACT>(p, m, grid, block, stream);
-    case 8: return launch_vec_L<8, ACT>(p, m, grid, block, stream);
+  switch (p.W * 16 + p.L) {
+    case 4 * 16 + 3: return launch_vec_L<3, 4, ACT>(p, m, grid, block, stream);
+    case 4 * 16 + 4: return launch_vec_L<4, 4, ACT>(p, m, grid, block, stream);
+    case 4 * 16 + 5: return launch_vec_L<5, 4, ACT>(p, m, grid, block, stream);
+    case 4 * 16 + 6: return launch_vec_L<6, 4, ACT>(p, m, grid, block, stream);
+    case 4 * 16 + 7: return launch_vec_L<7, 4, ACT>(p, m, grid, block, stream);
+    case 4 * 16 + 8: return launch_vec_L<8, 4, ACT>(p, m, grid, block, stream);
+    case 3 * 16 + 2: return launch_vec_L<2, 3, ACT>(p, m, grid, block, stream);
+    case 3 * 16 + 3: return launch_vec_L<3, 3, ACT>(p, m, grid, block, stream);
+    case 3 * 16 + 4: return launch_vec_L<4, 3, ACT>(p, m, grid, block, stream);
+    case 2 * 16 + 1: return launch_vec_L<1, 2, ACT>(p, m, grid, block, stream);
+    case 2 * 16 + 2: return launch_vec_L<2, 2, ACT>(p, m, grid, block, stream);
+    case 2 * 16 + 3: return launch_vec_L<3, 2, ACT>(p, m, grid, block, stream);
+    case 2 * 16 + 4: return launch_vec_L<4, 2, ACT>(p, m, grid, block, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define CCU_CONV1D_ABI_VERSION 1
+#define CCU_CONV1D_ABI_VERSION 2
 
 /* Every entry point is exported from the shared library (the rest is hidden). */
 #if defined(__GNUC__)
@@ -159,7 +159,7 @@ CCU_API ccu_status_t ccu_conv1d_update(const void *x, int64_t ld, void *conv_sta
  * implementation", last paragraph); a trap kills the CUDA context, so this library
  * reports instead: a row whose slot is < -1 or >= S is treated as a padding row (output
  * +0, no state access) and CCU_DEVERR_RANGE is ORed into *status_dev. Duplicate slots
- * are not detected here (see ccu_conv1d_check_indices).
+ * are not detected here (see ccu_conv1d_update_checked_ex, or ccu_conv1d_check_indices).
  *
  *   status_dev  device int32 word, not cleared by the call: errors accumulate until the
  *               caller resets it. 4-byte aligned, must not be NULL.
@@ -171,6 +171,43 @@ CCU_API ccu_status_t ccu_conv1d_update_checked(const void *x, int64_t ld, void *
                                        const int32_t *indices, const int32_t *cache_seqlens,
                                        int64_t N, int64_t D, int64_t S, int64_t L, int64_t W,
                                        void *out, int32_t *status_dev, ccu_stream_t stream);
+
+/*
+ * ccu_conv1d_update_checked_ex -- the checked update that also detects duplicate slots, in
+ * the same launch, on the kernel family `route` selects.
+ *
+ * The page's kernel checks the slot indices on the device and traps on values below -1, on
+ * slots past the cache and on non-padding slots repeated across rows ("Current native
+ * implementation", last paragraph; conv_state_indices paragraph). Here nothing traps: a row
+ * whose slot is out of range raises CCU_DEVERR_RANGE and a row whose slot another row has
+ * already claimed raises CCU_DEVERR_DUPLICATE, and either row is then treated as a padding
+ * row (output +0, no state access). Of the rows that share a slot exactly one updates it:
+ * whichever claims it first, which may differ from one call to the next; so the state of a
+ * repeated slot is one of its rows' updates, not a mix of them (the page leaves the update
+ * non-transactional).
+ *
+ *   status_dev    device int32 word as in ccu_conv1d_update_checked; must not be NULL.
+ *   slot_scratch  device int32 [S] (ccu_conv1d_slot_scratch_bytes(S) bytes), 4-byte
+ *                 aligned, owned by the caller. The call clears it on `stream` before the
+ *                 update (so its contents on entry do not matter) and leaves in it, for each
+ *                 slot, 1 + the row that updated it (0: no row). May be NULL only when
+ *                 indices is NULL (row n uses slot n: no slot can repeat). Calls that
+ *                 overlap on the GPU must not share it.
+ *   N             at most 2^31 - 2 (CCU_ERR_NOT_IMPLEMENTED beyond).
+ *   route         CCU_ROUTE_AUTO or a family, as in ccu_conv1d_update_ex.
+ * Other arguments and returns as ccu_conv1d_update.
+ */
+CCU_API ccu_status_t ccu_conv1d_update_checked_ex(const void *x, int64_t ld, void *conv_state,
+                                                  int64_t stride_s, int64_t stride_d, int64_t stride_l,
+                                                  const void *weight, const void *bias, ccu_act_t act,
+                                                  const int32_t *indices, const int32_t *cache_seqlens,
+                                                  int64_t N, int64_t D, int64_t S, int64_t L, int64_t W,
+                                                  void *out, int32_t *status_dev, int32_t *slot_scratch,
+                                                  int32_t route, ccu_stream_t stream);
+
+/* Bytes of slot_scratch ccu_conv1d_update_checked_ex needs for S slots (4 * S; 0 for
+ * S <= 0). */
+CCU_API int64_t ccu_conv1d_slot_scratch_bytes(int64_t S);
 
 /*
  * ccu_conv1d_update_ex -- the update with an explicit kernel family (for tests and A/B

@@ -48,7 +48,7 @@ def guarded_u16(a: np.ndarray, dev):
 
 
 def run_gpu(inp: synthetic.Inputs, layout="compact", route="auto", checked=False, dev="cuda:0",
-            stream=None, guards=True, cache_seqlens=None):
+            stream=None, guards=True, cache_seqlens=None, slot_scratch=None):
     """One update on the GPU through the torch binding (which calls the C-ABI).
 
     Returns (out, logical state [S, D, L], status or None, guards_ok).
@@ -70,10 +70,11 @@ def run_gpu(inp: synthetic.Inputs, layout="compact", route="auto", checked=False
     go = Guarded(N * D * 2, dev)
     out = go.view(torch.bfloat16, (N, D))
     status = torch.zeros((1,), dtype=torch.int32, device=dev) if checked else None
+
     ctx = torch.cuda.stream(stream) if stream is not None else torch.cuda.stream(torch.cuda.current_stream())
     with ctx:
         ccu.causal_conv1d_update(x, st, w, b, wl.act, conv_state_indices=idx, cache_seqlens=seq,
-                                 out=out, route=route, status=status)
+                                 out=out, route=route, status=status, slot_scratch=slot_scratch)
     torch.cuda.synchronize()
     got_out = from_dev_u16(out)
     mem = from_dev_u16(gs.view(torch.int16, state_mem.shape))

@@ -67,7 +67,7 @@ def test_status_strings(ccu):
     assert ccu.ccu_status_string(99) == "unknown status"
     assert [ccu.ccu_route_name(r) for r in range(5)] == ["auto", "scalar", "vector", "staged", "bulk"]
     assert ccu.ccu_route_name(5) == "unknown"
-    assert ccu.ccu_conv1d_abi_version() == 1
+    assert ccu.ccu_conv1d_abi_version() == 2
     assert ccu.ccu_conv1d_check_indices_scratch_bytes(0) == 0
     assert ccu.ccu_conv1d_check_indices_scratch_bytes(1) == 4
     assert ccu.ccu_conv1d_check_indices_scratch_bytes(32) == 4
@@ -154,8 +154,10 @@ def test_widths_2_and_3_are_served(ccu):
     # large compact batches take the bulk kernels, compiled for widths 2 and 3 up to L = 4
     assert select(ccu, W=3, L=2, N=1024, D=16384, S=1024) == (0, 4)
     assert select(ccu, W=3, L=2, N=4096, D=16384, S=4096) == (0, 2)  # window-only state, full batch
-    assert select(ccu, W=3, L=3, N=4096, D=16384, S=4096) == (0, 4)
+    assert select(ccu, W=3, L=3, N=512, D=16384, S=512) == (0, 4)
+    assert select(ccu, W=3, L=3, N=4096, D=16384, S=4096) == (0, 2)  # lean vector past 2^23
     assert select(ccu, W=2, L=2, N=4096, D=16384, S=4096) == (0, 4)
+    assert select(ccu, W=2, L=4, N=4096, D=16384, S=4096) == (0, 4)
     assert select(ccu, W=2, L=1, N=4096, D=16384, S=4096) == (0, 2)  # one-entry state: vector
     assert select(ccu, W=3, L=5, N=4096, D=16384, S=4096) == (0, 2)
     assert select(ccu, route=4, W=3, L=3) == (0, 4)
@@ -167,7 +169,8 @@ def test_widths_2_and_3_are_served(ccu):
 
 def test_ring_buffer_state_is_served(ccu):
     assert select(ccu, cache_seqlens=0x700000) == (0, 2)
-    assert select(ccu, cache_seqlens=0x700000, N=4096, D=16384, S=4096) == (0, 4)
+    assert select(ccu, cache_seqlens=0x700000, N=4096, D=16384, S=4096) == (0, 2)  # vector at every size
+    assert select(ccu, route=4, cache_seqlens=0x700000, N=4096, D=16384, S=4096) == (0, 4)
 
 
 def test_indices_allow_S_below_N(ccu):
@@ -185,7 +188,8 @@ ROUTE_CASES = [
     ("channel-last L3", dict(stride_s=192, stride_d=1, stride_l=64), "vector"),
     ("channel-last L12", dict(L=12, stride_s=768, stride_d=1, stride_l=64), "staged"),
     ("padded ld", dict(ld=72), "vector"),
-    ("large batch compact", dict(N=4096, D=16384, S=4096), "bulk"),
+    ("large batch compact", dict(N=4096, D=16384, S=4096), "vector"),
+    ("large batch compact L4", dict(N=4096, D=16384, S=4096, L=4), "bulk"),
     ("mid batch compact", dict(N=256, D=8192, S=256), "bulk"),
     ("below the bulk threshold", dict(N=64, D=8192, S=64), "vector"),
     ("large batch channel-last", dict(N=4096, D=16384, S=4096, stride_s=3 * 16384, stride_d=1,
@@ -246,20 +250,54 @@ def test_every_kernel_waits_for_prior_grids_first():
 
 
 def test_auto_route_thresholds(ccu):
-    """The AUTO route at the measured thresholds: compact batches take the bulk kernel from
-    2^20 (row, channel) elements; width 3 with a window-only state (L = 2) returns to the
-    vector kernel from 3 * 2^24; the channel-last state never takes the bulk kernel; a
-    one-entry state (L = 1) never does either."""
+    """The AUTO route at the measured thresholds: linear compact batches take the bulk kernel
+    from 2^20 (row, channel) elements, at L = 3, 5 and 6 only up to 2^23 (the lean vector
+    kernel beyond), at L = 4 and 7 at every size, never at L = 8 or L = 1; width 3 with a
+    window-only state (L = 2) returns to the vector kernel from 3 * 2^24; the ring state and
+    the channel-last state never take the bulk kernel."""
     D = 16384
     below, at = (1 << 20) // D - 1, (1 << 20) // D  # 63 and 64 rows
     assert select(ccu, N=below, S=below, D=D) == (0, 2)
     assert select(ccu, N=at, S=at, D=D) == (0, 4)
+    lean = (1 << 23) // D  # 512 rows
+    assert select(ccu, N=lean, S=lean, D=D) == (0, 4)
+    assert select(ccu, N=lean + 1, S=lean + 1, D=D) == (0, 2)
+    assert select(ccu, N=4096, S=4096, D=D) == (0, 2)
+    for L in (5, 6):
+        assert select(ccu, N=lean, S=lean, D=D, L=L, stride_s=D * L, stride_l=1, stride_d=L) == (0, 4)
+        assert select(ccu, N=4096, S=4096, D=D, L=L, stride_s=D * L, stride_l=1, stride_d=L) == (0, 2)
+    for L in (4, 7):
+        assert select(ccu, N=4096, S=4096, D=D, L=L, stride_s=D * L, stride_l=1, stride_d=L) == (0, 4)
+    assert select(ccu, N=4096, S=4096, D=D, L=8, stride_s=D * 8, stride_l=1, stride_d=8) == (0, 2)
     w3_below, w3_at = (3 << 24) // D - 1, (3 << 24) // D  # 3071 and 3072 rows
     assert select(ccu, N=w3_below, S=w3_below, D=D, W=3, L=2) == (0, 4)
     assert select(ccu, N=w3_at, S=w3_at, D=D, W=3, L=2) == (0, 2)
-    assert select(ccu, N=w3_at, S=w3_at, D=D, W=3, L=3) == (0, 4)  # L = 3 stays on bulk
+    assert select(ccu, N=lean, S=lean, D=D, W=3, L=3) == (0, 4)
+    assert select(ccu, N=w3_at, S=w3_at, D=D, W=3, L=3) == (0, 2)  # L = 3 past 2^23: lean vector
     cl = dict(stride_s=3 * D, stride_d=1, stride_l=D)
     for n in (at, 1024, w3_below, 4096):
         assert select(ccu, N=n, S=n, D=D, **cl) == (0, 2), n
         assert select(ccu, N=n, S=n, D=D, cache_seqlens=0x700000, **cl) == (0, 2), n
+        assert select(ccu, N=n, S=n, D=D, cache_seqlens=0x700000) == (0, 2), n
     assert select(ccu, N=4096, S=4096, D=D, W=2, L=1) == (0, 2)
+
+
+def test_checked_ex_declines(ccu):
+    """The duplicate-checking update: its own argument checks run before anything is
+    enqueued (placeholder pointers are never dereferenced)."""
+    assert ccu.ccu_conv1d_slot_scratch_bytes(0) == 0
+    assert ccu.ccu_conv1d_slot_scratch_bytes(4096) == 16384
+    base = dict(x=X, ld=64, st=ST, ss=192, sd=3, sl=1, w=WT, b=None, act=0, idx=IDX, seq=None,
+                N=4, D=64, S=4, L=3, W=4, out=OUT)
+
+    def call(status, scratch, **kw):
+        a = {**base, **kw}
+        return ccu.ccu_conv1d_update_checked_ex(a["x"], a["ld"], a["st"], a["ss"], a["sd"], a["sl"], a["w"],
+                                                a["b"], a["act"], a["idx"], a["seq"], a["N"], a["D"], a["S"],
+                                                a["L"], a["W"], a["out"], status, scratch, 0, None)
+
+    assert call(None, 0x700000) == 1            # no status word
+    assert call(0x800000, None) == 1            # indices but no scratch
+    assert call(0x800000, 0x700002) == 1        # scratch not 4-byte aligned
+    assert call(0x800000, 0x700000, N=(1 << 31) - 1, S=(1 << 31) - 1) == 2  # rows past the row tags
+    assert call(0x800000, 0x700000, N=0) == 0   # no-op

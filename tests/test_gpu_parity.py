@@ -449,6 +449,52 @@ def test_checked_path_clean_inputs_report_nothing():
     assert_parity(inp, got_out, got_state, want_out, want_state, "checked clean")
 
 
+DEDUP_CASES = ["valid", "duplicate", "range", "padding_only", "both"]
+
+
+@pytest.mark.parametrize("case", DEDUP_CASES)
+@pytest.mark.parametrize("layout", ["compact", "channel_last"])
+@pytest.mark.parametrize("route", ["scalar", "vector", "staged", "bulk"])
+def test_checked_update_detects_duplicates_in_the_same_launch(route, layout, case):
+    """ccu_conv1d_update_checked_ex: the status bits equal the oracle's index check; a row
+    whose slot is out of range or was claimed by another row behaves as a padding row; of
+    the rows sharing a slot exactly one updated it (the winner, read back from the slot
+    scratch), so output and state equal the oracle's update with the losers as padding."""
+    wl = synthetic.variant(synthetic.WORKLOADS["paged_n256_d8192_l3_s1024_pad10_silu"], name="dedup",
+                           N=40, D=1032, ld=1032, S=64, indices="distinct_pad", pad_frac=0.1)
+    inp = synthetic.generate(wl, seed=31 + DEDUP_CASES.index(case))
+    idx = inp.indices.copy()
+    active = np.flatnonzero(idx >= 0)
+    groups = []
+    if case in ("duplicate", "both"):
+        groups = [[active[2], active[17], active[30]], [active[5], active[6]]]
+        for g in groups:
+            idx[g] = idx[g[0]]
+    if case in ("range", "both"):
+        idx[active[9]] = -2
+        idx[active[12]] = wl.S
+    if case == "padding_only":
+        idx[:] = -1
+    want_status = oracle.check_indices(idx, wl.N, wl.S)
+    scratch = torch.full((wl.S,), 12345, dtype=torch.int32, device=DEV)  # dirty: the call clears it
+    got_out, got_state, status, ok = run_gpu(dataclasses.replace(inp, indices=idx), layout=layout, route=route,
+                                             checked=True, slot_scratch=scratch)
+    assert ok, "a guard band was overwritten"
+    assert status == want_status, (status, want_status)
+    owners = scratch.cpu().numpy()
+    ref_idx = idx.copy()
+    ref_idx[(idx < -1) | (idx >= wl.S)] = -1
+    for g in groups:
+        winner = owners[idx[g[0]]] - 1
+        assert winner in g, (winner, g)
+        ref_idx[[r for r in g if r != winner]] = -1
+    for n in np.flatnonzero(ref_idx >= 0):
+        assert owners[ref_idx[n]] == n + 1
+    assert np.count_nonzero(owners) == np.count_nonzero(ref_idx >= 0)
+    want_out, want_state = oracle_ref(dataclasses.replace(inp, indices=ref_idx), layout)
+    assert_parity(inp, got_out, got_state, want_out, want_state, f"dedup {route} {layout} {case}")
+
+
 @pytest.mark.parametrize("layout", ["compact", "channel_last"])
 @pytest.mark.parametrize("route", ["vector", "bulk"])
 def test_large_batch_routes_agree_bitwise(route, layout):
