@@ -251,7 +251,9 @@ def causal_conv1d_update(x, conv_state, weight, bias=None, activation=None, *, c
     ``bias`` BF16 ``[D]`` or None; ``activation`` None/"identity" or "silu"/"swish";
     ``conv_state_indices`` int32 ``[N]`` (``-1`` = padding row) or None; ``cache_seqlens``
     None (linear state) or int32 ``[N]``: the state is then a ring buffer whose oldest entry
-    is at ``cache_seqlens[n] % L`` and only that entry is overwritten. ``out`` (optional, preallocated ``[N, D]`` BF16), ``route`` (kernel
+    is at ``cache_seqlens[n] % L`` and only that entry is overwritten (use the channel-last
+    layout for a ring: it then moves only the window and one entry, the compact layout moves
+    the whole slab). ``out`` (optional, preallocated ``[N, D]`` BF16), ``route`` (kernel
     family), ``status`` (int32 device word: turns on the device range check) and
     ``slot_scratch`` (int32 ``[S]`` device tensor, with ``status``: also detects repeated
     slots in the same launch, see ccu_conv1d_update_checked_ex) are extensions of this

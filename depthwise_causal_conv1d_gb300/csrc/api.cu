@@ -440,7 +440,7 @@ ccu_status_t run_prefill(const PrefillArgs &a, int route, cudaStream_t stream) {
   if (!mul_le(a.B, a.D, lim) || !mul_le(a.B * a.D, a.T, lim) || !mul_le(a.B * a.D, a.L, lim))
     return fail(CCU_ERR_INVALID_ARGUMENT, "tensor sizes overflow 64-bit indexing");
 
-  const bool vec_ok = a.D % 8 == 0 && a.W == kW && a.sxd == 1 && a.sod == 1 && a.sxb % 8 == 0 &&
+  const bool vec_ok = a.D % 8 == 0 && a.sxd == 1 && a.sod == 1 && a.sxb % 8 == 0 &&
                       a.sxt % 8 == 0 && a.sob % 8 == 0 && a.sot % 8 == 0 && a.B <= 65535;
   PrefillParams f;
   f.B = a.B;

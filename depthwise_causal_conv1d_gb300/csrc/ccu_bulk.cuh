@@ -109,8 +109,9 @@ struct Slice {
 };
 
 // LC: L known at compile time. The cache_seqlens load is issued together with the index
-// load, as in resolve_row.
-template <int G, int LC>
+// load, as in resolve_row. DEDUP = false leaves out the duplicate check (the producer lane
+// makes it after issuing the slice's copies, see claim_after_issue).
+template <int G, int LC, bool DEDUP = true>
 __device__ __forceinline__ Slice slice_of(const UpdateParams &p, int64_t t, int64_t slices, bool report) {
   constexpr int64_t kSlice = 256 * G;
   Slice sl;
@@ -128,9 +129,11 @@ __device__ __forceinline__ Slice slice_of(const UpdateParams &p, int64_t t, int6
       sl.s = -1;
     }
     // Duplicate check (every slice of the row gets the same answer; see claim_slot).
-    if (p.owner != nullptr && sl.s >= 0 && !claim_slot(p.owner, sl.s, sl.n)) {
-      if (report) atomicOr(p.status, 2);  // CCU_DEVERR_DUPLICATE
-      sl.s = -1;
+    if constexpr (DEDUP) {
+      if (p.owner != nullptr && sl.s >= 0 && !claim_slot(p.owner, sl.s, sl.n)) {
+        if (report) atomicOr(p.status, 2);  // CCU_DEVERR_DUPLICATE
+        sl.s = -1;
+      }
     }
   }
   sl.q = 0;
@@ -144,6 +147,13 @@ __device__ __forceinline__ Slice slice_of(const UpdateParams &p, int64_t t, int6
     }
   }
   return sl;
+}
+
+// The producer lane's duplicate check, after it has issued the slice's copies: raises
+// CCU_DEVERR_DUPLICATE if another row owns the slot. The lanes that compute the slice call
+// slice_of with the check and get the same answer, so they drop the staged data.
+__device__ __forceinline__ void claim_after_issue(const UpdateParams &p, const Slice &sl) {
+  if (p.owner != nullptr && sl.s >= 0 && !claim_slot(p.owner, sl.s, sl.n)) atomicOr(p.status, 2);
 }
 
 }  // namespace bulk

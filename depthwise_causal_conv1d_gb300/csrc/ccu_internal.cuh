@@ -298,6 +298,41 @@ __device__ __forceinline__ RowSlot resolve_row(const UpdateParams &p, int64_t n)
   return r;
 }
 
+// The duplicate check of a row whose slot resolved without it (resolve_row<LC, false>),
+// made after the row's loads have been issued so that its latency overlaps theirs: if
+// another row owns the slot, the row becomes a padding row (the loaded values are dropped:
+// output +0, no state written; the reads stayed inside the range-checked slot).
+__device__ __forceinline__ void drop_if_duplicate(const UpdateParams &p, int64_t n, RowSlot &r) {
+  if (p.owner != nullptr && r.s >= 0 && !claim_slot(p.owner, r.s, n)) {
+    atomicOr(p.status, 2);  // CCU_DEVERR_DUPLICATE
+    r.s = -1;
+  }
+}
+
+// The lanes of the calling thread's warp whose 8-channel group g is below `groups` (the
+// others exit early in the vector kernels).
+__device__ __forceinline__ unsigned live_lanes(int64_t groups) {
+  const int64_t first = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31);
+  const int64_t live = groups - first;
+  return live >= 32 ? 0xffffffffu : ((1u << live) - 1u);
+}
+
+// drop_if_duplicate for the vector kernels, whose warps work on one row at a time and whose
+// lanes past the last 8-channel group (p.D / 8) have exited: lane 0 claims the slot for the
+// whole warp and passes the answer to the live lanes (lane 0 is always one of them), so a
+// row costs one claim per warp rather than one per thread (at N=4096, D=16384 per-thread
+// claims made the checked update 45 % slower).
+__device__ __forceinline__ void drop_if_duplicate_warp(const UpdateParams &p, int64_t n, RowSlot &r) {
+  if (p.owner == nullptr || r.s < 0) return;  // the same for every lane: one row per warp
+  const unsigned live = live_lanes(p.D >> 3);
+  int own = 1;
+  if ((threadIdx.x & 31) == 0) {
+    own = claim_slot(p.owner, r.s, n) ? 1 : 0;
+    if (!own) atomicOr(p.status, 2);  // CCU_DEVERR_DUPLICATE
+  }
+  if (!__shfl_sync(live, own, 0)) r.s = -1;
+}
+
 // The ring-buffer form of update8_compact for a ring position Q known at compile time:
 // the 8 channels' rings sit in `ow` (flat position c*L + l) and Q is the ring position of
 // the oldest entry. The history, oldest first, is ring[Q], ring[Q+1], ..., ring[Q+L-1]
@@ -405,34 +440,58 @@ __device__ __forceinline__ void widen8(const uint4 v, float2 (&f)[4]) {
   for (int i = 0; i < 4; ++i) f[i] = make_float2(bf16_lo(w[i]), bf16_hi(w[i]));
 }
 
-// The width-4 weights of channels c0..c0+7 as float pairs: wf[j][i] = weight[c0 + 2i (+1), j].
+// The width-W weights of channels c0..c0+7 as float pairs: wf[j][i] = weight[c0 + 2i (+1), j]
+// for j < W (taps j >= W are zero and unused).
+template <int W = kW>
 __device__ __forceinline__ void load_weights_f(const uint16_t *w, int64_t c0, float2 (&wf)[kW][4]) {
-  const uint16_t *wp = w + c0 * kW;
+  if constexpr (W == kW) {
+    const uint16_t *wp = w + c0 * kW;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {  // 16 bytes = channels 2k, 2k+1, all four taps each
-    const uint4 t = ld_keep(wp + 8 * k);
-    wf[0][k] = make_float2(bf16_lo(t.x), bf16_lo(t.z));
-    wf[1][k] = make_float2(bf16_hi(t.x), bf16_hi(t.z));
-    wf[2][k] = make_float2(bf16_lo(t.y), bf16_lo(t.w));
-    wf[3][k] = make_float2(bf16_hi(t.y), bf16_hi(t.w));
+    for (int k = 0; k < 4; ++k) {  // 16 bytes = channels 2k, 2k+1, all four taps each
+      const uint4 t = ld_keep(wp + 8 * k);
+      wf[0][k] = make_float2(bf16_lo(t.x), bf16_lo(t.z));
+      wf[1][k] = make_float2(bf16_hi(t.x), bf16_hi(t.z));
+      wf[2][k] = make_float2(bf16_lo(t.y), bf16_lo(t.w));
+      wf[3][k] = make_float2(bf16_hi(t.y), bf16_hi(t.w));
+    }
+  } else {
+    uint32_t wv[16];
+    load_weights_packed<W>(w, c0, wv);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int j = 0; j < kW; ++j)
+        wf[j][k] = j < W ? make_float2(bf16_bits(get16(wv, (2 * k) * W + j)), bf16_bits(get16(wv, (2 * k + 1) * W + j)))
+                         : make_float2(0.0f, 0.0f);
   }
 }
 
 // Outputs of 8 channels (4 pairs) for one token from the window a, b, c (oldest first) and
-// the token's inputs x. The accumulation order is the update's: ((0 + a*w0) + b*w1) + c*w2 +
-// x*w3, then the bias (each product of two BF16 values is exact in FP32); the paired FP32
-// instructions round each half exactly as the scalar ones.
-template <int ACT>
+// the token's inputs x. The accumulation order is the update's: width 4 ((0 + a*w0) + b*w1)
+// + c*w2 + x*w3, width 3 (0 + b*w0) + c*w1 + x*w2, width 2 (0 + c*w0) + x*w1, then the bias
+// (each product of two BF16 values is exact in FP32); the paired FP32 instructions round each
+// half exactly as the scalar ones.
+template <int ACT, int W = kW>
 __device__ __forceinline__ uint4 outputs8f(const float2 (&wf)[kW][4], const float2 (&bf)[4],
                                            bool has_bias, const float2 (&a)[4], const float2 (&b)[4],
                                            const float2 (&c)[4], const float2 (&x)[4]) {
   uint32_t y[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    float2 acc = __ffma2_rn(a[i], wf[0][i], make_float2(0.0f, 0.0f));
-    acc = __ffma2_rn(b[i], wf[1][i], acc);
-    acc = __ffma2_rn(c[i], wf[2][i], acc);
-    acc = __ffma2_rn(x[i], wf[3][i], acc);
+    float2 acc;
+    if constexpr (W == 4) {
+      acc = __ffma2_rn(a[i], wf[0][i], make_float2(0.0f, 0.0f));
+      acc = __ffma2_rn(b[i], wf[1][i], acc);
+      acc = __ffma2_rn(c[i], wf[2][i], acc);
+      acc = __ffma2_rn(x[i], wf[3][i], acc);
+    } else if constexpr (W == 3) {
+      acc = __ffma2_rn(b[i], wf[0][i], make_float2(0.0f, 0.0f));
+      acc = __ffma2_rn(c[i], wf[1][i], acc);
+      acc = __ffma2_rn(x[i], wf[2][i], acc);
+    } else {
+      acc = __ffma2_rn(c[i], wf[0][i], make_float2(0.0f, 0.0f));
+      acc = __ffma2_rn(x[i], wf[1][i], acc);
+    }
     if (has_bias) acc = __fadd2_rn(acc, bf[i]);
     const float2 v = activate2<ACT>(acc);
     y[i] = pack_bf16x2(v.x, v.y);

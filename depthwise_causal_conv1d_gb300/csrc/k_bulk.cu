@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(kThreads) k_update_bulk(UpdateParams p, int st
 
   // Lane 0: put this warp's k-th slice into stage k % P.
   auto issue = [&](int64_t k) {
-    const Slice sl = slice_of<G, L>(p, first + k * stride, slices, true);
+    const Slice sl = slice_of<G, L, false>(p, first + k * stride, slices, true);
     uint64_t *bar = &bars[k % P];
     unsigned char *buf = bufs + (k % P) * stage_bytes;
     if (sl.s < 0) {
@@ -86,6 +86,7 @@ __global__ void __launch_bounds__(kThreads) k_update_bulk(UpdateParams p, int st
       mbar_arrive_expect_tx(bar, bx + bs);
       bulk_load(buf, p.x + sl.n * p.ld + sl.c_base, bx, bar);
       bulk_load(buf + 2 * kSlice, p.state + sl.s * (p.D * L) + sl.c_base * L, bs, bar);
+      claim_after_issue(p, sl);
     }
   };
 

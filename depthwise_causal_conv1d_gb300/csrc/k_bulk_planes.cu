@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(kThreads) k_update_bulk_planes(UpdateParams p,
   };
 
   auto issue = [&](int64_t k) {
-    const Slice sl = slice_of<kG, L>(p, first_item + k * stride, slices, true);
+    const Slice sl = slice_of<kG, L, false>(p, first_item + k * stride, slices, true);
     uint64_t *bar = &bars[k % P];
     unsigned char *buf = bufs + (k % P) * stage_bytes;
     if (sl.s < 0) {
@@ -104,6 +104,7 @@ __global__ void __launch_bounds__(kThreads) k_update_bulk_planes(UpdateParams p,
 #pragma unroll
     for (int b = 0; b < NB; ++b)
       bulk_load(buf + (1 + b) * kPlane, slot + plane_of(b, sl.q) * plane_stride, bytes, bar);
+    claim_after_issue(p, sl);
   };
 
   const int64_t pre = A > 0 ? A : P;

@@ -78,7 +78,10 @@ __global__ void __launch_bounds__(256) k_prefill_scalar(UpdateParams p, PrefillP
 }
 
 // The window before token t0 for channels c0..c0+7: inputs t0-3, t0-2, t0-1 (from x, or the
-// initial state / zeros before the sequence).
+// initial state / zeros before the sequence). Width W reads only the last W - 1 of them (an
+// earlier one can lie before the initial state, which holds L >= W - 1 entries); the others
+// are set to zero and never used.
+template <int W>
 __device__ __forceinline__ void load_halo(const UpdateParams &p, const PrefillParams &f, int64_t b,
                                           int64_t c0, int64_t t0, float2 (&h0)[4], float2 (&h1)[4],
                                           float2 (&h2)[4]) {
@@ -87,6 +90,11 @@ __device__ __forceinline__ void load_halo(const UpdateParams &p, const PrefillPa
 #pragma unroll
   for (int k = 0; k < kW - 1; ++k) {
     const int64_t t = t0 - (kW - 1) + k;
+    if (k < kW - W) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) hs[k][i] = make_float2(0.0f, 0.0f);
+      continue;
+    }
     if (t >= 0) {
       float2 tmp[4];
       widen8(ld_keep(xb + t * f.sxt), tmp);
@@ -114,36 +122,42 @@ __device__ __forceinline__ void widen8s(const uint4 v, float (&f)[8]) {
   }
 }
 
-// The width-4 weights of channels c0..c0+7 as floats: wf[j][c] = weight[c0 + c, j].
+// The width-W weights of channels c0..c0+7 as floats: wf[j][c] = weight[c0 + c, j], j < W.
+template <int W>
 __device__ __forceinline__ void load_weights_s(const UpdateParams &p, int64_t c0, float (&wf)[kW][8]) {
-  const uint16_t *wp = p.w + c0 * kW;
+  uint32_t wv[16];
+  load_weights_packed<W>(p.w, c0, wv);
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const uint4 t = ld_keep(wp + 8 * k);
-    const uint32_t v[4] = {t.x, t.y, t.z, t.w};
+  for (int c = 0; c < 8; ++c)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int e = 8 * k + 2 * i;  // flat c*4 + j of the low half
-      wf[e % kW][e / kW] = bf16_lo(v[i]);
-      wf[(e + 1) % kW][(e + 1) / kW] = bf16_hi(v[i]);
-    }
-  }
+    for (int j = 0; j < kW; ++j) wf[j][c] = j < W ? bf16_bits(get16(wv, c * W + j)) : 0.0f;
 }
 
 // Outputs of 8 channels for one token from the window a, b, c (oldest first) and the token's
-// inputs x. The accumulation order is the update's: ((0 + a*w0) + b*w1) + c*w2 + x*w3, then
-// the bias (each product of two BF16 values is exact in FP32).
-template <int ACT>
+// inputs x. The accumulation order is the update's: for width 4 ((0 + a*w0) + b*w1) + c*w2 +
+// x*w3, for width 3 (0 + b*w0) + c*w1 + x*w2, for width 2 (0 + c*w0) + x*w1, then the bias
+// (each product of two BF16 values is exact in FP32).
+template <int ACT, int W>
 __device__ __forceinline__ uint4 outputs8s(const float (&wf)[kW][8], const float (&bf)[8],
                                            bool has_bias, const float (&a)[8], const float (&b)[8],
                                            const float (&c)[8], const float (&x)[8]) {
   float y[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    float acc = __fmaf_rn(a[i], wf[0][i], 0.0f);
-    acc = __fmaf_rn(b[i], wf[1][i], acc);
-    acc = __fmaf_rn(c[i], wf[2][i], acc);
-    acc = __fmaf_rn(x[i], wf[3][i], acc);
+    float acc;
+    if constexpr (W == 4) {
+      acc = __fmaf_rn(a[i], wf[0][i], 0.0f);
+      acc = __fmaf_rn(b[i], wf[1][i], acc);
+      acc = __fmaf_rn(c[i], wf[2][i], acc);
+      acc = __fmaf_rn(x[i], wf[3][i], acc);
+    } else if constexpr (W == 3) {
+      acc = __fmaf_rn(b[i], wf[0][i], 0.0f);
+      acc = __fmaf_rn(c[i], wf[1][i], acc);
+      acc = __fmaf_rn(x[i], wf[2][i], acc);
+    } else {
+      acc = __fmaf_rn(c[i], wf[0][i], 0.0f);
+      acc = __fmaf_rn(x[i], wf[1][i], acc);
+    }
     if (has_bias) acc = acc + bf[i];
     y[i] = activate<ACT>(acc);
   }
@@ -153,6 +167,7 @@ __device__ __forceinline__ uint4 outputs8s(const float (&wf)[kW][8], const float
 
 // The window before token t0 for channels c0..c0+7: inputs t0-3, t0-2, t0-1 (from x, or the
 // initial state / zeros before the sequence).
+template <int W>
 __device__ __forceinline__ void load_halo_s(const UpdateParams &p, const PrefillParams &f, int64_t b,
                                           int64_t c0, int64_t t0, float (&h0)[8], float (&h1)[8],
                                           float (&h2)[8]) {
@@ -161,6 +176,11 @@ __device__ __forceinline__ void load_halo_s(const UpdateParams &p, const Prefill
 #pragma unroll
   for (int k = 0; k < kW - 1; ++k) {
     const int64_t t = t0 - (kW - 1) + k;
+    if (k < kW - W) {  // outside a width-W window (see load_halo)
+#pragma unroll
+      for (int c = 0; c < 8; ++c) hs[k][c] = 0.0f;
+      continue;
+    }
     if (t >= 0) {
       float tmp[8];
       widen8s(ld_keep(xb + t * f.sxt), tmp);
@@ -173,14 +193,14 @@ __device__ __forceinline__ void load_halo_s(const UpdateParams &p, const Prefill
   }
 }
 
-// 8 channels per thread, width 4; x and out channel-contiguous (one 16-byte vector per
+// 8 channels per thread, width W (2..4); x and out channel-contiguous (one 16-byte vector per
 // token). The prefill moves 4 bytes per element, a quarter of the decode update's 16, so its
 // arithmetic is kept lean: weights and bias are widened to floats once, the width-4 window
 // is kept as floats, and tokens go four at a time so the window slides by register
 // renaming; the next four tokens' loads are issued before the current four are computed
 // (measured on B=8, T=4096, D=4096 with SiLU: 298 us for the first version, 159 us with
 // float windows, 105 us with the loads one group ahead).
-template <int ACT>
+template <int ACT, int W>
 __global__ void __launch_bounds__(256) k_prefill_vector(UpdateParams p, PrefillParams f) {
   grid_dependency_boundary();
   const int64_t groups = p.D >> 3;
@@ -193,7 +213,7 @@ __global__ void __launch_bounds__(256) k_prefill_vector(UpdateParams p, PrefillP
   const int64_t t1 = t0 + f.chunk < f.T ? t0 + f.chunk : f.T;
 
   float wf[kW][8];  // wf[j][c] = weight[c0 + c, j]
-  load_weights_s(p, c0, wf);
+  load_weights_s<W>(p, c0, wf);
   const bool has_bias = p.bias != nullptr;
   float bf[8];
   if (has_bias) {
@@ -202,12 +222,12 @@ __global__ void __launch_bounds__(256) k_prefill_vector(UpdateParams p, PrefillP
 
   // The window before the chunk: inputs t0-3, t0-2, t0-1 (from x, or the initial state).
   float h0[8], h1[8], h2[8];
-  load_halo_s(p, f, b, c0, t0, h0, h1, h2);
+  load_halo_s<W>(p, f, b, c0, t0, h0, h1, h2);
   const uint16_t *xb = p.x + b * f.sxb + c0;
 
   auto outputs = [&](const float (&a)[8], const float (&bb)[8], const float (&cc)[8],
                      const float (&xx)[8]) -> uint4 {
-    return outputs8s<ACT>(wf, bf, has_bias, a, bb, cc, xx);
+    return outputs8s<ACT, W>(wf, bf, has_bias, a, bb, cc, xx);
   };
 
   uint16_t *ob = p.out + b * f.sob + c0;
@@ -258,7 +278,7 @@ __global__ void __launch_bounds__(256) k_prefill_vector(UpdateParams p, PrefillP
 
 // ------------------------------------------------------------------ bulk-copy prefill
 //
-// Width 4, channel-contiguous x and out. The vector kernel above keeps its next four tokens
+// Width W (2..4), channel-contiguous x and out. The vector kernel above keeps its next four tokens
 // in registers, and at 128 registers a thread only 16 warps fit on an SM: too few bytes in
 // flight for HBM. Here x travels through shared memory instead. Each warp is a pipeline over
 // a run of consecutive tokens of one sequence and 256 channels (8 per lane): lane 0 brings
@@ -331,7 +351,7 @@ struct Cursor {
 };
 static_assert(kP * 8 + 8 + sizeof(Cursor) <= kHeadBytes, "warp header too small");
 
-template <int ACT>
+template <int ACT, int W>
 __global__ void __launch_bounds__(kPThreads, 1) k_prefill_bulk(UpdateParams p, PrefillParams f) {
   grid_dependency_boundary();
   using namespace bulk;
@@ -403,10 +423,10 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_bulk(UpdateParams p, P
     const int64_t c0 = r.c_base + 8 * lane;
     if (active) {
       if (r.c_base != w_base) {
-        load_weights_f(p.w, c0, wf);
+        load_weights_f<W>(p.w, c0, wf);
         if (has_bias) widen8(ld_keep(p.bias + c0), bf);
       }
-      load_halo(p, f, r.b, c0, r.t0, h0, h1, h2);
+      load_halo<W>(p, f, r.b, c0, r.t0, h0, h1, h2);
     }
     w_base = r.c_base;
     const bool ends = f.fin != nullptr && r.t1 == f.T;
@@ -425,14 +445,14 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_bulk(UpdateParams p, P
           for (int k = 0; k < kTG; ++k) {  // unrolled: the window slides by register renaming
             float2 xk[4];
             widen8(row[k * (kRowBytes / 16)], xk);
-            st_stream(ob + k * f.sot, outputs8f<ACT>(wf, bf, has_bias, h0, h1, h2, xk));
+            st_stream(ob + k * f.sot, outputs8f<ACT, W>(wf, bf, has_bias, h0, h1, h2, xk));
             slide(h0, h1, h2, xk);
           }
         } else {
           for (int k = 0; k < (int)left; ++k) {
             float2 xk[4];
             widen8(row[k * (kRowBytes / 16)], xk);
-            st_stream(ob + k * f.sot, outputs8f<ACT>(wf, bf, has_bias, h0, h1, h2, xk));
+            st_stream(ob + k * f.sot, outputs8f<ACT, W>(wf, bf, has_bias, h0, h1, h2, xk));
             slide(h0, h1, h2, xk);
           }
         }
@@ -469,21 +489,21 @@ __global__ void __launch_bounds__(kPThreads, 1) k_prefill_bulk(UpdateParams p, P
 }
 
 constexpr int kMaxDevices = 64;
-std::atomic<bool> g_bulk_opted_in[kMaxDevices][2];
+std::atomic<bool> g_bulk_opted_in[kMaxDevices][2][kW + 1];
 
-template <int ACT>
-cudaError_t launch_prefill_bulk_act(const UpdateParams &p, PrefillParams f, cudaStream_t stream) {
+template <int ACT, int W>
+cudaError_t launch_prefill_bulk_aw(const UpdateParams &p, PrefillParams f, cudaStream_t stream) {
   const size_t smem = (size_t)kPWarps * kWarpBytes;
   const int dev = current_device();
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!g_bulk_opted_in[dev][ACT].load(std::memory_order_acquire)) {
-    cudaError_t e = cudaFuncSetAttribute(k_prefill_bulk<ACT>,
+  if (!g_bulk_opted_in[dev][ACT][W].load(std::memory_order_acquire)) {
+    cudaError_t e = cudaFuncSetAttribute(k_prefill_bulk<ACT, W>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    g_bulk_opted_in[dev][ACT].store(true, std::memory_order_release);
+    g_bulk_opted_in[dev][ACT][W].store(true, std::memory_order_release);
   }
   int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_prefill_bulk<ACT>,
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_prefill_bulk<ACT, W>,
                                                                 kPThreads, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
@@ -492,7 +512,28 @@ cudaError_t launch_prefill_bulk_act(const UpdateParams &p, PrefillParams f, cuda
   const int64_t groups = f.B * ((p.D + kRunCh - 1) / kRunCh) * ((f.T + kTG - 1) / kTG);
   int64_t grid = (groups + kPWarps - 1) / kPWarps;
   if (grid > ctas) grid = ctas;
-  return launch_overlapped(k_prefill_bulk<ACT>, dim3((unsigned)grid), dim3(kPThreads), smem, stream, p, f);
+  return launch_overlapped(k_prefill_bulk<ACT, W>, dim3((unsigned)grid), dim3(kPThreads), smem, stream, p, f);
+}
+
+template <int ACT>
+cudaError_t launch_prefill_bulk_act(const UpdateParams &p, const PrefillParams &f, cudaStream_t stream) {
+  switch (p.W) {
+    case 2: return launch_prefill_bulk_aw<ACT, 2>(p, f, stream);
+    case 3: return launch_prefill_bulk_aw<ACT, 3>(p, f, stream);
+    case 4: return launch_prefill_bulk_aw<ACT, 4>(p, f, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int ACT>
+cudaError_t launch_prefill_vector_act(const UpdateParams &p, const PrefillParams &f, dim3 grid, int threads,
+                                      cudaStream_t stream) {
+  switch (p.W) {
+    case 2: return launch_overlapped(k_prefill_vector<ACT, 2>, grid, dim3(threads), 0, stream, p, f);
+    case 3: return launch_overlapped(k_prefill_vector<ACT, 3>, grid, dim3(threads), 0, stream, p, f);
+    case 4: return launch_overlapped(k_prefill_vector<ACT, 4>, grid, dim3(threads), 0, stream, p, f);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
@@ -507,8 +548,8 @@ cudaError_t launch_prefill(const UpdateParams &p, const PrefillParams &f, int ac
     const int64_t gy = (f.T + f.chunk - 1) / f.chunk;
     if (gy > 65535 || f.B > 65535) return cudaErrorInvalidConfiguration;
     const dim3 grid((unsigned)gx, (unsigned)gy, (unsigned)f.B);
-    return act == 1 ? launch_overlapped(k_prefill_vector<1>, grid, dim3(threads), 0, stream, p, f)
-                    : launch_overlapped(k_prefill_vector<0>, grid, dim3(threads), 0, stream, p, f);
+    return act == 1 ? launch_prefill_vector_act<1>(p, f, grid, threads, stream)
+                    : launch_prefill_vector_act<0>(p, f, grid, threads, stream);
   } else {
     const int threads = 256;
     const int64_t chunks = (f.T + f.chunk - 1) / f.chunk;

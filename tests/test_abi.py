@@ -238,7 +238,7 @@ def test_every_kernel_waits_for_prior_grids_first():
 
     csrc = pathlib.Path(ROOT) / "depthwise_causal_conv1d_gb300" / "csrc"
     kernels = 0
-    for path in sorted(csrc.glob("*.cu")):
+    for path in sorted(list(csrc.glob("*.cu")) + list(csrc.glob("*.cuh"))):
         src = path.read_text()
         assert "<<<" not in src, f"{path.name}: launch outside launch_overlapped"
         for m in re.finditer(r"__global__ void[^{;]*\{", src):
