@@ -55,7 +55,7 @@ _CSRC = os.path.join(ROOT, "depthwise_causal_conv1d_gb300", "csrc")
 # workload, and the sources whose hash that capture was taken with.
 PROFILE_SUMMARIES = {
     "vector": (os.path.join(ROOT, "profiles", "update_vector_large_n4096_d16384.txt"),
-               [os.path.join(_CSRC, f) for f in ("k_vector.cu", "ccu_internal.cuh")]),
+               [os.path.join(_CSRC, f) for f in ("k_vector.cu", "ccu_vector.cuh", "ccu_internal.cuh")]),
     "bulk": (os.path.join(ROOT, "profiles", "update_bulk_large_n4096_d16384.txt"),
              [os.path.join(_CSRC, f) for f in ("k_bulk.cu", "ccu_bulk.cuh", "ccu_internal.cuh")]),
 }
