@@ -143,34 +143,31 @@ bool route_serves(int route, const Args &a, Layout layout) {
 // 27.5 us at 512).
 constexpr int64_t kBulkMinElements = 1 << 20;
 constexpr int64_t kWindowOnlyW3VectorElements = int64_t(3) << 24;
-// Above this many elements the lean vector kernel leads at L = 3, 5 and 6.
-constexpr int64_t kLeanVectorElements = int64_t(1) << 23;
 
 ccu_status_t choose(int requested, const Args &a, Layout layout, int *chosen) {
   if (requested < 0 || requested >= CCU_ROUTE_COUNT)
     return fail(CCU_ERR_INVALID_ARGUMENT, "unknown route %d", requested);
   if (requested == CCU_ROUTE_AUTO) {
     // The bulk kernel serves the linear compact state from 2^20 elements where it measured
-    // ahead of the vector kernel (D = 16384, back to back, us, bulk / vector):
-    //  - L = 3 up to 2^23 elements (N = 384: 16.2 / 17.5, N = 512: 19.9 / 20.6; but N = 256:
-    //    12.6 / 12.0), beyond it the vector kernel (N = 640: 27.0 / 25.7, N = 1024: 45.3 / 42.7,
-    //    N = 4096: 160.1 / 155.5); L = 5 and 6 likewise (N = 4096: 247.3 / 237.8 and 289.2 /
-    //    286.7);
-    //  - L = 4 and L = 7 at every size (N = 4096: 199.6 / 201.0 and 310.2 / 362.9);
-    //  - not L = 8 (N = 4096: 570.4 / 530.7; a lane's 128-byte state makes the bulk kernel's
-    //    shared-memory accesses bank-conflicted), nor L = 1, which moves 8 bytes per element,
-    //    too little per 512-channel slice (W = 2: 100.8 / 80.7);
-    //  - width 3 with L = 2 (a state of just the window) below 3 * 2^24 elements (4096 rows:
-    //    119.0 / 116.5 vector; 1024 rows: 36.8 bulk / 41.0).
-    // The ring state stays on the vector kernel at every size (compact, N = 4096: 161.5 /
-    // 158.6; N = 1024: 45.3 / 43.7; N = 256: 13.8 / 13.3), and so does the channel-last state
+    // ahead of the vector kernel (D = 16384, us, bulk / vector):
+    //  - L = 4 and L = 7 (N = 4096, back to back: 199.6 / 201.0 and 310.2 / 362.9);
+    //  - width 3 with L = 2 (a state of just the window) below 3 * 2^24 elements (back to
+    //    back, 1024 rows: 36.8 / 41.0; 4096 rows: 119.0 / 116.5).
+    // Everything else takes the vector kernel: L = 3, 5, 6 at every size (cold, on rotating
+    // copies: N = 64 6.6 / 6.0, N = 256 15.7 / 13.9, N = 512 25.9 / 23.4, N = 768 37.2 / 33.2,
+    // N = 256 at D = 8192 10.0 / 9.2; back to back the two are within 8 % from 2^20 to 2^23
+    // elements and the vector kernel leads beyond: N = 4096 160.1 / 155.5; L = 5 and 6:
+    // 247.3 / 237.8 and 289.2 / 286.7); L = 8 (570.4 / 530.7: a lane's 128-byte state makes
+    // the bulk kernel's shared-memory accesses bank-conflicted); L = 1, which moves 8 bytes
+    // per element, too little per 512-channel slice (W = 2: 100.8 / 80.7); the ring state
+    // (compact, N = 4096: 161.5 / 158.6; N = 1024: 45.3 / 43.7) and the channel-last state
     // (linear: N = 4096, 162.3 plane-bulk / 154.3; ring: the vector kernel leads from 128 rows).
     const int64_t elements = a.N * a.D;
     const bool ring = a.cache_seqlens != nullptr;
     const bool window_only_w3 = a.W == 3 && a.L == 2 && elements >= kWindowOnlyW3VectorElements;
-    const bool lean_leads = (a.L == 3 || a.L == 5 || a.L == 6) && elements > kLeanVectorElements;
+    const bool vector_leads = a.L == 3 || a.L == 5 || a.L == 6;
     const bool bulk_size = layout == Layout::Compact && !ring && elements >= kBulkMinElements && a.L >= 2 &&
-                           a.L != 8 && !window_only_w3 && !lean_leads;
+                           a.L != 8 && !window_only_w3 && !vector_leads;
     if (bulk_size && route_serves(CCU_ROUTE_BULK, a, layout)) {
       *chosen = CCU_ROUTE_BULK;
     } else if (route_serves(CCU_ROUTE_VECTOR, a, layout)) {

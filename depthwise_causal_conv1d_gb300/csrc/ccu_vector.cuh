@@ -133,13 +133,14 @@ __host__ __device__ constexpr int lean_min_ctas() {
 // 154.2 / 165.4, L = 5 237.8 / 242.1; but L = 4 211.1 / 201.0, L = 8 549.5 / 530.7 (N=64,
 // D=6144: 8.2 / 7.0), W = 2 at L = 1 88.9 / 80.4 and W = 3 at L = 2 117.5 / 116.5. The
 // second form runs at four CTAs per SM for L = 1 (64 registers), three for L = 2 (85; at
-// W = 3, L = 2: 118.6 us against 130.7 us with the compiler's budget), two up to L = 4 and
-// at the compiler's budget beyond.
+// W = 3, L = 2: 118.6 us against 130.7 us with the compiler's budget) and two beyond (128;
+// at L = 8 the compiler's budget of 181 registers left one CTA per SM: N=64, D=6144 cold
+// 7.76 against 7.13 us at two, N=4096 533.7 against 526.5 us).
 template <int L, int W, int LAYOUT, bool RING>
 __host__ __device__ constexpr VecCfg vec_cfg() {
   constexpr bool compact_linear = LAYOUT == (int)Layout::Compact && !RING;
   constexpr bool keep_regs = compact_linear && (L == 4 || L >= 8 || (L == W - 1 && W < 4));
-  if constexpr (keep_regs) return VecCfg{2, L == 1 ? 4 : (L == 2 ? 3 : (L <= 4 ? 2 : 1)), true};
+  if constexpr (keep_regs) return VecCfg{2, L == 1 ? 4 : (L == 2 ? 3 : 2), true};
   return VecCfg{1, lean_min_ctas<L, W, LAYOUT, RING>(), false};
 }
 

@@ -154,8 +154,8 @@ def test_widths_2_and_3_are_served(ccu):
     # large compact batches take the bulk kernels, compiled for widths 2 and 3 up to L = 4
     assert select(ccu, W=3, L=2, N=1024, D=16384, S=1024) == (0, 4)
     assert select(ccu, W=3, L=2, N=4096, D=16384, S=4096) == (0, 2)  # window-only state, full batch
-    assert select(ccu, W=3, L=3, N=512, D=16384, S=512) == (0, 4)
-    assert select(ccu, W=3, L=3, N=4096, D=16384, S=4096) == (0, 2)  # lean vector past 2^23
+    assert select(ccu, W=3, L=3, N=512, D=16384, S=512) == (0, 2)
+    assert select(ccu, W=3, L=3, N=4096, D=16384, S=4096) == (0, 2)
     assert select(ccu, W=2, L=2, N=4096, D=16384, S=4096) == (0, 4)
     assert select(ccu, W=2, L=4, N=4096, D=16384, S=4096) == (0, 4)
     assert select(ccu, W=2, L=1, N=4096, D=16384, S=4096) == (0, 2)  # one-entry state: vector
@@ -190,7 +190,8 @@ ROUTE_CASES = [
     ("padded ld", dict(ld=72), "vector"),
     ("large batch compact", dict(N=4096, D=16384, S=4096), "vector"),
     ("large batch compact L4", dict(N=4096, D=16384, S=4096, L=4), "bulk"),
-    ("mid batch compact", dict(N=256, D=8192, S=256), "bulk"),
+    ("mid batch compact", dict(N=256, D=8192, S=256), "vector"),
+    ("mid batch compact L7", dict(N=256, D=8192, S=256, L=7), "bulk"),
     ("below the bulk threshold", dict(N=64, D=8192, S=64), "vector"),
     ("large batch channel-last", dict(N=4096, D=16384, S=4096, stride_s=3 * 16384, stride_d=1,
                                       stride_l=16384), "vector"),
@@ -251,29 +252,27 @@ def test_every_kernel_waits_for_prior_grids_first():
 
 def test_auto_route_thresholds(ccu):
     """The AUTO route at the measured thresholds: linear compact batches take the bulk kernel
-    from 2^20 (row, channel) elements, at L = 3, 5 and 6 only up to 2^23 (the lean vector
-    kernel beyond), at L = 4 and 7 at every size, never at L = 8 or L = 1; width 3 with a
-    window-only state (L = 2) returns to the vector kernel from 3 * 2^24; the ring state and
-    the channel-last state never take the bulk kernel."""
+    from 2^20 (row, channel) elements at L = 4 and 7; L = 3, 5, 6, 8 and L = 1 stay on the
+    vector kernel at every size; width 3 with a window-only state (L = 2) takes the bulk
+    kernel from 2^20 and returns to the vector kernel from 3 * 2^24; the ring state and the
+    channel-last state never take the bulk kernel."""
     D = 16384
     below, at = (1 << 20) // D - 1, (1 << 20) // D  # 63 and 64 rows
-    assert select(ccu, N=below, S=below, D=D) == (0, 2)
-    assert select(ccu, N=at, S=at, D=D) == (0, 4)
-    lean = (1 << 23) // D  # 512 rows
-    assert select(ccu, N=lean, S=lean, D=D) == (0, 4)
-    assert select(ccu, N=lean + 1, S=lean + 1, D=D) == (0, 2)
-    assert select(ccu, N=4096, S=4096, D=D) == (0, 2)
-    for L in (5, 6):
-        assert select(ccu, N=lean, S=lean, D=D, L=L, stride_s=D * L, stride_l=1, stride_d=L) == (0, 4)
-        assert select(ccu, N=4096, S=4096, D=D, L=L, stride_s=D * L, stride_l=1, stride_d=L) == (0, 2)
+    c4 = dict(L=4, stride_s=D * 4, stride_d=4, stride_l=1)
+    assert select(ccu, N=below, S=below, D=D, **c4) == (0, 2)
+    assert select(ccu, N=at, S=at, D=D, **c4) == (0, 4)
+    for n in (below, at, 512, 513, 4096):
+        assert select(ccu, N=n, S=n, D=D) == (0, 2), n
+    for L in (5, 6, 8):
+        for n in (at, 512, 4096):
+            assert select(ccu, N=n, S=n, D=D, L=L, stride_s=D * L, stride_l=1, stride_d=L) == (0, 2), (L, n)
     for L in (4, 7):
         assert select(ccu, N=4096, S=4096, D=D, L=L, stride_s=D * L, stride_l=1, stride_d=L) == (0, 4)
-    assert select(ccu, N=4096, S=4096, D=D, L=8, stride_s=D * 8, stride_l=1, stride_d=8) == (0, 2)
     w3_below, w3_at = (3 << 24) // D - 1, (3 << 24) // D  # 3071 and 3072 rows
     assert select(ccu, N=w3_below, S=w3_below, D=D, W=3, L=2) == (0, 4)
     assert select(ccu, N=w3_at, S=w3_at, D=D, W=3, L=2) == (0, 2)
-    assert select(ccu, N=lean, S=lean, D=D, W=3, L=3) == (0, 4)
-    assert select(ccu, N=w3_at, S=w3_at, D=D, W=3, L=3) == (0, 2)  # L = 3 past 2^23: lean vector
+    assert select(ccu, N=512, S=512, D=D, W=3, L=3) == (0, 2)
+    assert select(ccu, N=w3_at, S=w3_at, D=D, W=3, L=3) == (0, 2)
     cl = dict(stride_s=3 * D, stride_d=1, stride_l=D)
     for n in (at, 1024, w3_below, 4096):
         assert select(ccu, N=n, S=n, D=D, **cl) == (0, 2), n
