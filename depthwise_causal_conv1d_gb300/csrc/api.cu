@@ -157,8 +157,9 @@ ccu_status_t choose(int requested, const Args &a, Layout layout, int *chosen) {
     // copies: N = 64 6.6 / 6.0, N = 256 15.7 / 13.9, N = 512 25.9 / 23.4, N = 768 37.2 / 33.2,
     // N = 256 at D = 8192 10.0 / 9.2; back to back the two are within 8 % from 2^20 to 2^23
     // elements and the vector kernel leads beyond: N = 4096 160.1 / 155.5; L = 5 and 6:
-    // 247.3 / 237.8 and 289.2 / 286.7); L = 8 (570.4 / 530.7: a lane's 128-byte state makes
-    // the bulk kernel's shared-memory accesses bank-conflicted); L = 1, which moves 8 bytes
+    // 247.3 / 237.8 and 289.2 / 286.7); L = 8 (570.4 / 337.1, where the vector route takes
+    // one channel per lane; a lane's 128-byte state makes the bulk kernel's shared-memory
+    // accesses bank-conflicted); L = 1, which moves 8 bytes
     // per element, too little per 512-channel slice (W = 2: 100.8 / 80.7); the ring state
     // (compact, N = 4096: 161.5 / 158.6; N = 1024: 45.3 / 43.7) and the channel-last state
     // (linear: N = 4096, 162.3 plane-bulk / 154.3; ring: the vector kernel leads from 128 rows).

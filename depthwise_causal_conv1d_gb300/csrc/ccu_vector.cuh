@@ -26,6 +26,7 @@
 namespace ccu {
 
 int device_sm_count();
+cudaError_t launch_lanes(const UpdateParams &p, int act, cudaStream_t stream);
 
 namespace {
 
@@ -130,16 +131,15 @@ __host__ __device__ constexpr int lean_min_ctas() {
 // Measured at N=4096, D=16384 (us, lean form / weights in registers with two rows in
 // flight): compact L = 3 155.6 / 162.4, compact ring L = 3 160.5 / 165.0, channel-last L = 3
 // 154.3 / 157.3, channel-last ring 125.9 / 125.2 (N=1024: 32.2 / 34.6), W = 3 at L = 3
-// 154.2 / 165.4, L = 5 237.8 / 242.1; but L = 4 211.1 / 201.0, L = 8 549.5 / 530.7 (N=64,
-// D=6144: 8.2 / 7.0), W = 2 at L = 1 88.9 / 80.4 and W = 3 at L = 2 117.5 / 116.5. The
+// 154.2 / 165.4, L = 5 237.8 / 242.1; but L = 4 211.1 / 201.0, W = 2 at L = 1 88.9 / 80.4
+// and W = 3 at L = 2 117.5 / 116.5. The
 // second form runs at four CTAs per SM for L = 1 (64 registers), three for L = 2 (85; at
-// W = 3, L = 2: 118.6 us against 130.7 us with the compiler's budget) and two beyond (128;
-// at L = 8 the compiler's budget of 181 registers left one CTA per SM: N=64, D=6144 cold
-// 7.76 against 7.13 us at two, N=4096 533.7 against 526.5 us).
+// W = 3, L = 2: 118.6 us against 130.7 us with the compiler's budget) and two at L = 4. The
+// compact linear state at L = 8 runs on neither (see launch_LW).
 template <int L, int W, int LAYOUT, bool RING>
 __host__ __device__ constexpr VecCfg vec_cfg() {
   constexpr bool compact_linear = LAYOUT == (int)Layout::Compact && !RING;
-  constexpr bool keep_regs = compact_linear && (L == 4 || L >= 8 || (L == W - 1 && W < 4));
+  constexpr bool keep_regs = compact_linear && (L == 4 || (L == W - 1 && W < 4));
   if constexpr (keep_regs) return VecCfg{2, L == 1 ? 4 : (L == 2 ? 3 : 2), true};
   return VecCfg{1, lean_min_ctas<L, W, LAYOUT, RING>(), false};
 }
@@ -417,13 +417,26 @@ cudaError_t launch_one(UpdateParams p, int64_t gx, int threads, cudaStream_t str
                            dim3(threads), 0, stream, p);
 }
 
+// The linear compact states that run one channel per lane (k_lanes.cu) instead: L = 8
+// (N=4096, D=16384: 337.1 us, 1.007 of the copy rate, against 527.2 us on this family, where
+// each 16-byte access of a lane's 128-byte state costs its own L1 wavefront; N=64, D=6144
+// cold 5.0 against 7.1 us).
+template <int L, int W>
+__host__ __device__ constexpr bool lanes_form() {
+  return L == 8;
+}
+
 template <int L, int W, int ACT, bool DEDUP>
 cudaError_t launch_LW(const UpdateParams &p, int64_t gx, int threads, cudaStream_t stream) {
   const bool ring = p.seqlens != nullptr;
   constexpr int kC = (int)Layout::Compact, kCL = (int)Layout::ChannelLast;
   if (p.layout == kC) {
-    return ring ? launch_one<L, W, ACT, kC, true, DEDUP>(p, gx, threads, stream)
-                : launch_one<L, W, ACT, kC, false, DEDUP>(p, gx, threads, stream);
+    if constexpr (lanes_form<L, W>()) {
+      return ring ? launch_one<L, W, ACT, kC, true, DEDUP>(p, gx, threads, stream) : launch_lanes(p, ACT, stream);
+    } else {
+      return ring ? launch_one<L, W, ACT, kC, true, DEDUP>(p, gx, threads, stream)
+                  : launch_one<L, W, ACT, kC, false, DEDUP>(p, gx, threads, stream);
+    }
   }
   return ring ? launch_one<L, W, ACT, kCL, true, DEDUP>(p, gx, threads, stream)
               : launch_one<L, W, ACT, kCL, false, DEDUP>(p, gx, threads, stream);

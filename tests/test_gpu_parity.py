@@ -495,6 +495,41 @@ def test_checked_update_detects_duplicates_in_the_same_launch(route, layout, cas
     assert_parity(inp, got_out, got_state, want_out, want_state, f"dedup {route} {layout} {case}")
 
 
+@pytest.mark.parametrize("case", ["duplicate", "both"])
+@pytest.mark.parametrize("route,W", [("vector", 2), ("vector", 3), ("vector", 4), ("bulk", 4)])
+def test_checked_update_detects_duplicates_at_l8(route, W, case):
+    """The duplicate check at L = 8, where the vector route runs one channel per lane: as
+    test_checked_update_detects_duplicates_in_the_same_launch, on a ragged D (not a multiple
+    of the 2048 channels a CTA covers) and a padded x row stride."""
+    wl = synthetic.variant(synthetic.WORKLOADS["strided_n64_d6144_ld6152_l8_perm_identity"], name="dedup8",
+                           N=40, D=2056, ld=2064, S=64, W=W, indices="distinct_pad", pad_frac=0.1,
+                           act="silu", bias_std=0.1)
+    inp = synthetic.generate(wl, seed=71 + W)
+    idx = inp.indices.copy()
+    active = np.flatnonzero(idx >= 0)
+    groups = [[active[2], active[17], active[30]], [active[5], active[6]]]
+    for g in groups:
+        idx[g] = idx[g[0]]
+    if case == "both":
+        idx[active[9]] = -2
+        idx[active[12]] = wl.S
+    want_status = oracle.check_indices(idx, wl.N, wl.S)
+    scratch = torch.full((wl.S,), 12345, dtype=torch.int32, device=DEV)
+    got_out, got_state, status, ok = run_gpu(dataclasses.replace(inp, indices=idx), route=route, checked=True,
+                                             slot_scratch=scratch)
+    assert ok, "a guard band was overwritten"
+    assert status == want_status, (status, want_status)
+    owners = scratch.cpu().numpy()
+    ref_idx = idx.copy()
+    ref_idx[(idx < -1) | (idx >= wl.S)] = -1
+    for g in groups:
+        winner = owners[idx[g[0]]] - 1
+        assert winner in g, (winner, g)
+        ref_idx[[r for r in g if r != winner]] = -1
+    want_out, want_state = oracle_ref(dataclasses.replace(inp, indices=ref_idx))
+    assert_parity(inp, got_out, got_state, want_out, want_state, f"dedup L8 {route} {case} W{W}")
+
+
 @pytest.mark.parametrize("layout", ["compact", "channel_last"])
 @pytest.mark.parametrize("route", ["vector", "bulk"])
 def test_large_batch_routes_agree_bitwise(route, layout):
