@@ -150,7 +150,9 @@ ccu_status_t choose(int requested, const Args &a, Layout layout, int *chosen) {
   if (requested == CCU_ROUTE_AUTO) {
     // The bulk kernel serves the linear compact state from 2^20 elements where it measured
     // ahead of the vector kernel (D = 16384, us, bulk / vector):
-    //  - L = 4 and L = 7 (N = 4096, back to back: 199.6 / 201.0 and 310.2 / 362.9);
+    //  - L = 7 (N = 4096, back to back: 310.2 / 362.9), and L = 4 at widths 2 and 3 (width 3:
+    //    199.9 / 203.2); width 4 at L = 4 takes the vector route's one-channel-per-lane kernel
+    //    (cold, N = 1024: 56.8 / 53.5; back to back at N = 4096 199.0 / 200.6);
     //  - width 3 with L = 2 (a state of just the window) below 3 * 2^24 elements (back to
     //    back, 1024 rows: 36.8 / 41.0; 4096 rows: 119.0 / 116.5).
     // Everything else takes the vector kernel: L = 3, 5, 6 at every size (cold, on rotating
@@ -166,7 +168,7 @@ ccu_status_t choose(int requested, const Args &a, Layout layout, int *chosen) {
     const int64_t elements = a.N * a.D;
     const bool ring = a.cache_seqlens != nullptr;
     const bool window_only_w3 = a.W == 3 && a.L == 2 && elements >= kWindowOnlyW3VectorElements;
-    const bool vector_leads = a.L == 3 || a.L == 5 || a.L == 6;
+    const bool vector_leads = a.L == 3 || a.L == 5 || a.L == 6 || (a.L == 4 && a.W == kW);
     const bool bulk_size = layout == Layout::Compact && !ring && elements >= kBulkMinElements && a.L >= 2 &&
                            a.L != 8 && !window_only_w3 && !vector_leads;
     if (bulk_size && route_serves(CCU_ROUTE_BULK, a, layout)) {

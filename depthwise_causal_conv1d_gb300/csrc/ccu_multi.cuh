@@ -182,7 +182,11 @@ __global__ void __launch_bounds__(256, 2) k_multi_vector(UpdateParams p, MultiPa
 
 // L = 7 and 8: one row in flight and the compiler's register budget (the two-row form
 // spills 300-600 bytes there under the cap; N=1024, D=16384, T=4: L = 7 148.3 against
-// 192.8 us, L = 8 144.7 against 206.9 us).
+// 192.8 us, L = 8 144.7 against 206.9 us). One channel per lane, as the single-token
+// update runs L = 8, lost here (each lane stepping 8 channels' states through the tokens,
+// four tokens' inputs loaded ahead): L = 8 took 165.7 against 144.2 us and L = 4 138.8
+// against 90.2 us (T = 8, L = 8: 262.9 against 187.3 us); only T = 1 was faster (99.7
+// against 131.3 us), and a single token goes through the update itself.
 template <int L, int W, int ACT, int LAYOUT, bool RING>
 __global__ void __launch_bounds__(256) k_multi_vector_long(UpdateParams p, MultiParams m) {
   grid_dependency_boundary();

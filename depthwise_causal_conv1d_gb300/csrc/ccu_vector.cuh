@@ -144,8 +144,9 @@ __host__ __device__ constexpr VecCfg vec_cfg() {
   return VecCfg{1, lean_min_ctas<L, W, LAYOUT, RING>(), false};
 }
 
-// The lean form: weights and bias from the CTA's shared-memory tables.
-template <int L, int W, int ACT, int LAYOUT, bool RING, bool DEDUP>
+// The lean form: weights and bias from the CTA's shared-memory tables. TWO_ROWS: two rows'
+// loads in flight per thread (the small-batch form, see launch_one).
+template <int L, int W, int ACT, int LAYOUT, bool RING, bool DEDUP, bool TWO_ROWS>
 __device__ __forceinline__ void update_vector(const UpdateParams &p, PairTables &tab) {
   constexpr VecCfg cfg = vec_cfg<L, W, LAYOUT, RING>();
   const int t = threadIdx.x;
@@ -289,7 +290,7 @@ __device__ __forceinline__ void update_vector(const UpdateParams &p, PairTables 
 
   // A CTA walks R consecutive rows (rows_per_cta), rif rows' loads in flight per thread.
   // Slots are unique within a call, so one row's stores never touch another row's state.
-  constexpr int RIF = cfg.rif;
+  constexpr int RIF = TWO_ROWS ? 2 : cfg.rif;
   const int64_t R = p.rows_per_cta;
   for (int64_t r0 = (int64_t)blockIdx.y * R; r0 < p.N; r0 += (int64_t)gridDim.y * R) {
     const int64_t r1 = r0 + R < p.N ? r0 + R : p.N;
@@ -371,22 +372,31 @@ __device__ __forceinline__ void update_vector_regs(const UpdateParams &p) {
 
 // The duplicate check's warp-wide claim needs a few more registers: its instances are
 // budgeted for one resident CTA fewer (at the lean form's budget they spilled up to 56 bytes).
-template <int L, int W, bool DEDUP, int LAYOUT, bool RING>
+// The two-rows-in-flight lean form holds a second row's x and state: four CTAs per SM.
+template <int L, int W, bool DEDUP, int LAYOUT, bool RING, bool TWO_ROWS>
 __host__ __device__ constexpr int kernel_min_ctas() {
-  constexpr int m = vec_cfg<L, W, LAYOUT, RING>().minb;
+  constexpr int m = TWO_ROWS ? 4 : vec_cfg<L, W, LAYOUT, RING>().minb;
   return (DEDUP && m > 1) ? m - 1 : m;
 }
 
-template <int L, int W, int ACT, int LAYOUT, bool RING, bool DEDUP>
-__global__ void __launch_bounds__(kThreads, kernel_min_ctas<L, W, DEDUP, LAYOUT, RING>())
+template <int L, int W, int ACT, int LAYOUT, bool RING, bool DEDUP, bool TWO_ROWS>
+__global__ void __launch_bounds__(kThreads, kernel_min_ctas<L, W, DEDUP, LAYOUT, RING, TWO_ROWS>())
     k_update_vector(UpdateParams p) {
   grid_dependency_boundary();
   if constexpr (vec_cfg<L, W, LAYOUT, RING>().wreg) {
     update_vector_regs<L, W, ACT, DEDUP>(p);
   } else {
     __shared__ PairTables tab;
-    update_vector<L, W, ACT, LAYOUT, RING, DEDUP>(p, tab);
+    update_vector<L, W, ACT, LAYOUT, RING, DEDUP, TWO_ROWS>(p, tab);
   }
+}
+
+// The small-batch two-row form is built for the compact linear state at L = 3, width 4 (at
+// widths 2 and 3 it measured 2 % slower: N=256, D=8192 cold 8.18 / 8.30 against 7.98 / 8.11
+// us).
+template <int L, int W, int LAYOUT, bool RING>
+__host__ __device__ constexpr bool two_row_form() {
+  return L == 3 && W == 4 && LAYOUT == (int)Layout::Compact && !RING && !vec_cfg<L, W, LAYOUT, RING>().wreg;
 }
 
 // Rows per CTA once the batch fills the GPU. Lean form: enough that the weights a CTA
@@ -407,23 +417,41 @@ cudaError_t launch_one(UpdateParams p, int64_t gx, int threads, cudaStream_t str
     if (R < 4) R = work >= 4 * 2 * sms ? 4 : 1;
   } else {
     // Small batches take one row per CTA: every (row, channel block) is a CTA of its own.
+    // From six to eight (row, channel block) pairs per SM, the compact linear L = 3 state
+    // takes two rows per CTA, both in flight, at four CTAs per SM: one wave instead of a
+    // wave and a ragged second at five one-row CTAs per SM (cold, us, two rows / one row: N=256,
+    // D=8192 8.51 / 9.21; N=300, D=8192 9.01 / 10.14; N=128, D=16384 8.55 / 9.09; but N=192,
+    // D=8192, where one-row CTAs fit one wave, 8.16 / 7.32).
     constexpr int64_t kRows = (RING && LAYOUT == (int)Layout::Compact) ? 4 : 3;
     R = work >= 8 * sms ? kRows : 1;
+    if constexpr (two_row_form<L, W, LAYOUT, RING>()) {
+      if (R == 1 && work >= 6 * sms) {
+        int64_t gy = (p.N + 1) / 2;
+        if (gy > 65535) gy = 65535;
+        p.rows_per_cta = 2;
+        return launch_overlapped(k_update_vector<L, W, ACT, LAYOUT, RING, DEDUP, true>,
+                                 dim3((unsigned)gx, (unsigned)gy), dim3(threads), 0, stream, p);
+      }
+    }
   }
   int64_t gy = (p.N + R - 1) / R;
   if (gy > 65535) gy = 65535;  // the row loop strides over the rest
   p.rows_per_cta = (int)R;
-  return launch_overlapped(k_update_vector<L, W, ACT, LAYOUT, RING, DEDUP>, dim3((unsigned)gx, (unsigned)gy),
-                           dim3(threads), 0, stream, p);
+  return launch_overlapped(k_update_vector<L, W, ACT, LAYOUT, RING, DEDUP, false>,
+                           dim3((unsigned)gx, (unsigned)gy), dim3(threads), 0, stream, p);
 }
 
 // The linear compact states that run one channel per lane (k_lanes.cu) instead: L = 8
 // (N=4096, D=16384: 337.1 us, 1.007 of the copy rate, against 527.2 us on this family, where
 // each 16-byte access of a lane's 128-byte state costs its own L1 wavefront; N=64, D=6144
-// cold 5.0 against 7.1 us).
+// cold 5.0 against 7.1 us) and width 4 at L = 4 (cold, N=1024: 53.5 against 56.1 us, and
+// 56.8 on the bulk kernel; N=256, D=8192: 10.1 against 11.4 and 12.6; back to back at
+// N=4096 200.6 against 202.9 and 199.0). Widths 3 at L = 4 (212.7 against 203.2 us), and
+// L = 1 and 2, whose 2- and 4-byte states make many small accesses (W = 2, L = 1: 115.4
+// against 80.6 us), stay here.
 template <int L, int W>
 __host__ __device__ constexpr bool lanes_form() {
-  return L == 8;
+  return L == 8 || (L == 4 && W == 4);
 }
 
 template <int L, int W, int ACT, bool DEDUP>

@@ -189,7 +189,8 @@ ROUTE_CASES = [
     ("channel-last L12", dict(L=12, stride_s=768, stride_d=1, stride_l=64), "staged"),
     ("padded ld", dict(ld=72), "vector"),
     ("large batch compact", dict(N=4096, D=16384, S=4096), "vector"),
-    ("large batch compact L4", dict(N=4096, D=16384, S=4096, L=4), "bulk"),
+    ("large batch compact L4", dict(N=4096, D=16384, S=4096, L=4), "vector"),
+    ("large batch compact L7", dict(N=4096, D=16384, S=4096, L=7), "bulk"),
     ("mid batch compact", dict(N=256, D=8192, S=256), "vector"),
     ("mid batch compact L7", dict(N=256, D=8192, S=256, L=7), "bulk"),
     ("below the bulk threshold", dict(N=64, D=8192, S=64), "vector"),
@@ -252,22 +253,23 @@ def test_every_kernel_waits_for_prior_grids_first():
 
 def test_auto_route_thresholds(ccu):
     """The AUTO route at the measured thresholds: linear compact batches take the bulk kernel
-    from 2^20 (row, channel) elements at L = 4 and 7; L = 3, 5, 6, 8 and L = 1 stay on the
-    vector kernel at every size; width 3 with a window-only state (L = 2) takes the bulk
+    from 2^20 (row, channel) elements at L = 7 and at L = 4 for widths 2 and 3; L = 3, 5, 6, 8,
+    L = 1 and width 4 at L = 4 stay on the vector route at every size; width 3 with a window-only state (L = 2) takes the bulk
     kernel from 2^20 and returns to the vector kernel from 3 * 2^24; the ring state and the
     channel-last state never take the bulk kernel."""
     D = 16384
     below, at = (1 << 20) // D - 1, (1 << 20) // D  # 63 and 64 rows
-    c4 = dict(L=4, stride_s=D * 4, stride_d=4, stride_l=1)
-    assert select(ccu, N=below, S=below, D=D, **c4) == (0, 2)
-    assert select(ccu, N=at, S=at, D=D, **c4) == (0, 4)
+    c7 = dict(L=7, stride_s=D * 7, stride_d=7, stride_l=1)
+    assert select(ccu, N=below, S=below, D=D, **c7) == (0, 2)
+    assert select(ccu, N=at, S=at, D=D, **c7) == (0, 4)
     for n in (below, at, 512, 513, 4096):
         assert select(ccu, N=n, S=n, D=D) == (0, 2), n
     for L in (5, 6, 8):
         for n in (at, 512, 4096):
             assert select(ccu, N=n, S=n, D=D, L=L, stride_s=D * L, stride_l=1, stride_d=L) == (0, 2), (L, n)
-    for L in (4, 7):
-        assert select(ccu, N=4096, S=4096, D=D, L=L, stride_s=D * L, stride_l=1, stride_d=L) == (0, 4)
+    assert select(ccu, N=4096, S=4096, D=D, L=7, stride_s=D * 7, stride_l=1, stride_d=7) == (0, 4)
+    assert select(ccu, N=4096, S=4096, D=D, L=4, stride_s=D * 4, stride_l=1, stride_d=4) == (0, 2)
+    assert select(ccu, N=4096, S=4096, D=D, W=3, L=4, stride_s=D * 4, stride_l=1, stride_d=4) == (0, 4)
     w3_below, w3_at = (3 << 24) // D - 1, (3 << 24) // D  # 3071 and 3072 rows
     assert select(ccu, N=w3_below, S=w3_below, D=D, W=3, L=2) == (0, 4)
     assert select(ccu, N=w3_at, S=w3_at, D=D, W=3, L=2) == (0, 2)

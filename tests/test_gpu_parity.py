@@ -530,6 +530,46 @@ def test_checked_update_detects_duplicates_at_l8(route, W, case):
     assert_parity(inp, got_out, got_state, want_out, want_state, f"dedup L8 {route} {case} W{W}")
 
 
+def _two_row_batch():
+    """A row count at which the vector route's small-batch two-row form runs at D = 8192
+    (1024 channels per CTA): between six and eight (row, channel block) pairs per SM, odd,
+    so the last CTA holds one row."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return (7 * sms) // 4 | 1
+
+
+@pytest.mark.parametrize("case", ["unchecked", "duplicate"])
+def test_small_batch_two_row_form(case):
+    """The two-rows-in-flight form of the vector kernel (compact linear L = 3, width 4, small
+    batches): bit-exact state and 1-ulp outputs against the oracle with padding rows, and in
+    the checked update the duplicate check of test_checked_update_detects_duplicates_in_the_same_launch."""
+    N = _two_row_batch()
+    wl = synthetic.variant(synthetic.WORKLOADS["paged_n256_d8192_l3_s1024_pad10_silu"], name="two_row", N=N)
+    inp = synthetic.generate(wl, seed=91)
+    if case == "unchecked":
+        _check(inp, route="vector", what=f"two-row N={N}")
+        return
+    idx = inp.indices.copy()
+    active = np.flatnonzero(idx >= 0)
+    groups = [[active[3], active[len(active) // 2], active[-1]], [active[7], active[8]]]
+    for g in groups:
+        idx[g] = idx[g[0]]
+    want_status = oracle.check_indices(idx, wl.N, wl.S)
+    scratch = torch.full((wl.S,), 12345, dtype=torch.int32, device=DEV)
+    got_out, got_state, status, ok = run_gpu(dataclasses.replace(inp, indices=idx), route="vector", checked=True,
+                                             slot_scratch=scratch)
+    assert ok, "a guard band was overwritten"
+    assert status == want_status, (status, want_status)
+    owners = scratch.cpu().numpy()
+    ref_idx = idx.copy()
+    for g in groups:
+        winner = owners[idx[g[0]]] - 1
+        assert winner in g, (winner, g)
+        ref_idx[[r for r in g if r != winner]] = -1
+    want_out, want_state = oracle_ref(dataclasses.replace(inp, indices=ref_idx))
+    assert_parity(inp, got_out, got_state, want_out, want_state, f"two-row dedup N={N}")
+
+
 @pytest.mark.parametrize("layout", ["compact", "channel_last"])
 @pytest.mark.parametrize("route", ["vector", "bulk"])
 def test_large_batch_routes_agree_bitwise(route, layout):
