@@ -115,14 +115,28 @@ cudaError_t launch_multi_scalar(const UpdateParams &p, const MultiParams &m, int
                   : launch_overlapped(k_multi_scalar<0>, grid, block, 0, stream, p, m);
 }
 
+// CTAs per SM the grid is sized for: one wave (two per SM, each CTA walking its rows two at
+// a time) where that measured faster, four waves elsewhere. N=1024, D=16384, T=4, us, one
+// wave / four waves: L = 3 77.8 / 81.4 (T = 1 45.8 / 48.7, T = 8 136.2 / 138.1; N=256 20.2 /
+// 22.1; N=128 11.4 / 13.6), L = 4 85.8 / 89.0, L = 6 113.2 / 116.0, L = 7 141.1 / 148.5,
+// L = 8 142.0 / 144.2, channel-last L = 3 86.1 / 87.0 and L = 7 137.7 / 141.0; but L = 5 111.9
+// / 107.6 (channel-last 110.2 / 108.3), channel-last L = 8 123.3 / 120.3 and the compact
+// ring at L = 8 172.4 / 165.5 (others within 1 %). A form that kept each thread's next rows
+// in flight in shared memory (cp.async, three rows ahead, one wave) measured 83.3 at L = 3,
+// 100.4 at L = 4 and 183.9 at L = 8.
+static int multi_grid_ctas_per_sm(const UpdateParams &p) {
+  const bool four_waves =
+      p.L == 5 || (p.L == 8 && (p.layout == (int)Layout::ChannelLast || p.seqlens != nullptr));
+  return four_waves ? 8 : 2;
+}
+
 cudaError_t launch_multi_vector(const UpdateParams &p, const MultiParams &m, int act,
                                 cudaStream_t stream) {
   const int64_t groups = p.D / 8;
   int threads = 256;
   if (groups < threads) threads = (int)((groups + 31) / 32 * 32);
   const int64_t gx = (groups + threads - 1) / threads;
-  // one row per CTA row-step: each row already carries T tokens of work
-  int64_t gy = (int64_t)device_sm_count() * 8 / gx;
+  int64_t gy = (int64_t)device_sm_count() * multi_grid_ctas_per_sm(p) / gx;
   if (gy < 1) gy = 1;
   if (gy > p.N) gy = p.N;
   if (gy > 65535) gy = 65535;

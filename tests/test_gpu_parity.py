@@ -835,6 +835,25 @@ def _check_multi(case, route, layout, seed):
     assert bf16_ulp_distance(got_out, want_out).max() <= 1, "outputs"
 
 
+# The vector multi-token kernel runs one wave of CTAs, each walking many rows two at a time:
+# rows enough for several turns of that loop (and an odd count per CTA), more than four
+# tokens (the later ones loaded per group of four), ragged D (CTAs with idle threads) and
+# intermediate states, in both layouts.
+MULTI_MANY_ROWS = [
+    dict(N=1200, D=264, T=6, L=3, S=1300, ring=False, x_layout="tokens_major"),
+    dict(N=900, D=264, T=4, L=5, S=901, ring=False, x_layout="tokens_major"),
+    dict(N=700, D=2056, T=3, L=8, S=700, ring=False, x_layout="tokens_major"),
+    dict(N=640, D=520, T=1, L=4, S=640, ring=False, x_layout="tokens_major"),
+]
+
+
+@pytest.mark.parametrize("route", ["auto", "vector"])
+@pytest.mark.parametrize("layout", ["compact", "channel_last"])
+@pytest.mark.parametrize("ci", range(len(MULTI_MANY_ROWS)))
+def test_multi_token_many_rows_per_cta(route, layout, ci):
+    _check_multi(MULTI_MANY_ROWS[ci], route, layout, 500 + ci)
+
+
 @pytest.mark.parametrize("route", ["auto", "vector"])
 def test_multi_large_batch(route):
     """A large multi-token batch (N=1024, D=16384, T=4, ring state)."""
