@@ -139,7 +139,7 @@ typedef enum ccu_route {
  *               layout for a ring: there a step reads the W - 1 window planes and writes one
  *               plane, so it moves 12 bytes per element at W = 4; in the compact layout the
  *               L entries of a channel share their 32-byte sectors, so the whole slab is read
- *               and written, 16 bytes per element at L = 3 (large batch: 124 against 158 us).
+ *               and written, 16 bytes per element at L = 3 (large batch: 118 against 157 us).
  *   N, D, S     rows, channels, cache slots. N == 0 or D == 0 is a no-op.
  *   L, W        state length and filter width, L >= W - 1. Served: W = 2, 3 or 4 (the page's
  *               native width is 4; it names other widths as semantically valid), any L.

@@ -326,6 +326,67 @@ def test_cuda_graph_replay_matches_eager():
     assert torch.equal(eager_state.view(torch.int16), st.view(torch.int16))
 
 
+def test_cuda_graph_checked_update_with_duplicates():
+    """The range- and duplicate-checked update captured in a CUDA graph: the clearing of the
+    slot scratch is part of the captured work, so every replay finds the duplicate and the
+    out-of-range row from a dirty scratch, and its status, outputs and state equal the
+    oracle's update with the losing row (read back from the scratch) as padding."""
+    import depthwise_causal_conv1d_gb300 as ccu
+
+    wl = synthetic.variant(synthetic.WORKLOADS["paged_n256_d8192_l3_s1024_pad10_silu"], name="graph_dedup",
+                           N=96, D=2048, ld=2048, S=128)
+    inp = synthetic.generate(wl, seed=17)
+    idx = inp.indices.copy()
+    active = np.flatnonzero(idx >= 0)
+    pair = [active[4], active[40]]
+    idx[pair[0]] = idx[pair[1]]  # a repeated slot
+    idx[active[7]] = wl.S  # out of range
+    want_status = oracle.check_indices(idx, wl.N, wl.S)
+
+    x = to_dev_u16(inp.x, DEV)[:, :wl.D]
+    w = to_dev_u16(inp.weight, DEV)
+    b = to_dev_u16(inp.bias, DEV)
+    idx_dev = torch.from_numpy(idx).to(DEV)
+    st0 = to_dev_u16(inp.conv_state, DEV)
+    state = st0.clone()
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    scratch = torch.full((wl.S,), 7, dtype=torch.int32, device=DEV)
+    out = torch.empty((wl.N, wl.D), dtype=torch.bfloat16, device=DEV)
+
+    def run():
+        ccu.causal_conv1d_update(x, state, w, b, "silu", conv_state_indices=idx_dev, out=out, status=status,
+                                 slot_scratch=scratch)
+
+    def check(what):
+        assert int(status.item()) == want_status, what
+        owners = scratch.cpu().numpy()
+        winner = owners[idx[pair[0]]] - 1
+        assert winner in pair, (what, winner)
+        ref_idx = idx.copy()
+        ref_idx[idx >= wl.S] = -1
+        ref_idx[[r for r in pair if r != winner]] = -1
+        want_out, want_state = oracle_ref(dataclasses.replace(inp, indices=ref_idx))
+        assert_parity(inp, from_dev_u16(out), from_dev_u16(state), want_out, want_state, what)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # the eager call, which also warms the signature before capture
+        run()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    check("eager")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run()
+    for k in range(3):
+        state.copy_(st0)
+        status.zero_()
+        scratch.fill_(7)  # dirty scratch: the captured clear must run
+        g.replay()
+        torch.cuda.synchronize()
+        check(f"replay {k}")
+
+
 def test_cuda_graph_prefill_multi_decode_sequence():
     """One CUDA graph holding a serving sequence on one state: a bulk prefill that writes the
     channel-last hand-off state, a multi-token update and a (bulk) decode step. Every replay
@@ -690,6 +751,40 @@ def _check_ring(inp, seq, layout="compact", route="auto", what=""):
     got_out, got_state, _, ok = run_gpu(inp, layout, route, cache_seqlens=seq)
     assert ok, f"{what}: a guard band was overwritten"
     assert_parity(inp, got_out, got_state, want_out, want_state, what)
+
+
+@pytest.mark.parametrize("case", ["unchecked", "duplicate"])
+@pytest.mark.parametrize("N", [401, 4900])
+def test_ring_channel_last_two_rows(N, case):
+    """The channel-last ring state on the vector kernel once the batch fills the GPU: two
+    rows in flight, four (N=401) or six (N=4900) rows per CTA, a ragged last CTA and a ragged
+    D; bit-exact state and 1-ulp outputs, and with the duplicate check the losing rows as
+    padding."""
+    wl = synthetic.variant(synthetic.RING_WORKLOADS["large_n4096_d16384_l3_perm_pad5_silu_ring_chlast"],
+                           name="ring_chlast_two_rows", N=N, S=N + 3, D=6408, ld=6408,
+                           indices="distinct_pad")
+    inp = synthetic.generate(wl, seed=61)
+    seq = ring_seqlens(np.random.default_rng(62), inp)
+    if case == "unchecked":
+        _check_ring(inp, seq, layout="channel_last", route="vector", what=f"ring chlast two rows N={N}")
+        return
+    idx = inp.indices.copy()
+    active = np.flatnonzero(idx >= 0)
+    pair = [active[3], active[len(active) // 2]]
+    idx[pair[0]] = idx[pair[1]]
+    inp = dataclasses.replace(inp, indices=idx)
+    seq[pair[0]] = seq[pair[1]]
+    scratch = torch.full((wl.S,), 9, dtype=torch.int32, device=DEV)
+    got_out, got_state, status, ok = run_gpu(inp, "channel_last", "vector", checked=True, cache_seqlens=seq,
+                                             slot_scratch=scratch)
+    assert ok, "a guard band was overwritten"
+    assert status == oracle.check_indices(idx, wl.N, wl.S)
+    winner = scratch.cpu().numpy()[idx[pair[0]]] - 1
+    assert winner in pair
+    ref_idx = idx.copy()
+    ref_idx[[r for r in pair if r != winner]] = -1
+    want_out, want_state = oracle_ref(dataclasses.replace(inp, indices=ref_idx), "channel_last", cache_seqlens=seq)
+    assert_parity(inp, got_out, got_state, want_out, want_state, f"ring chlast two rows dedup N={N}")
 
 
 @pytest.mark.parametrize("route", ["scalar", "vector", "staged", "bulk"])
