@@ -241,7 +241,7 @@ ccu_status_t run(const Args &a, int route, cudaStream_t stream) {
   p.rows_per_cta = 1;
 
   cudaError_t e = cudaSuccess;
-  if (p.owner != nullptr && a.S > 0) e = cudaMemsetAsync(p.owner, 0, (size_t)a.S * sizeof(int32_t), stream);
+  if (p.owner != nullptr && a.S > 0) e = launch_clear_words(p.owner, a.S, stream);
   if (e != cudaSuccess)
     return fail(CCU_ERR_CUDA, "clearing slot_scratch failed: %s", cudaGetErrorString(e));
   e = cudaErrorInvalidValue;

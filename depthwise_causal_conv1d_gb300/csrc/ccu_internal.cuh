@@ -533,6 +533,8 @@ cudaError_t launch_prefill(const UpdateParams &p, const PrefillParams &f, int ac
 cudaError_t launch_prefill_bulk(const UpdateParams &p, const PrefillParams &f, int act,
                                 cudaStream_t stream);
 cudaError_t take_prefill_error(int32_t *bits);
+// Zeroes n words on the stream as a kernel in the overlapped launch sequence (k_scalar.cu).
+cudaError_t launch_clear_words(int32_t *w, int64_t n, cudaStream_t stream);
 cudaError_t launch_check_indices(const int32_t *idx, int64_t N, int64_t S, uint32_t *bitmap,
                                  int32_t *status, cudaStream_t stream);
 

@@ -71,6 +71,16 @@ __global__ void __launch_bounds__(256) k_check_indices(const int32_t *idx, int64
   }
 }
 
+// Zeroes n 32-bit words (the duplicate check's slot scratch). A kernel rather than a
+// memset so that it joins the programmatic overlap of consecutive launches: it waits, at its
+// boundary, for the previous kernel on the stream (which may still read the scratch), and
+// the update launched after it waits for it in the same way.
+__global__ void __launch_bounds__(256) k_clear_words(int32_t *w, int64_t n) {
+  grid_dependency_boundary();
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    w[i] = 0;
+}
+
 int64_t grid_for(int64_t work, int threads) {
   const int64_t blocks = (work + threads - 1) / threads;
   const int64_t cap = (int64_t)device_sm_count() * 16;
@@ -84,6 +94,12 @@ cudaError_t launch_scalar(const UpdateParams &p, int act, cudaStream_t stream) {
   const dim3 grid((unsigned)grid_for(p.N * p.D, threads));
   return act == 1 ? launch_overlapped(k_update_scalar<1>, grid, dim3(threads), 0, stream, p)
                   : launch_overlapped(k_update_scalar<0>, grid, dim3(threads), 0, stream, p);
+}
+
+cudaError_t launch_clear_words(int32_t *w, int64_t n, cudaStream_t stream) {
+  const int threads = 256;
+  const dim3 grid((unsigned)grid_for(n, threads));
+  return launch_overlapped(k_clear_words, grid, dim3(threads), 0, stream, w, n);
 }
 
 cudaError_t launch_check_indices(const int32_t *idx, int64_t N, int64_t S, uint32_t *bitmap,
