@@ -397,7 +397,7 @@ def causal_conv1d_fwd(x, weight, bias=None, activation=None, *, initial_states=N
 
     Returns ``out`` [B, D, T] (laid out like ``x``) and, when ``return_final_states`` or
     ``final_states_out`` is given, the final state [B, D, L]: the last L inputs, by default
-    L = W - 1 in the channel-last layout (strides (L*D, 1, D)) that the decode update
+    L = max(W - 1, 1) in the channel-last layout (strides (L*D, 1, D)) that the decode update
     accepts without a copy. ``initial_states`` [B, D, L] (any strides) holds the inputs
     before the sequence (zeros when None).
     """
@@ -419,7 +419,8 @@ def causal_conv1d_fwd(x, weight, bias=None, activation=None, *, initial_states=N
         _check_tensor("bias", bias, torch.bfloat16, torch)
         if bias.shape != (D,) or not bias.is_contiguous():
             raise ValueError("bias must be a contiguous [D] tensor")
-    L = final_state_len if final_state_len is not None else W - 1
+    # the shortest state the width allows (a width-1 filter still keeps one entry)
+    L = final_state_len if final_state_len is not None else max(W - 1, 1)
     if initial_states is not None:
         _check_tensor("initial_states", initial_states, torch.bfloat16, torch)
         if initial_states.dim() != 3 or initial_states.shape[:2] != (B, D):

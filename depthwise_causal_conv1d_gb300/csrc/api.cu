@@ -3,8 +3,9 @@
 // The contract checked here is the one of the cuDNN page "Causal Conv1d Decode Update":
 // "Semantic tensor contract" (shapes, ld rule, L >= W - 1, the two state layouts) and
 // "Current native implementation" (16-byte pointer alignment for BF16 tensors, 4 bytes
-// for indices; widths 2 and 3 and the multi-token, ring-buffer and prefill forms the page
-// names but does not serve are served here too). The declines follow the
+// for indices). Widths other than 4 (any W >= 1 with L >= 1) and the multi-token,
+// ring-buffer and prefill forms, which the page names but does not serve, are served here
+// too. The declines follow the
 // cuDNN page "Composing multi-kernel blocks", section "The shape of a block": a contract
 // violation is CCU_ERR_INVALID_ARGUMENT, a valid but unserved request
 // CCU_ERR_NOT_IMPLEMENTED, and nothing is launched or changed in either case.
@@ -66,9 +67,9 @@ ccu_status_t validate(const Args &a, bool *noop, Layout *layout) {
   if (a.L < a.W - 1)
     return fail(CCU_ERR_INVALID_ARGUMENT, "L must be >= W - 1 (L=%lld, W=%lld)", (long long)a.L,
                 (long long)a.W);
-  if (a.W < 2 || a.W > kW)
-    return fail(CCU_ERR_NOT_IMPLEMENTED, "widths W = 2, 3 and 4 are served, got W=%lld",
-                (long long)a.W);
+  if (a.L < 1) return fail(CCU_ERR_NOT_IMPLEMENTED, "an empty state (L = 0) is not served");
+  if (!mul_le(a.D, a.W, INT64_MAX / 4))
+    return fail(CCU_ERR_INVALID_ARGUMENT, "tensor sizes overflow 64-bit indexing");
   if (a.status != nullptr && !aligned(a.status, 4))
     return fail(CCU_ERR_INVALID_ARGUMENT, "status word must be 4-byte aligned");
   if (a.owner != nullptr) {
@@ -124,7 +125,9 @@ ccu_status_t validate(const Args &a, bool *noop, Layout *layout) {
 constexpr int64_t kBulkNarrowMaxL = 4;
 
 bool route_serves(int route, const Args &a, Layout layout) {
-  const bool vec8 = (a.D % 8 == 0) && (a.ld % 8 == 0);
+  // The 8-channel kernels are compiled for widths 2 to 4; every other width runs on the
+  // scalar kernel.
+  const bool vec8 = (a.D % 8 == 0) && (a.ld % 8 == 0) && a.W >= 2 && a.W <= kW;
   switch (route) {
     case CCU_ROUTE_SCALAR: return true;
     case CCU_ROUTE_VECTOR: return vec8 && a.L <= kVectorMaxL;
@@ -278,9 +281,9 @@ ccu_status_t validate_multi(const MultiArgs &m, bool *noop, Layout *layout) {
   if (a.L < a.W - 1)
     return fail(CCU_ERR_INVALID_ARGUMENT, "L must be >= W - 1 (L=%lld, W=%lld)", (long long)a.L,
                 (long long)a.W);
-  if (a.W < 2 || a.W > kW)
-    return fail(CCU_ERR_NOT_IMPLEMENTED, "widths W = 2, 3 and 4 are served, got W=%lld",
-                (long long)a.W);
+  if (a.L < 1) return fail(CCU_ERR_NOT_IMPLEMENTED, "an empty state (L = 0) is not served");
+  if (!mul_le(a.D, a.W, INT64_MAX / 4))
+    return fail(CCU_ERR_INVALID_ARGUMENT, "tensor sizes overflow 64-bit indexing");
   if (a.status != nullptr && !aligned(a.status, 4))
     return fail(CCU_ERR_INVALID_ARGUMENT, "status word must be 4-byte aligned");
   if (a.N == 0 || a.D == 0 || m.T == 0) {
@@ -325,9 +328,9 @@ constexpr int64_t kMultiNarrowMaxL = 4;
 
 bool multi_vector_serves(const MultiArgs &m) {
   const Args &a = m.a;
-  // width 4 up to L = 8; widths 2 and 3 up to L = 4
+  // width 4 up to L = 8; widths 2 and 3 up to L = 4; other widths on the scalar kernel
   const bool served_l = a.W == kW ? a.L <= kVectorMaxL : a.L <= kMultiNarrowMaxL;
-  return a.D % 8 == 0 && served_l && m.sxd == 1 && m.sod == 1 &&
+  return a.W >= 2 && a.W <= kW && a.D % 8 == 0 && served_l && m.sxd == 1 && m.sod == 1 &&
          m.sxn % 8 == 0 && m.sxt % 8 == 0 && m.son % 8 == 0 && m.sot % 8 == 0;
 }
 
@@ -419,9 +422,9 @@ ccu_status_t run_prefill(const PrefillArgs &a, int route, cudaStream_t stream) {
   if (a.L < a.W - 1)
     return fail(CCU_ERR_INVALID_ARGUMENT, "L must be >= W - 1 (L=%lld, W=%lld)", (long long)a.L,
                 (long long)a.W);
-  if (a.W < 2 || a.W > kW)
-    return fail(CCU_ERR_NOT_IMPLEMENTED, "widths W = 2, 3 and 4 are served, got W=%lld",
-                (long long)a.W);
+  if (a.L < 1) return fail(CCU_ERR_NOT_IMPLEMENTED, "an empty state (L = 0) is not served");
+  if (!mul_le(a.D, a.W, INT64_MAX / 4))
+    return fail(CCU_ERR_INVALID_ARGUMENT, "tensor sizes overflow 64-bit indexing");
   if (a.B == 0 || a.D == 0 || a.T == 0) return CCU_OK;
   const int64_t strides[] = {a.sxb, a.sxd, a.sxt, a.sib, a.sid, a.sil, a.sob, a.sod, a.sot,
                              a.sfb, a.sfd, a.sfl};
@@ -440,7 +443,8 @@ ccu_status_t run_prefill(const PrefillArgs &a, int route, cudaStream_t stream) {
   if (!mul_le(a.B, a.D, lim) || !mul_le(a.B * a.D, a.T, lim) || !mul_le(a.B * a.D, a.L, lim))
     return fail(CCU_ERR_INVALID_ARGUMENT, "tensor sizes overflow 64-bit indexing");
 
-  const bool vec_ok = a.D % 8 == 0 && a.sxd == 1 && a.sod == 1 && a.sxb % 8 == 0 &&
+  // The vector and bulk kernels serve widths 2 to 4; other widths run on the scalar kernel.
+  const bool vec_ok = a.W >= 2 && a.W <= kW && a.D % 8 == 0 && a.sxd == 1 && a.sod == 1 && a.sxb % 8 == 0 &&
                       a.sxt % 8 == 0 && a.sob % 8 == 0 && a.sot % 8 == 0 && a.B <= 65535;
   PrefillParams f;
   f.B = a.B;

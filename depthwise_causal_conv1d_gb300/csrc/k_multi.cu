@@ -20,7 +20,7 @@ cudaError_t launch_multi_vector_narrow(const UpdateParams &p, const MultiParams 
 
 namespace {
 
-// One thread per (row, channel), any x / out strides, any L: the correctness anchor.
+// One thread per (row, channel), any x / out strides, any L and W: the correctness anchor.
 template <int ACT>
 __global__ void __launch_bounds__(256) k_multi_scalar(UpdateParams p, MultiParams m) {
   grid_dependency_boundary();
@@ -48,13 +48,21 @@ __global__ void __launch_bounds__(256) k_multi_scalar(UpdateParams p, MultiParam
       return xp[(k - L) * m.sxt];
     };
     // the W-1 window entries before the first token (newest last), in hw[3-(W-1) .. 2]
+    // (widths up to 4; a wider window is read from the history tap by tap)
     uint16_t hw[3] = {0, 0, 0};
-    for (int64_t k = 0; k < W - 1; ++k) hw[3 - (W - 1) + k] = hist(L - (W - 1) + k);
+    if (W <= kW)
+      for (int64_t k = 0; k < W - 1; ++k) hw[3 - (W - 1) + k] = hist(L - (W - 1) + k);
     for (int64_t t = 0; t < m.T; ++t) {
       const uint16_t xv = xp[t * m.sxt];
       float acc = 0.0f;
-      for (int64_t k = 0; k < W - 1; ++k)
-        acc = __fmaf_rn(bf16_bits(hw[3 - (W - 1) + k]), bf16_bits(w[k]), acc);
+      if (W <= kW) {
+        for (int64_t k = 0; k < W - 1; ++k)
+          acc = __fmaf_rn(bf16_bits(hw[3 - (W - 1) + k]), bf16_bits(w[k]), acc);
+      } else {
+        // token t is history entry L + t; its window is entries L + t - (W-1) .. L + t
+        for (int64_t k = 0; k < W - 1; ++k)
+          acc = __fmaf_rn(bf16_bits(hist(L + t - (W - 1) + k)), bf16_bits(w[k]), acc);
+      }
       acc = __fmaf_rn(bf16_bits(xv), bf16_bits(w[W - 1]), acc);
       if (p.bias != nullptr) acc = acc + bf16_bits(p.bias[d]);
       p.out[n * m.son + d * m.sod + t * m.sot] = round_bf16(activate<ACT>(acc));

@@ -42,7 +42,7 @@ __device__ __forceinline__ void write_final(const UpdateParams &p, const Prefill
     f.fin[b * f.sfb + d * f.sfd + l * f.sfl] = (uint16_t)input_at(p, f, b, d, f.T - p.L + l);
 }
 
-// One thread per (batch row, channel, token chunk); any strides.
+// One thread per (batch row, channel, token chunk); any strides and widths.
 template <int ACT>
 __global__ void __launch_bounds__(256) k_prefill_scalar(UpdateParams p, PrefillParams f) {
   grid_dependency_boundary();
@@ -58,14 +58,21 @@ __global__ void __launch_bounds__(256) k_prefill_scalar(UpdateParams p, PrefillP
     const int64_t t1 = t0 + f.chunk < f.T ? t0 + f.chunk : f.T;
     const int64_t W = p.W;
     const uint16_t *w = p.w + d * W;
-    // the W-1 inputs before the chunk (newest last) in hw[3-(W-1) .. 2]
+    // the W-1 inputs before the chunk (newest last) in hw[3-(W-1) .. 2] (widths up to 4; a
+    // wider window is read input by input)
     uint32_t hw[3] = {0u, 0u, 0u};
-    for (int64_t k = 0; k < W - 1; ++k) hw[3 - (W - 1) + k] = input_at(p, f, b, d, t0 - (W - 1) + k);
+    if (W <= kW)
+      for (int64_t k = 0; k < W - 1; ++k) hw[3 - (W - 1) + k] = input_at(p, f, b, d, t0 - (W - 1) + k);
     for (int64_t t = t0; t < t1; ++t) {
       const uint32_t xv = p.x[b * f.sxb + d * f.sxd + t * f.sxt];
       float acc = 0.0f;
-      for (int64_t k = 0; k < W - 1; ++k)
-        acc = __fmaf_rn(bf16_bits(hw[3 - (W - 1) + k]), bf16_bits(w[k]), acc);
+      if (W <= kW) {
+        for (int64_t k = 0; k < W - 1; ++k)
+          acc = __fmaf_rn(bf16_bits(hw[3 - (W - 1) + k]), bf16_bits(w[k]), acc);
+      } else {
+        for (int64_t k = 0; k < W - 1; ++k)
+          acc = __fmaf_rn(bf16_bits(input_at(p, f, b, d, t - (W - 1) + k)), bf16_bits(w[k]), acc);
+      }
       acc = __fmaf_rn(bf16_bits(xv), bf16_bits(w[W - 1]), acc);
       if (p.bias != nullptr) acc = acc + bf16_bits(p.bias[d]);
       p.out[b * f.sob + d * f.sod + t * f.sot] = round_bf16(activate<ACT>(acc));

@@ -1,5 +1,6 @@
-// Scalar kernels: the correctness anchor of the update (any D, any ld, any W in 2..4 and
-// L >= W - 1, both state layouts through explicit strides) and the index checker.
+// Scalar kernels: the correctness anchor of the update (any D, any ld, any width W >= 1
+// and L >= max(W - 1, 1), both state layouts through explicit strides) and the index
+// checker.
 //
 // Update definition: cuDNN page "Causal Conv1d Decode Update", introduction (update
 // block) and the conv_state_indices paragraph.

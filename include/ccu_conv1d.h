@@ -73,7 +73,7 @@ typedef struct CUstream_st *ccu_stream_t;
 typedef enum ccu_status {
   CCU_OK = 0,
   CCU_ERR_INVALID_ARGUMENT = 1, /* the arguments break the tensor contract */
-  CCU_ERR_NOT_IMPLEMENTED = 2,  /* valid, but not served (e.g. a width W > 4) */
+  CCU_ERR_NOT_IMPLEMENTED = 2,  /* valid, but not served (e.g. an empty state, L = 0) */
   CCU_ERR_CUDA = 3              /* a CUDA launch or runtime call failed */
 } ccu_status_t;
 
@@ -85,10 +85,10 @@ typedef enum ccu_act { CCU_ACT_IDENTITY = 0, CCU_ACT_SILU = 1 } ccu_act_t;
  * when it cannot serve the arguments. */
 typedef enum ccu_route {
   CCU_ROUTE_AUTO = 0,
-  CCU_ROUTE_SCALAR = 1, /* one thread per (row, channel); any D, ld, L and layout */
-  CCU_ROUTE_VECTOR = 2, /* 8 channels per thread, 16-byte vectors; D % 8 == 0, L <= 8
-                           (multi-token and prefill: width 4 only) */
-  CCU_ROUTE_STAGED = 3, /* shared-memory staged tiles; D % 8 == 0, any L <= 256 */
+  CCU_ROUTE_SCALAR = 1, /* one thread per (row, channel); any D, ld, L, W and layout */
+  CCU_ROUTE_VECTOR = 2, /* 8 channels per thread, 16-byte vectors; D % 8 == 0, W = 2..4,
+                           L <= 8 (multi-token widths 2 and 3: L <= 4) */
+  CCU_ROUTE_STAGED = 3, /* shared-memory staged tiles; D % 8 == 0, W = 2..4, L <= 256 */
   CCU_ROUTE_BULK = 4,   /* persistent CTAs, bulk async copies through shared memory;
                            D % 8 == 0; width 4 with L <= 8 in both layouts, widths 2
                            and 3 with L <= 4 in the compact layout */
@@ -141,8 +141,11 @@ typedef enum ccu_route {
  *               L entries of a channel share their 32-byte sectors, so the whole slab is read
  *               and written, 16 bytes per element at L = 3 (large batch: 118 against 157 us).
  *   N, D, S     rows, channels, cache slots. N == 0 or D == 0 is a no-op.
- *   L, W        state length and filter width, L >= W - 1. Served: W = 2, 3 or 4 (the page's
- *               native width is 4; it names other widths as semantically valid), any L.
+ *   L, W        state length and filter width, L >= W - 1 (W >= 1). Served: every W with
+ *               L >= 1 (the page's native width is 4; it names other widths as semantically
+ *               valid). Widths 2, 3 and 4 run on every kernel family; W = 1 and W > 4 run on
+ *               the scalar kernel (AUTO picks it). An empty state (W = 1, L = 0) is declined
+ *               with CCU_ERR_NOT_IMPLEMENTED.
  *   out         BF16, contiguous [N, D], written for every row (+0 for padding rows).
  *               16-byte aligned; must not overlap any input.
  *
@@ -307,8 +310,9 @@ CCU_API ccu_status_t ccu_conv1d_update_multi(const void *x, int64_t x_stride_n, 
  * (b, d, l). For the
  * hand-off layout pass final strides (L*D, 1, D). initial_states and final_states may be
  * NULL; final_states must not overlap initial_states, x or out, and out must not overlap x.
- * W = 2, 3 or 4 (CCU_ERR_NOT_IMPLEMENTED otherwise; every kernel serves each of them) and
- * L >= W - 1. B, D or T == 0 is a
+ * Any W >= 1 with L >= W - 1 and L >= 1 (L = 0 is declined with CCU_ERR_NOT_IMPLEMENTED);
+ * widths 2, 3 and 4 run on every kernel, other widths on the scalar kernel (AUTO picks it;
+ * the vector and bulk routes decline them). B, D or T == 0 is a
  * no-op. route: CCU_ROUTE_AUTO, CCU_ROUTE_SCALAR, CCU_ROUTE_VECTOR or CCU_ROUTE_BULK (x staged
  * through shared memory by cp.async.bulk; the vector kernel's conditions; AUTO takes it from
  * B*D*T >= 2^20). The bulk kernel bounds its waits: on expiry it stops and raises

@@ -437,12 +437,13 @@ def pin_multi_vs_full(lib):
 
 
 def pin_widths_one_hot_and_chain(lib):
-    # W = 2 and 3 (the page's other "semantically valid widths"), L from W - 1 up: one-hot
-    # weights reproduce x delayed by W-1-k steps; a chain of updates equals the direct
-    # convolution; the direct convolution equals numpy.convolve within the FP32 bound.
+    # Widths other than 4 (the page's other "semantically valid widths": 1, 2, 3 and wider
+    # ones), L from max(W - 1, 1) up: one-hot weights reproduce x delayed by W-1-k steps; a
+    # chain of updates equals the direct convolution; the direct convolution equals
+    # numpy.convolve within the FP32 bound.
     rng = np.random.default_rng(16)
-    for W in (2, 3):
-        for L in (W - 1, W, 5):
+    for W in (1, 2, 3, 5, 7):
+        for L in sorted({max(W - 1, 1), W, max(5, W + 1)}):
             D, T = 6, 9
             x_seq = rand_bf16(rng, (T, D))
             init = rand_bf16(rng, (D, L))
@@ -470,9 +471,10 @@ def pin_widths_one_hot_and_chain(lib):
 
 
 def pin_widths_multi_and_ring(lib):
-    # The multi-token and ring forms at W = 2, 3 equal the single-token linear steps.
+    # The multi-token and ring forms at widths other than 4 equal the single-token linear steps.
     rng = np.random.default_rng(17)
-    for W, L, T in [(2, 1, 3), (3, 2, 4), (2, 3, 2), (3, 5, 6)]:
+    for W, L, T in [(2, 1, 3), (3, 2, 4), (2, 3, 2), (3, 5, 6), (1, 1, 3), (1, 4, 2), (5, 4, 5),
+                    (7, 9, 3)]:
         N, D, S = 3, 5, 4
         x = rand_bf16(rng, (N, T, D))
         weight = rand_bf16(rng, (D, W))

@@ -96,8 +96,8 @@ def select(ccu, route=0, **kw):
 
 DECLINES = [
     ("misaligned cache_seqlens", dict(cache_seqlens=0x700002), 1, "cache_seqlens must be 4-byte"),
-    ("width 5", dict(W=5, L=4), 2, "W = 2, 3 and 4"),
-    ("width 1", dict(W=1, L=1), 2, "W = 2, 3 and 4"),
+    ("empty state", dict(W=1, L=0), 2, "empty state"),
+    ("L < W-1 at width 6", dict(W=6, L=4), 1, "L must be >= W - 1"),
     ("L < W-1", dict(L=2), 1, "L must be >= W - 1"),
     ("ld < D", dict(ld=32), 1, "ld must be >= D"),
     ("padded ld not multiple of 8", dict(ld=68), 1, "multiple of 8"),
@@ -165,6 +165,36 @@ def test_widths_2_and_3_are_served(ccu):
     assert select(ccu, route=4, W=3, L=5)[0] == 2
     assert select(ccu, route=4, W=3, L=2, stride_s=128, stride_d=1, stride_l=64)[0] == 2  # channel-last: width 4
     assert select(ccu, W=3, L=1)[0] == 1  # L < W - 1
+
+
+def test_other_widths_run_on_the_scalar_kernel(ccu):
+    # W = 1 and W > 4 are valid ("other semantically valid widths"); only the scalar kernel
+    # takes them, so AUTO picks it and the 8-channel routes decline
+    for W, L in [(1, 1), (1, 3), (5, 4), (6, 8), (8, 7), (16, 20)]:
+        assert select(ccu, W=W, L=L) == (0, 1), (W, L)
+        assert select(ccu, W=W, L=L, N=4096, D=16384, S=4096) == (0, 1), (W, L)
+        assert select(ccu, W=W, L=L, cache_seqlens=0x700000) == (0, 1), (W, L)
+        assert select(ccu, route=1, W=W, L=L) == (0, 1), (W, L)
+        for route in (2, 3, 4):
+            assert select(ccu, route=route, W=W, L=L)[0] == 2, (W, L, route)
+
+
+def test_multi_and_prefill_width_declines(ccu):
+    # checked before any CUDA call, so placeholder pointers are never touched
+    N, D, T, S = 4, 64, 2, 4
+
+    def multi(W, L):
+        return ccu.ccu_conv1d_update_multi(X, T * D, 1, D, ST, D * L, L, 1, WT, BS, 0, None, None,
+                                           N, D, T, S, L, W, OUT, T * D, 1, D, None, None, 0, None)
+
+    def prefill(W, L):
+        return ccu.ccu_causal_conv1d_fwd(X, T * D, 1, D, WT, BS, 0, None, 0, 0, 0, 1, D, T, L, W, OUT,
+                                         T * D, 1, D, None, 0, 0, 0, 0, None)
+
+    for fn in (multi, prefill):
+        assert fn(1, 0) == 2 and "empty state" in ccu.ccu_conv1d_last_error()
+        assert fn(6, 4) == 1 and "L must be >= W - 1" in ccu.ccu_conv1d_last_error()
+        assert fn(0, 3) == 1 and "W must be >= 1" in ccu.ccu_conv1d_last_error()
 
 
 def test_ring_buffer_state_is_served(ccu):

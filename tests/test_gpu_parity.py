@@ -695,9 +695,12 @@ def test_typed_declines_through_binding():
         ccu.causal_conv1d_update(x.view(4, 64, 1, 1), st, w)
     with pytest.raises(ValueError, match="intermediate_states"):
         ccu.causal_conv1d_update(x, st, w, intermediate_states=torch.empty((4, 1, 64, 3), dtype=torch.bfloat16, device=DEV))
-    with pytest.raises(NotImplementedError, match="W = 2, 3 and 4"):
+    with pytest.raises(NotImplementedError, match="empty state"):
+        ccu.causal_conv1d_update(x, torch.empty((4, 64, 0), device=DEV, dtype=torch.bfloat16),
+                                 torch.randn((64, 1), device=DEV).to(torch.bfloat16))
+    with pytest.raises(NotImplementedError, match="does not serve"):
         ccu.causal_conv1d_update(x, torch.randn((4, 64, 4), device=DEV).to(torch.bfloat16),
-                                 torch.randn((64, 5), device=DEV).to(torch.bfloat16))
+                                 torch.randn((64, 5), device=DEV).to(torch.bfloat16), route="vector")
     with pytest.raises(ValueError, match="L must be >= W - 1"):
         ccu.causal_conv1d_update(x, st[:, :, :2].contiguous(), w)
     base = torch.randn((4 * 72 + 8,), device=DEV).to(torch.bfloat16)
@@ -1249,6 +1252,133 @@ def test_widths_prefill(W):
         y, f = oracle.full_causal_conv(x_btd[b], weight, bias, "silu", init[b], L)
         assert bf16_ulp_distance(from_dev_u16(out[b]), y.T).max() <= 1
         assert np.array_equal(from_dev_u16(fin[b]), f)
+
+
+# ------------------------------------------------------------------- widths 1 and wider than 4
+
+# The page calls every width with L >= W - 1 semantically valid; widths other than 2, 3 and 4
+# run on the scalar kernels (AUTO picks them).
+OTHER_WIDTH_CASES = [(1, 1), (1, 3), (5, 4), (5, 9), (6, 5), (8, 7), (8, 12), (16, 15)]
+
+
+@pytest.mark.parametrize("ring", [False, True])
+@pytest.mark.parametrize("route", ["auto", "scalar"])
+@pytest.mark.parametrize("layout", ["compact", "channel_last"])
+@pytest.mark.parametrize("W,L", OTHER_WIDTH_CASES)
+def test_other_widths(W, L, layout, route, ring):
+    wl = synthetic.variant(synthetic.WORKLOADS["paged_n256_d8192_l3_s1024_pad10_silu"], name="width",
+                           N=9, D=77, ld=80, S=12, W=W, L=L, pad_frac=0.25)
+    inp = synthetic.generate(wl, seed=W * 100 + L)
+    if ring:
+        _check_ring(inp, ring_seqlens(np.random.default_rng(L), inp), layout, route,
+                    what=f"W={W} L={L} ring {route} {layout}")
+    else:
+        _check(inp, layout=layout, route=route, what=f"W={W} L={L} {route} {layout}")
+
+
+@pytest.mark.parametrize("layout", ["compact", "channel_last"])
+@pytest.mark.parametrize("W,L", [(1, 2), (5, 4), (8, 9)])
+def test_other_widths_checked_duplicates(W, L, layout):
+    """The duplicate-checking update at other widths (scalar kernel): the status bits equal
+    the oracle's index check, and every row but the one that claimed a shared slot (read
+    back from the slot scratch) acts as padding, as do out-of-range rows."""
+    wl = synthetic.variant(synthetic.WORKLOADS["paged_n256_d8192_l3_s1024_pad10_silu"], name="width_dup",
+                           N=40, D=72, ld=72, S=48, W=W, L=L, indices="distinct_pad", pad_frac=0.1)
+    inp = synthetic.generate(wl, seed=300 + W)
+    idx = inp.indices.copy()
+    active = np.flatnonzero(idx >= 0)
+    groups = [[active[2], active[17], active[30]], [active[5], active[6]]]
+    for g in groups:
+        idx[g] = idx[g[0]]
+    idx[active[9]] = -2
+    idx[active[12]] = wl.S
+    want_status = oracle.check_indices(idx, wl.N, wl.S)
+    scratch = torch.full((wl.S,), 777, dtype=torch.int32, device=DEV)  # dirty: the call clears it
+    got_out, got_state, status, ok = run_gpu(dataclasses.replace(inp, indices=idx), layout=layout,
+                                             checked=True, slot_scratch=scratch)
+    assert ok, "a guard band was overwritten"
+    assert status == want_status, (status, want_status)
+    owners = scratch.cpu().numpy()
+    ref_idx = idx.copy()
+    ref_idx[(idx < -1) | (idx >= wl.S)] = -1
+    for g in groups:
+        winner = owners[idx[g[0]]] - 1
+        assert winner in g, (winner, g)
+        ref_idx[[r for r in g if r != winner]] = -1
+    want_out, want_state = oracle_ref(dataclasses.replace(inp, indices=ref_idx), layout)
+    assert_parity(inp, got_out, got_state, want_out, want_state, f"dedup W={W} L={L} {layout}")
+
+
+@pytest.mark.parametrize("W,L,T", [(1, 1, 3), (1, 3, 5), (5, 4, 4), (7, 9, 3), (8, 7, 10)])
+@pytest.mark.parametrize("ring", [False, True])
+@pytest.mark.parametrize("layout", ["compact", "channel_last"])
+def test_other_widths_multi_token(W, L, T, ring, layout):
+    import depthwise_causal_conv1d_gb300 as ccu
+
+    rng = np.random.default_rng(W * 7 + L + T)
+    N, D, S = 5, 40, 6
+    x_tok = synthetic.f64_to_bf16_bits(rng.standard_normal((N, T, D)))
+    weight = synthetic.f64_to_bf16_bits(rng.standard_normal((D, W)))
+    bias = synthetic.f64_to_bf16_bits(rng.standard_normal(D) * 0.1)
+    state = synthetic.f64_to_bf16_bits(rng.standard_normal((S, D, L)))
+    idx = np.array([4, -1, 0, 2, 5], np.int32)
+    seq = np.array([3, 0, L + 2, 1, 11], np.int32) if ring else None
+    st_ref = state.copy()
+    want_out, want_inter = oracle.conv1d_update_multi(x_tok, (T * D, 1, D), st_ref, (D * L, L, 1), weight,
+                                                      bias, "silu", idx, seq, N, D, T, S, L, W,
+                                                      with_inter=True)
+    if layout == "compact":
+        st = to_dev_u16(state, DEV)
+    else:
+        st = to_dev_u16(np.ascontiguousarray(state.transpose(0, 2, 1)), DEV).permute(0, 2, 1)
+    inter = torch.zeros((N, T, D, L), dtype=torch.bfloat16, device=DEV)
+    out = ccu.causal_conv1d_update(to_dev_u16(x_tok, DEV).permute(0, 2, 1), st, to_dev_u16(weight, DEV),
+                                   to_dev_u16(bias, DEV), "silu",
+                                   conv_state_indices=torch.from_numpy(idx).to(DEV),
+                                   cache_seqlens=None if seq is None else torch.from_numpy(seq).to(DEV),
+                                   intermediate_states=inter)
+    torch.cuda.synchronize()
+    from oracle_pins import bf16_ulp_distance
+
+    assert np.array_equal(from_dev_u16(st.contiguous()), st_ref), "state"
+    assert np.array_equal(from_dev_u16(inter), want_inter), "intermediate states"
+    assert bf16_ulp_distance(from_dev_u16(out), want_out).max() <= 1
+
+
+@pytest.mark.parametrize("route", ["auto", "scalar"])
+@pytest.mark.parametrize("W,L", [(1, 1), (1, 2), (5, 4), (7, 8), (9, 8)])
+def test_other_widths_prefill(W, L, route):
+    import depthwise_causal_conv1d_gb300 as ccu
+
+    rng = np.random.default_rng(60 + W + L)
+    B, D, T = 2, 72, 37
+    x_btd = synthetic.f64_to_bf16_bits(rng.standard_normal((B, T, D)))
+    weight = synthetic.f64_to_bf16_bits(rng.standard_normal((D, W)))
+    bias = synthetic.f64_to_bf16_bits(rng.standard_normal(D) * 0.1)
+    init = synthetic.f64_to_bf16_bits(rng.standard_normal((B, D, L)))
+    for with_init in (False, True):
+        out, fin = ccu.causal_conv1d_fwd(to_dev_u16(x_btd, DEV).permute(0, 2, 1), to_dev_u16(weight, DEV),
+                                         to_dev_u16(bias, DEV), "silu",
+                                         initial_states=to_dev_u16(init, DEV) if with_init else None,
+                                         final_state_len=L, return_final_states=True, route=route)
+        torch.cuda.synchronize()
+        from oracle_pins import bf16_ulp_distance
+
+        for b in range(B):
+            y, f = oracle.full_causal_conv(x_btd[b], weight, bias, "silu", init[b] if with_init else None, L)
+            assert bf16_ulp_distance(from_dev_u16(out[b]), y.T).max() <= 1, (b, with_init)
+            assert np.array_equal(from_dev_u16(fin[b]), f), (b, with_init)
+
+
+def test_other_widths_decline_on_8_channel_routes():
+    import depthwise_causal_conv1d_gb300 as ccu
+
+    wl = synthetic.variant(synthetic.WORKLOADS["paged_n256_d8192_l3_s1024_pad10_silu"], name="width",
+                           N=4, D=64, ld=64, S=8, W=5, L=4)
+    inp = synthetic.generate(wl, seed=5)
+    for route in ("vector", "staged", "bulk"):
+        with pytest.raises(NotImplementedError):
+            run_gpu(inp, "compact", route)
 
 
 # ----------------------------------------------------------------------------- timed workloads
