@@ -46,13 +46,12 @@ __device__ __forceinline__ void compact_to_planes(const uint32_t (&cw)[4 * L], u
 }
 
 // 8 channels per thread, x and out channel-contiguous (16-byte vectors per token), state in
-// registers in compact order for the whole row, L and layout compile-time. A thread issues
-// two rows' loads (state and first four tokens) before computing either: bound by load
-// latency with one row in flight, the multi-token workload went from 92.4 to 85.9 us (and
-// the T = 1 shape from 217 to 180 us) at the same two CTAs per SM, which the 128-register
-// cap keeps (without the cap the kernel takes 170 registers, one CTA per SM, and loses).
-// The SiLU runs on channel pairs (the arithmetic is not hidden here: 86.0 -> 84.1 us), at
-// 72 spilled bytes.
+// registers in compact order for the whole row, L and layout compile-time. ROWS = 2: a thread
+// issues two rows' loads (state and first four tokens) before computing either (on the
+// compact L = 3 workload that took 92.4 to 85.9 us against the one-row loop of the time, at
+// the same two CTAs per SM, which the 128-register cap keeps; the choice per state is in
+// multi_two_rows). The SiLU runs on channel pairs (the arithmetic is not hidden here: 86.0
+// -> 84.1 us).
 template <int L, int W, int ACT, int LAYOUT, bool RING, int ROWS>
 __device__ __forceinline__ void multi_vector_body(const UpdateParams &p, const MultiParams &m) {
   const int64_t groups = p.D >> 3;
@@ -173,33 +172,45 @@ __device__ __forceinline__ void multi_vector_body(const UpdateParams &p, const M
   }
 }
 
-// Up to L = 6: two rows in flight under a 128-register cap (two CTAs per SM).
+// Two rows in flight under a 128-register cap (two CTAs per SM).
 template <int L, int W, int ACT, int LAYOUT, bool RING>
 __global__ void __launch_bounds__(256, 2) k_multi_vector(UpdateParams p, MultiParams m) {
   grid_dependency_boundary();
   multi_vector_body<L, W, ACT, LAYOUT, RING, 2>(p, m);
 }
 
-// L = 7 and 8: one row in flight and the compiler's register budget (the two-row form
-// spills 300-600 bytes there under the cap; N=1024, D=16384, T=4: L = 7 148.3 against
-// 192.8 us, L = 8 144.7 against 206.9 us). One channel per lane, as the single-token
-// update runs L = 8, lost here (each lane stepping 8 channels' states through the tokens,
-// four tokens' inputs loaded ahead): L = 8 took 165.7 against 144.2 us and L = 4 138.8
-// against 90.2 us (T = 8, L = 8: 262.9 against 187.3 us); only T = 1 was faster (99.7
-// against 131.3 us), and a single token goes through the update itself.
+// One row in flight at the compiler's register budget (the two-row form spills 300-600
+// bytes at L = 7, 8 under the cap). One channel per lane, as the single-token update runs
+// L = 8, lost here (each lane stepping 8 channels' states through the tokens, four tokens'
+// inputs loaded ahead): L = 8 took 165.7 against 144.2 us and L = 4 138.8 against 90.2 us
+// (T = 8, L = 8: 262.9 against 187.3 us); only T = 1 was faster (99.7 against 131.3 us), and
+// a single token goes through the update itself.
 template <int L, int W, int ACT, int LAYOUT, bool RING>
-__global__ void __launch_bounds__(256) k_multi_vector_long(UpdateParams p, MultiParams m) {
+__global__ void __launch_bounds__(256) k_multi_vector_one_row(UpdateParams p, MultiParams m) {
   grid_dependency_boundary();
   multi_vector_body<L, W, ACT, LAYOUT, RING, 1>(p, m);
+}
+
+// The two-row form is kept where it measured ahead or level: the compact linear state up to
+// L = 3 and the compact ring at L = 4. Everywhere else one row in flight wins. N=1024,
+// D=16384, T=4, SiLU, us, one row (at its best grid) / two rows: compact L = 3 79.5 / 79.6,
+// L = 4 87.6 / 88.8, L = 5 96.0 / 110.6, L = 6 107.2 / 115.6, L = 7 144.7 / 192.8; compact
+// ring L = 3 89.2 / 99.4, L = 4 110.0 / 108.3, L = 5 123.8 / 126.0, L = 6 117.9 / 141.1;
+// channel-last L = 3 80.5 / 88.4, L = 4 87.2 / 97.9, L = 5 95.0 / 114.5, L = 6 103.6 / 132.5;
+// channel-last ring L = 3 90.4 / 105.0, L = 4 103.2 / 108.8, L = 5 106.9 / 138.1, L = 6
+// 125.4 / 162.3.
+template <int L, int LAYOUT, bool RING>
+__host__ __device__ constexpr bool multi_two_rows() {
+  return LAYOUT == (int)Layout::Compact && (RING ? L == 4 : L <= 3);
 }
 
 template <int L, int W, int ACT, int LAYOUT, bool RING>
 cudaError_t launch_vec_one(const UpdateParams &p, const MultiParams &m, dim3 grid, dim3 block,
                            cudaStream_t stream) {
-  if constexpr (L >= 7) {
-    return launch_overlapped(k_multi_vector_long<L, W, ACT, LAYOUT, RING>, grid, block, 0, stream, p, m);
-  } else {
+  if constexpr (multi_two_rows<L, LAYOUT, RING>()) {
     return launch_overlapped(k_multi_vector<L, W, ACT, LAYOUT, RING>, grid, block, 0, stream, p, m);
+  } else {
+    return launch_overlapped(k_multi_vector_one_row<L, W, ACT, LAYOUT, RING>, grid, block, 0, stream, p, m);
   }
 }
 

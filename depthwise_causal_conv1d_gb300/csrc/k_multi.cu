@@ -123,18 +123,24 @@ cudaError_t launch_multi_scalar(const UpdateParams &p, const MultiParams &m, int
                   : launch_overlapped(k_multi_scalar<0>, grid, block, 0, stream, p, m);
 }
 
-// CTAs per SM the grid is sized for: one wave (two per SM, each CTA walking its rows two at
-// a time) where that measured faster, four waves elsewhere. N=1024, D=16384, T=4, us, one
-// wave / four waves: L = 3 77.8 / 81.4 (T = 1 45.8 / 48.7, T = 8 136.2 / 138.1; N=256 20.2 /
-// 22.1; N=128 11.4 / 13.6), L = 4 85.8 / 89.0, L = 6 113.2 / 116.0, L = 7 141.1 / 148.5,
-// L = 8 142.0 / 144.2, channel-last L = 3 86.1 / 87.0 and L = 7 137.7 / 141.0; but L = 5 111.9
-// / 107.6 (channel-last 110.2 / 108.3), channel-last L = 8 123.3 / 120.3 and the compact
-// ring at L = 8 172.4 / 165.5 (others within 1 %). A form that kept each thread's next rows
-// in flight in shared memory (cp.async, three rows ahead, one wave) measured 83.3 at L = 3,
-// 100.4 at L = 4 and 183.9 at L = 8.
+// CTAs per SM the grid is sized for: one wave (two per SM, each CTA walking its rows) or
+// four waves (eight per SM), whichever measured faster. N=1024, D=16384, T=4, us, one wave /
+// four waves, one row in flight: ring states (compact L = 3 90.1 / 89.2, L = 5 135.8 / 123.8,
+// L = 6 119.3 / 117.9, L = 7 176.0 / 160.5, L = 8 172.4 / 165.5; channel-last L = 3 91.1 /
+// 90.4, L = 4 105.7 / 103.2, L = 5 111.4 / 106.9, L = 6 133.3 / 125.4, L = 7 132.8 / 128.3)
+// and the linear state at L = 6 (compact 109.9 / 107.2, channel-last 105.2 / 103.6) and at
+// L = 8 in the channel-last layout (123.3 / 120.3) take four waves; the other linear states
+// one (compact L = 4 87.6 / 89.1, L = 5 96.0 / 97.8, L = 7 144.7 / 152.7, L = 8 142.0 / 144.2;
+// channel-last L = 3 80.5 / 81.0, L = 7 140.3 / 143.2; the two-row form at compact L = 3
+// 77.8 / 81.4, T = 1 45.8 / 48.7, T = 8 136.2 / 138.1, N=256 20.2 / 22.1, N=128 11.4 / 13.6,
+// and at the compact ring L = 4). A form that kept each thread's next rows in flight in
+// shared memory (cp.async, three rows ahead, one wave) measured 83.3 at L = 3, 100.4 at
+// L = 4 and 183.9 at L = 8.
 static int multi_grid_ctas_per_sm(const UpdateParams &p) {
-  const bool four_waves =
-      p.L == 5 || (p.L == 8 && (p.layout == (int)Layout::ChannelLast || p.seqlens != nullptr));
+  const bool ring = p.seqlens != nullptr;
+  const bool compact = p.layout == (int)Layout::Compact;
+  if (ring) return (compact && p.L == 4) ? 2 : 8;  // the compact ring at L = 4 runs two rows
+  const bool four_waves = p.L == 6 || (p.L == 8 && !compact);
   return four_waves ? 8 : 2;
 }
 
