@@ -179,14 +179,17 @@ __global__ void __launch_bounds__(256, 2) k_multi_vector(UpdateParams p, MultiPa
   multi_vector_body<L, W, ACT, LAYOUT, RING, 2>(p, m);
 }
 
-// One row in flight at the compiler's register budget (the two-row form spills 300-600
-// bytes at L = 7, 8 under the cap). One channel per lane, as the single-token update runs
+// One row in flight (the two-row form spills 300-600 bytes at L = 7, 8 under its cap). The
+// compiler keeps it within 128 registers, two CTAs per SM, except at L = 7, where it took
+// up to 166 and one CTA per SM: held to two CTAs there (36 to 72 spilled bytes), N=1024,
+// D=16384, T=4, compact L = 7 takes 121.5 against 145.6 us, channel-last 119.7 against
+// 141.0. One channel per lane, as the single-token update runs
 // L = 8, lost here (each lane stepping 8 channels' states through the tokens, four tokens'
 // inputs loaded ahead): L = 8 took 165.7 against 144.2 us and L = 4 138.8 against 90.2 us
 // (T = 8, L = 8: 262.9 against 187.3 us); only T = 1 was faster (99.7 against 131.3 us), and
 // a single token goes through the update itself.
 template <int L, int W, int ACT, int LAYOUT, bool RING>
-__global__ void __launch_bounds__(256) k_multi_vector_one_row(UpdateParams p, MultiParams m) {
+__global__ void __launch_bounds__(256, L == 7 ? 2 : 1) k_multi_vector_one_row(UpdateParams p, MultiParams m) {
   grid_dependency_boundary();
   multi_vector_body<L, W, ACT, LAYOUT, RING, 1>(p, m);
 }
@@ -194,7 +197,7 @@ __global__ void __launch_bounds__(256) k_multi_vector_one_row(UpdateParams p, Mu
 // The two-row form is kept where it measured ahead or level: the compact linear state up to
 // L = 3 and the compact ring at L = 4. Everywhere else one row in flight wins. N=1024,
 // D=16384, T=4, SiLU, us, one row (at its best grid) / two rows: compact L = 3 79.5 / 79.6,
-// L = 4 87.6 / 88.8, L = 5 96.0 / 110.6, L = 6 107.2 / 115.6, L = 7 144.7 / 192.8; compact
+// L = 4 87.6 / 88.8, L = 5 96.0 / 110.6, L = 6 107.2 / 115.6, L = 7 121.5 / 192.8; compact
 // ring L = 3 89.2 / 99.4, L = 4 110.0 / 108.3, L = 5 123.8 / 126.0, L = 6 117.9 / 141.1;
 // channel-last L = 3 80.5 / 88.4, L = 4 87.2 / 97.9, L = 5 95.0 / 114.5, L = 6 103.6 / 132.5;
 // channel-last ring L = 3 90.4 / 105.0, L = 4 103.2 / 108.8, L = 5 106.9 / 138.1, L = 6
