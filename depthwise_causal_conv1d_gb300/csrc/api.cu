@@ -334,6 +334,16 @@ bool multi_vector_serves(const MultiArgs &m) {
          m.sxn % 8 == 0 && m.sxt % 8 == 0 && m.son % 8 == 0 && m.sot % 8 == 0;
 }
 
+// The bulk-copy multi-token kernel: width 4, the compact state at L = 3..8, T <= 8 tokens,
+// no intermediate states, the vector kernel's stride conditions, and x and out in device
+// memory (checked last: it queries the pointers).
+bool multi_bulk_serves(const MultiArgs &m, Layout layout) {
+  const Args &a = m.a;
+  return a.W == kW && a.L >= 3 && a.L <= kVectorMaxL && layout == Layout::Compact && m.T >= 1 &&
+         m.T <= kMultiBulkMaxT && m.inter == nullptr && multi_vector_serves(m) && !is_host_memory(a.x) &&
+         !is_host_memory(a.out);
+}
+
 ccu_status_t run_multi(const MultiArgs &m, int route, cudaStream_t stream) {
   bool noop = false;
   Layout layout = Layout::Compact;
@@ -341,8 +351,19 @@ ccu_status_t run_multi(const MultiArgs &m, int route, cudaStream_t stream) {
   if (st != CCU_OK || noop) return st;
   int chosen;
   if (route == CCU_ROUTE_AUTO) {
-    chosen = multi_vector_serves(m) ? CCU_ROUTE_VECTOR : CCU_ROUTE_SCALAR;
-  } else if (route == CCU_ROUTE_SCALAR || (route == CCU_ROUTE_VECTOR && multi_vector_serves(m))) {
+    // The bulk-copy kernel where it measured ahead of the vector kernel: the compact ring
+    // state at L = 4, 5 and 7 (N=1024, D=16384, T=4, us, bulk / vector: 98.9 / 109.4, 107.0 /
+    // 123.4, 131.2 / 158.8). Elsewhere the vector kernel leads (compact linear L = 3 95.2 /
+    // 81.0, L = 5 112.5 / 97.1, L = 8 185.7 / 145.2; ring L = 3 97.3 / 89.6, L = 6 128.2 /
+    // 119.3, L = 8 184.8 / 170.5; T = 1, 2, 8 and N = 256, 4096 at L = 3 likewise).
+    const bool bulk_leads = m.a.cache_seqlens != nullptr && (m.a.L == 4 || m.a.L == 5 || m.a.L == 7);
+    if (bulk_leads && layout == Layout::Compact && multi_bulk_serves(m, layout)) {
+      chosen = CCU_ROUTE_BULK;
+    } else {
+      chosen = multi_vector_serves(m) ? CCU_ROUTE_VECTOR : CCU_ROUTE_SCALAR;
+    }
+  } else if (route == CCU_ROUTE_SCALAR || (route == CCU_ROUTE_VECTOR && multi_vector_serves(m)) ||
+             (route == CCU_ROUTE_BULK && multi_bulk_serves(m, layout))) {
     chosen = route;
   } else if (route >= 0 && route < CCU_ROUTE_COUNT) {
     return fail(CCU_ERR_NOT_IMPLEMENTED, "route '%s' does not serve these multi-token arguments",
@@ -380,8 +401,9 @@ ccu_status_t run_multi(const MultiArgs &m, int route, cudaStream_t stream) {
   mp.sod = m.sod;
   mp.sot = m.sot;
   mp.inter = static_cast<uint16_t *>(const_cast<void *>(m.inter));
-  cudaError_t e = chosen == CCU_ROUTE_VECTOR ? launch_multi_vector(p, mp, a.act, stream)
-                                             : launch_multi_scalar(p, mp, a.act, stream);
+  cudaError_t e = chosen == CCU_ROUTE_BULK     ? launch_multi_bulk(p, mp, a.act, stream)
+                  : chosen == CCU_ROUTE_VECTOR ? launch_multi_vector(p, mp, a.act, stream)
+                                               : launch_multi_scalar(p, mp, a.act, stream);
   if (e != cudaSuccess)
     return fail(CCU_ERR_CUDA, "launch of the multi-token %s kernel failed: %s",
                 ccu_route_name(chosen), cudaGetErrorString(e));

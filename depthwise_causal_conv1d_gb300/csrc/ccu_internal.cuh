@@ -533,6 +533,10 @@ cudaError_t launch_prefill(const UpdateParams &p, const PrefillParams &f, int ac
 cudaError_t launch_prefill_bulk(const UpdateParams &p, const PrefillParams &f, int act,
                                 cudaStream_t stream);
 cudaError_t take_prefill_error(int32_t *bits);
+// Bulk-copy multi-token update (compact state, width 4, L = 3..8, T <= kMultiBulkMaxT, no
+// intermediate states, x and out in device memory with channel-contiguous token rows).
+cudaError_t launch_multi_bulk(const UpdateParams &p, const MultiParams &m, int act, cudaStream_t stream);
+cudaError_t take_multi_bulk_error(int32_t *bits);
 // Zeroes n words on the stream as a kernel in the overlapped launch sequence (k_scalar.cu).
 cudaError_t launch_clear_words(int32_t *w, int64_t n, cudaStream_t stream);
 cudaError_t launch_check_indices(const int32_t *idx, int64_t N, int64_t S, uint32_t *bitmap,
@@ -542,6 +546,8 @@ cudaError_t launch_check_indices(const int32_t *idx, int64_t N, int64_t S, uint3
 constexpr int32_t kDevErrTimeout = 4;
 // Largest L the register-resident vector and bulk kernels are compiled for.
 constexpr int64_t kVectorMaxL = 8;
+// Most tokens per row the bulk-copy multi-token kernel takes.
+constexpr int64_t kMultiBulkMaxT = 8;
 // Largest L the shared-memory staged kernel accepts.
 constexpr int64_t kStagedMaxL = 256;
 

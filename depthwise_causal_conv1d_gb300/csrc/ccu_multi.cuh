@@ -179,17 +179,25 @@ __global__ void __launch_bounds__(256, 2) k_multi_vector(UpdateParams p, MultiPa
   multi_vector_body<L, W, ACT, LAYOUT, RING, 2>(p, m);
 }
 
-// One row in flight (the two-row form spills 300-600 bytes at L = 7, 8 under its cap). The
-// compiler keeps it within 128 registers, two CTAs per SM, except at L = 7, where it took
-// up to 166 and one CTA per SM: held to two CTAs there (36 to 72 spilled bytes), N=1024,
-// D=16384, T=4, compact L = 7 takes 121.5 against 145.6 us, channel-last 119.7 against
-// 141.0. One channel per lane, as the single-token update runs
+// One row in flight (the two-row form spills 300-600 bytes at L = 7, 8 under its cap). With
+// no occupancy hint the compiler keeps it within 128 registers, two CTAs per SM, except at
+// L = 7, where it took up to 166 and one CTA per SM; that instance is held to two CTAs
+// (36 to 72 spilled bytes; N=1024, D=16384, T=4: compact L = 7 121.5 against 145.6 us,
+// channel-last 119.7 against 141.0). A hint of one CTA per SM lets the compiler take 162 to
+// 200 registers at L = 4, 5, 6, 8 instead, and those ran 15 to 30 % slower. One channel per
+// lane, as the single-token update runs
 // L = 8, lost here (each lane stepping 8 channels' states through the tokens, four tokens'
 // inputs loaded ahead): L = 8 took 165.7 against 144.2 us and L = 4 138.8 against 90.2 us
 // (T = 8, L = 8: 262.9 against 187.3 us); only T = 1 was faster (99.7 against 131.3 us), and
 // a single token goes through the update itself.
 template <int L, int W, int ACT, int LAYOUT, bool RING>
-__global__ void __launch_bounds__(256, L == 7 ? 2 : 1) k_multi_vector_one_row(UpdateParams p, MultiParams m) {
+__global__ void __launch_bounds__(256) k_multi_vector_one_row(UpdateParams p, MultiParams m) {
+  grid_dependency_boundary();
+  multi_vector_body<L, W, ACT, LAYOUT, RING, 1>(p, m);
+}
+
+template <int L, int W, int ACT, int LAYOUT, bool RING>
+__global__ void __launch_bounds__(256, 2) k_multi_vector_one_row_2cta(UpdateParams p, MultiParams m) {
   grid_dependency_boundary();
   multi_vector_body<L, W, ACT, LAYOUT, RING, 1>(p, m);
 }
@@ -212,6 +220,8 @@ cudaError_t launch_vec_one(const UpdateParams &p, const MultiParams &m, dim3 gri
                            cudaStream_t stream) {
   if constexpr (multi_two_rows<L, LAYOUT, RING>()) {
     return launch_overlapped(k_multi_vector<L, W, ACT, LAYOUT, RING>, grid, block, 0, stream, p, m);
+  } else if constexpr (L == 7) {
+    return launch_overlapped(k_multi_vector_one_row_2cta<L, W, ACT, LAYOUT, RING>, grid, block, 0, stream, p, m);
   } else {
     return launch_overlapped(k_multi_vector_one_row<L, W, ACT, LAYOUT, RING>, grid, block, 0, stream, p, m);
   }

@@ -286,7 +286,7 @@ cudaError_t take_async_error(int32_t *bits) {
   // kept for the next call rather than lost between a read and a clear.
   static std::mutex serial;
   std::lock_guard<std::mutex> lock(serial);
-  int32_t mine = 0, planes = 0, prefill = 0;
+  int32_t mine = 0, planes = 0, prefill = 0, multi = 0;
   cudaError_t e = cudaDeviceSynchronize();
   if (e == cudaSuccess) {
     e = launch_overlapped(k_exchange_async_error, dim3(1), dim3(1), 0, (cudaStream_t)0);
@@ -294,7 +294,8 @@ cudaError_t take_async_error(int32_t *bits) {
   if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&mine, g_async_error_taken, sizeof(int32_t));
   if (e == cudaSuccess) e = take_planes_error(&planes);
   if (e == cudaSuccess) e = take_prefill_error(&prefill);
-  if (e == cudaSuccess) *bits = mine | planes | prefill;
+  if (e == cudaSuccess) e = take_multi_bulk_error(&multi);
+  if (e == cudaSuccess) *bits = mine | planes | prefill | multi;
   return e;
 }
 

@@ -91,7 +91,8 @@ typedef enum ccu_route {
   CCU_ROUTE_STAGED = 3, /* shared-memory staged tiles; D % 8 == 0, W = 2..4, L <= 256 */
   CCU_ROUTE_BULK = 4,   /* persistent CTAs, bulk async copies through shared memory;
                            D % 8 == 0; width 4 with L <= 8 in both layouts, widths 2
-                           and 3 with L <= 4 in the compact layout */
+                           and 3 with L <= 4 in the compact layout (multi-token: width 4,
+                           compact, 3 <= L <= 8, T <= 8; prefill: widths 2 to 4) */
   CCU_ROUTE_COUNT = 5
 } ccu_route_t;
 
@@ -273,7 +274,14 @@ CCU_API ccu_status_t ccu_conv1d_select_route(const void *x, int64_t ld, const vo
  *                linear or ring) after token t. Padding rows' entries are not written.
  *   T            tokens per row; T == 0 is a no-op.
  *   status_dev   NULL, or a device status word as in ccu_conv1d_update_checked.
- *   route        CCU_ROUTE_AUTO, CCU_ROUTE_SCALAR or CCU_ROUTE_VECTOR (others decline).
+ *   route        CCU_ROUTE_AUTO, CCU_ROUTE_SCALAR, CCU_ROUTE_VECTOR or CCU_ROUTE_BULK (others
+ *                decline). BULK: the bulk-copy kernel (x rows and the state slab staged through
+ *                shared memory by cp.async.bulk) for width 4, the compact state at L = 3..8,
+ *                T <= 8, no intermediate states, x and out in device memory with the vector
+ *                kernel's stride conditions; AUTO takes it for the compact ring state at
+ *                L = 4, 5 and 7, where it measured faster. Its waits are bounded: on expiry it
+ *                stops and raises CCU_DEVERR_TIMEOUT (the status word, else the library's own,
+ *                read with ccu_conv1d_take_device_error).
  * Other arguments (state layouts, weight, bias, act, indices, cache_seqlens, N, D, S, L, W,
  * stream) and returns as ccu_conv1d_update.
  */

@@ -895,8 +895,9 @@ def test_multi_token(route, layout, ci):
     _check_multi(case, route, layout, 300 + ci)
 
 
-def _check_multi(case, route, layout, seed):
-    """One multi-token call against the oracle: outputs, intermediate states, final state."""
+def _check_multi(case, route, layout, seed, with_inter=True):
+    """One multi-token call against the oracle: outputs, intermediate states (when asked
+    for), final state."""
     import depthwise_causal_conv1d_gb300 as ccu
 
     N, D, T, L, S = case["N"], case["D"], case["T"], case["L"], case["S"]
@@ -916,7 +917,7 @@ def _check_multi(case, route, layout, seed):
         st = to_dev_u16(state, DEV)
     else:
         st = to_dev_u16(synthetic.to_channel_last(state), DEV).permute(0, 2, 1)
-    inter = torch.zeros((N, T, D, L), dtype=torch.bfloat16, device=DEV)
+    inter = torch.zeros((N, T, D, L), dtype=torch.bfloat16, device=DEV) if with_inter else None
     out = ccu.causal_conv1d_update(x, st, to_dev_u16(weight, DEV), to_dev_u16(bias, DEV), "silu",
                                    conv_state_indices=torch.from_numpy(idx).to(DEV),
                                    cache_seqlens=None if seq is None else torch.from_numpy(seq).to(DEV),
@@ -925,12 +926,19 @@ def _check_multi(case, route, layout, seed):
     assert out.stride() == x.stride()
     got_out = from_dev_u16(out.permute(0, 2, 1).contiguous().permute(0, 2, 1))
     got_state = from_dev_u16(st.contiguous())
-    got_inter = from_dev_u16(inter)
     from oracle_pins import bf16_ulp_distance
 
     assert np.array_equal(got_state, want_state), "final state"
-    assert np.array_equal(got_inter, want_inter), "intermediate states"
+    if with_inter:
+        assert np.array_equal(from_dev_u16(inter), want_inter), "intermediate states"
     assert bf16_ulp_distance(got_out, want_out).max() <= 1, "outputs"
+
+
+def _multi_bulk_serves(case, layout):
+    return (layout == "compact" and case["D"] % 8 == 0 and 3 <= case["L"] <= 8 and 1 <= case["T"] <= 8
+            and case["x_layout"] == "tokens_major")
+
+
 
 
 # The vector multi-token kernel runs one wave of CTAs, each walking many rows two at a time:
@@ -950,6 +958,38 @@ MULTI_MANY_ROWS = [
 @pytest.mark.parametrize("ci", range(len(MULTI_MANY_ROWS)))
 def test_multi_token_many_rows_per_cta(route, layout, ci):
     _check_multi(MULTI_MANY_ROWS[ci], route, layout, 500 + ci)
+
+
+# The bulk-copy multi-token kernel: the compact state at L = 3..8, up to 8 tokens, no
+# intermediate states; on every other case the forced route declines.
+@pytest.mark.parametrize("layout", ["compact", "channel_last"])
+@pytest.mark.parametrize("ci", range(len(MULTI) + len(MULTI_MANY_ROWS)))
+def test_multi_token_bulk(layout, ci):
+    case = (MULTI + MULTI_MANY_ROWS)[ci]
+    if not _multi_bulk_serves(case, layout):
+        with pytest.raises(NotImplementedError):
+            _check_multi(case, "bulk", layout, 700 + ci, with_inter=False)
+        return
+    _check_multi(case, "bulk", layout, 700 + ci, with_inter=False)
+    with pytest.raises(NotImplementedError):  # intermediate states are the vector kernel's
+        _check_multi(case, "bulk", layout, 700 + ci, with_inter=True)
+
+
+@pytest.mark.parametrize("L", [4, 5, 7])
+def test_multi_token_auto_ring_state(L):
+    """AUTO sends the compact ring state at L = 4, 5, 7 (no intermediate states) to the
+    bulk-copy kernel: parity with the oracle on a batch with padding rows and a ragged D."""
+    case = dict(N=300, D=1032, T=4, L=L, S=310, ring=True, x_layout="tokens_major")
+    _check_multi(case, "auto", "compact", 950 + L, with_inter=False)
+
+
+@pytest.mark.parametrize("ring", [False, True])
+@pytest.mark.parametrize("L,T", [(3, 4), (5, 8), (8, 2), (7, 1)])
+def test_multi_token_bulk_large_batch(L, T, ring):
+    """The bulk-copy multi-token kernel on a batch that gives every warp many slices (N=600,
+    D=16384: 64 slices a row), with padding rows, against the oracle."""
+    case = dict(N=600, D=16384, T=T, L=L, S=640, ring=ring, x_layout="tokens_major")
+    _check_multi(case, "bulk", "compact", 900 + 10 * L + T, with_inter=False)
 
 
 @pytest.mark.parametrize("route", ["auto", "vector"])
@@ -1000,7 +1040,7 @@ def test_multi_token_vector_extremes(T):
     assert bf16_ulp_distance(from_dev_u16(out.permute(0, 2, 1)).transpose(0, 2, 1), want_out).max() <= 1
 
 
-@pytest.mark.parametrize("route", ["scalar", "vector"])
+@pytest.mark.parametrize("route", ["scalar", "vector", "bulk"])
 def test_multi_token_checked_bad_index(route):
     """Checked multi-token call: an out-of-range slot raises CCU_DEVERR_RANGE and its row
     behaves as padding (zero outputs, no state access); the other rows are exact."""
