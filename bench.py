@@ -703,6 +703,8 @@ def multi_token_rows(dev, stream, reps=50, route=0, singles_too=True):
         st = to_dev(inp.conv_state, dev)
         w, b = to_dev(inp.weight, dev), to_dev(inp.bias, dev)
         idx = torch.from_numpy(inp.indices).to(dev)
+        seq = torch.from_numpy(inp.cache_seqlens).to(dev) if inp.cache_seqlens is not None else None
+        seq_ptr = None if seq is None else seq.data_ptr()
         out = torch.empty((N, T, D), dtype=torch.bfloat16, device=dev)
         out1 = torch.empty((N, D), dtype=torch.bfloat16, device=dev)  # one token's output
         act = ccu.CCU_ACT_SILU if wl.act == "silu" else ccu.CCU_ACT_IDENTITY
@@ -710,19 +712,23 @@ def multi_token_rows(dev, stream, reps=50, route=0, singles_too=True):
         def multi():
             stat = ccu.lib.ccu_conv1d_update_multi(
                 x.data_ptr(), T * D, 1, D, st.data_ptr(), D * L, L, 1, w.data_ptr(), b.data_ptr(), act,
-                idx.data_ptr(), None, N, D, T, wl.S, L, wl.W, out.data_ptr(), T * D, 1, D, None, None,
+                idx.data_ptr(), seq_ptr, N, D, T, wl.S, L, wl.W, out.data_ptr(), T * D, 1, D, None, None,
                 route, stream.cuda_stream)
             if stat != 0:
                 ccu.raise_for_status(stat)
 
         def singles():
+            # a ring state advances one entry per token: the token's position comes from
+            # cache_seqlens + t (the counts a caller would pass), here precomputed per token
             for t in range(T):
                 stat = ccu.lib.ccu_conv1d_update(
                     x[:, t].data_ptr(), T * D, st.data_ptr(), D * L, L, 1, w.data_ptr(), b.data_ptr(),
-                    act, idx.data_ptr(), None, N, D, wl.S, L, wl.W, out1.data_ptr(),
-                    stream.cuda_stream)
+                    act, idx.data_ptr(), None if seq is None else seqs[t].data_ptr(), N, D, wl.S, L, wl.W,
+                    out1.data_ptr(), stream.cuda_stream)
                 if stat != 0:
                     ccu.raise_for_status(stat)
+
+        seqs = [seq + t for t in range(T)] if seq is not None else None
 
         res = {}
         for label, fn in (("multi", multi), ("singles", singles))[:2 if singles_too else 1]:

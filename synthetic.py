@@ -101,7 +101,8 @@ WIDTH_WORKLOADS = {
 }
 
 # Multi-token update: four tokens per row in one call (x token-major [N, T, D]), at the
-# width-4 window-only state (L = 3), at longer states (L = 5, 8) and at width 3 (L = 2).
+# width-4 window-only state (L = 3), at longer states (L = 5, 8), at width 3 (L = 2), and with
+# a ring-buffer state (L = 5, cache_seqlens drawn as for RING_WORKLOADS).
 _MULTI_BASE = Workload("multi_n1024_d16384_t4_l3_bias_silu", N=1024, D=16384, W=4, L=3, S=1024, ld=16384,
                        x_dist=("normal", 1.0), w_dist=("normal", 1.0), bias_std=0.1, act="silu",
                        indices="perm_pad", pad_frac=0.05, T=4)
@@ -112,6 +113,7 @@ MULTI_WORKLOADS = {
         dataclasses.replace(_MULTI_BASE, name="multi_n1024_d16384_t4_l5_bias_silu", L=5),
         dataclasses.replace(_MULTI_BASE, name="multi_n1024_d16384_t4_l8_bias_silu", L=8),
         dataclasses.replace(_MULTI_BASE, name="multi_n1024_d16384_t4_w3_l2_bias_silu", W=3, L=2),
+        dataclasses.replace(_MULTI_BASE, name="multi_n1024_d16384_t4_l5_ring_bias_silu", L=5, ring=True),
     ]
 }
 

@@ -1446,7 +1446,9 @@ def test_timed_multi_token_full_size(name):
     N, D, T, L, S = wl.N, wl.D, wl.T, wl.L, wl.S
     want_state = inp.conv_state.copy()
     want_out = oracle.conv1d_update_multi(inp.x, (T * D, 1, D), want_state, (D * L, L, 1), inp.weight,
-                                          inp.bias, wl.act, inp.indices, None, N, D, T, S, L, wl.W)
+                                          inp.bias, wl.act, inp.indices, inp.cache_seqlens, N, D, T, S, L,
+                                          wl.W)
+    seq = torch.from_numpy(inp.cache_seqlens).to(DEV) if inp.cache_seqlens is not None else None
     x = to_dev_u16(inp.x, DEV)  # [N, T, D] memory
     st = to_dev_u16(inp.conv_state, DEV)
     w = to_dev_u16(inp.weight, DEV)
@@ -1457,7 +1459,8 @@ def test_timed_multi_token_full_size(name):
     stream = torch.cuda.current_stream()
     rc = ccu.lib.ccu_conv1d_update_multi(
         x.data_ptr(), T * D, 1, D, st.data_ptr(), D * L, L, 1, w.data_ptr(),
-        None if b is None else b.data_ptr(), act, None if idx is None else idx.data_ptr(), None, N, D, T, S, L, wl.W, out.data_ptr(), T * D, 1, D, None, None,
+        None if b is None else b.data_ptr(), act, None if idx is None else idx.data_ptr(),
+        None if seq is None else seq.data_ptr(), N, D, T, S, L, wl.W, out.data_ptr(), T * D, 1, D, None, None,
         ccu.ROUTES["auto"], stream.cuda_stream)
     assert rc == 0, ccu.ccu_conv1d_last_error()
     torch.cuda.synchronize()
