@@ -30,7 +30,10 @@
  *    on those two pointers (launching entry points only, large calls only). The library never
  *    allocates, frees or copies between host and device, and only
  *    ccu_conv1d_take_device_error synchronizes. The update entry points only enqueue
- *    kernels on `stream`, so an update call can be captured in a CUDA graph. Launch
+ *    kernels on `stream`, so an update call can be captured in a CUDA graph. The first
+ *    launch of a bulk-copy kernel on a device (the bulk route of the update, the
+ *    multi-token update and the prefill) sets that kernel's shared-memory limit with
+ *    cudaFuncSetAttribute, so make one such call before capturing it. Launch
  *    errors are reported as CCU_ERR_CUDA; errors of the asynchronous execution surface
  *    at the caller's next synchronization.
  *  - `stream` is a cudaStream_t; NULL is the legacy default stream.
