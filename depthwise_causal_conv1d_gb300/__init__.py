@@ -247,7 +247,9 @@ def causal_conv1d_update(x, conv_state, weight, bias=None, activation=None, *, c
 
     Follows the cuDNN page "Causal Conv1d Decode Update" ("Python API" and "Semantic
     tensor contract"): ``x`` BF16 ``[N, D]`` with strides ``(ld, 1)``; ``conv_state`` BF16
-    ``[S, D, L]``, compact or channel-last ``(L*D, 1, D)``; ``weight`` BF16 ``[D, 4]``;
+    ``[S, D, L]``, compact or channel-last ``(L*D, 1, D)``; ``weight`` BF16 ``[D, W]``
+    (the page's width 4; widths 2 and 3 run on every kernel, other widths with L >= 1 on the
+    scalar kernel);
     ``bias`` BF16 ``[D]`` or None; ``activation`` None/"identity" or "silu"/"swish";
     ``conv_state_indices`` int32 ``[N]`` (``-1`` = padding row) or None; ``cache_seqlens``
     None (linear state) or int32 ``[N]``: the state is then a ring buffer whose oldest entry
