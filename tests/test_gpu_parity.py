@@ -172,8 +172,8 @@ def _every_finite_bf16():
     return bits[((bits >> 7) & 0xFF) != 0xFF].astype(np.uint16)  # 65280 values, +-0 included
 
 
-@pytest.mark.parametrize("path", ["scalar", "vector", "staged", "bulk", "multi", "prefill_vector",
-                                  "prefill_bulk"])
+@pytest.mark.parametrize("path", ["scalar", "vector", "staged", "bulk", "multi", "multi_bulk",
+                                  "prefill_vector", "prefill_bulk"])
 def test_silu_every_finite_bf16_input(path):
     """SiLU of every finite BF16 value (subnormals, +-0, both tails) through each kernel
     family: weights (0, 0, 0, 1), a zero state and no bias make the accumulator equal x, so
@@ -193,9 +193,10 @@ def test_silu_every_finite_bf16_input(path):
     if path in ("scalar", "vector", "staged", "bulk"):
         st = torch.zeros((2, D, 3), dtype=torch.bfloat16, device=DEV)
         got = ccu.causal_conv1d_update(to_dev_u16(x2, DEV), st, w, None, "silu", route=path)
-    elif path == "multi":
+    elif path in ("multi", "multi_bulk"):
         st = torch.zeros((1, D, 3), dtype=torch.bfloat16, device=DEV)
-        got = ccu.causal_conv1d_update(to_dev_u16(x2[None], DEV).permute(0, 2, 1), st, w, None, "silu")
+        got = ccu.causal_conv1d_update(to_dev_u16(x2[None], DEV).permute(0, 2, 1), st, w, None, "silu",
+                                       route="bulk" if path == "multi_bulk" else "auto")
         got = got.permute(0, 2, 1)[0]
     else:
         x = to_dev_u16(x2[None], DEV).permute(0, 2, 1)  # [1, D, 2], token-major memory
@@ -385,6 +386,52 @@ def test_cuda_graph_checked_update_with_duplicates():
         g.replay()
         torch.cuda.synchronize()
         check(f"replay {k}")
+
+
+def test_cuda_graph_multi_token_bulk_ring():
+    """Multi-token calls on the bulk-copy kernel (AUTO, compact ring state at L = 5) captured
+    in a CUDA graph: each replay from the same starting state equals the eager calls bit for
+    bit."""
+    import depthwise_causal_conv1d_gb300 as ccu
+
+    rng = np.random.default_rng(23)
+    N, D, T, L = 384, 2048, 4, 5
+    x = to_dev_u16(synthetic.f64_to_bf16_bits(rng.standard_normal((N, T, D))), DEV).permute(0, 2, 1)
+    w = to_dev_u16(synthetic.f64_to_bf16_bits(rng.standard_normal((D, 4)) * 0.5), DEV)
+    b = to_dev_u16(synthetic.f64_to_bf16_bits(rng.standard_normal(D) * 0.1), DEV)
+    st0 = to_dev_u16(synthetic.f64_to_bf16_bits(rng.standard_normal((N, D, L))), DEV)
+    idx = torch.from_numpy(rng.permutation(N).astype(np.int32)).to(DEV)
+    seq = torch.from_numpy(rng.integers(0, 1000, N).astype(np.int32)).to(DEV)
+
+    def calls(st, y0, y1):
+        ccu.causal_conv1d_update(x, st, w, b, "silu", conv_state_indices=idx, cache_seqlens=seq, out=y0)
+        ccu.causal_conv1d_update(x, st, w, b, "silu", conv_state_indices=idx, cache_seqlens=seq + T, out=y1)
+
+    eager = (st0.clone(), torch.empty_like(x), torch.empty_like(x))
+    calls(*eager)
+    torch.cuda.synchronize()
+    graphed = (st0.clone(), torch.empty_like(x), torch.empty_like(x))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # the first launch sets the kernel's shared-memory limit
+        calls(*graphed)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    seq_next = seq + T  # allocated outside the capture
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        ccu.causal_conv1d_update(x, graphed[0], w, b, "silu", conv_state_indices=idx, cache_seqlens=seq,
+                                 out=graphed[1])
+        ccu.causal_conv1d_update(x, graphed[0], w, b, "silu", conv_state_indices=idx, cache_seqlens=seq_next,
+                                 out=graphed[2])
+    for _ in range(3):
+        graphed[0].copy_(st0)
+        graphed[1].zero_()
+        graphed[2].zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for a, c in zip(eager, graphed):
+            assert torch.equal(a.contiguous().view(torch.int16), c.contiguous().view(torch.int16))
 
 
 def test_cuda_graph_prefill_multi_decode_sequence():
@@ -1575,7 +1622,7 @@ def _big_slots():
 
 
 @pytest.mark.parametrize("layout", ["compact", "channel_last"])
-@pytest.mark.parametrize("route", ["scalar", "vector", "staged", "bulk", "multi"])
+@pytest.mark.parametrize("route", ["scalar", "vector", "staged", "bulk", "multi", "multi_bulk"])
 def test_state_offsets_past_int32(layout, route):
     """Slots whose state starts past element 2^31 of a 4.3 GB state, on every route. The
     oracle runs on the touched slots only (a row's update reads and writes its own slot
@@ -1587,7 +1634,9 @@ def test_state_offsets_past_int32(layout, route):
     mem, st = _big_state(layout)
     idx_np = _big_slots()
     N = len(idx_np)
-    T = 3 if route == "multi" else 1
+    if route == "multi_bulk" and layout != "compact":
+        pytest.skip("the bulk-copy multi-token kernel serves the compact state")
+    T = 3 if route.startswith("multi") else 1
     rng = np.random.default_rng(8)
     x_np = synthetic.f64_to_bf16_bits(rng.standard_normal((N, T, D)))
     w_np = synthetic.f64_to_bf16_bits(rng.standard_normal((D, W)) * 0.5)
@@ -1603,11 +1652,12 @@ def test_state_offsets_past_int32(layout, route):
     idx_mini = np.array([remap[int(s)] if s >= 0 else -1 for s in idx_np], dtype=np.int32)
     w, b = to_dev_u16(w_np, DEV), to_dev_u16(b_np, DEV)
     idx = torch.from_numpy(idx_np).to(DEV)
-    if route == "multi":
+    if route.startswith("multi"):
         want_out = oracle.conv1d_update_multi(x_np, (T * D, 1, D), mini, (D * L, L, 1), w_np, b_np, "silu",
                                               idx_mini, None, N, D, T, len(touched), L, W)
         x = to_dev_u16(x_np, DEV).permute(0, 2, 1)  # [N, D, T] view of [N, T, D] memory
-        out = ccu.causal_conv1d_update(x, st, w, b, "silu", conv_state_indices=idx)
+        out = ccu.causal_conv1d_update(x, st, w, b, "silu", conv_state_indices=idx,
+                                       route="bulk" if route == "multi_bulk" else "auto")
         got_out = from_dev_u16(out)
     else:
         x2 = np.ascontiguousarray(x_np[:, 0, :])
