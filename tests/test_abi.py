@@ -197,6 +197,23 @@ def test_multi_and_prefill_width_declines(ccu):
         assert fn(0, 3) == 1 and "W must be >= 1" in ccu.ccu_conv1d_last_error()
 
 
+def test_multi_token_bulk_route_declines(ccu):
+    # The bulk-copy multi-token kernel serves width 4, the compact state at L = 3..8, T <= 8
+    # and no intermediate states; a forced bulk route declines everything else before any
+    # CUDA call (placeholder pointers are never touched).
+    N, D = 4, 64
+
+    def multi(T=4, L=3, W=4, layout="compact", inter=None):
+        ss = (D * L, L, 1) if layout == "compact" else (L * D, 1, D)
+        return ccu.ccu_conv1d_update_multi(X, T * D, 1, D, ST, *ss, WT, BS, 0, None, None,
+                                           N, D, T, N, L, W, OUT, T * D, 1, D, inter, None, 4, None)
+
+    for kw in (dict(layout="channel_last"), dict(T=9), dict(L=2, W=3), dict(W=3), dict(L=9),
+               dict(inter=0x900000), dict(W=5, L=4)):
+        assert multi(**kw) == 2, kw
+        assert "does not serve" in ccu.ccu_conv1d_last_error()
+
+
 def test_ring_buffer_state_is_served(ccu):
     assert select(ccu, cache_seqlens=0x700000) == (0, 2)
     assert select(ccu, cache_seqlens=0x700000, N=4096, D=16384, S=4096) == (0, 2)  # vector at every size
