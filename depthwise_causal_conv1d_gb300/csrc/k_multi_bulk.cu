@@ -184,7 +184,6 @@ __global__ void __launch_bounds__(kThreads) k_multi_bulk(UpdateParams p, MultiPa
   if (lane == 0) bulk_wait_all();  // stores complete before the warp retires
 }
 
-
 constexpr int kMaxDevices = 64;
 std::atomic<bool> g_opted_in[kMaxDevices][kVectorMaxL + 1][2][2];
 
