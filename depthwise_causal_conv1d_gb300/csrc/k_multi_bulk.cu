@@ -188,7 +188,9 @@ constexpr int kMaxDevices = 64;
 std::atomic<bool> g_opted_in[kMaxDevices][kVectorMaxL + 1][2][2];
 
 // Stage bytes a warp may hold: two stages of T + L rows at T = 4, L = 3 (7 KB), a CTA of 8
-// warps then needing 57 KB.
+// warps then needing 57 KB. Larger budgets (more stages, fewer CTAs per SM) lost: N=1024,
+// D=16384, T=4, us, 8 / 12 / 16 KB: ring L = 4 99.3 / 112.1 / 177.2, ring L = 5 106.9 / 107.3 /
+// 121.8, L = 3 95.7 / 105.7 / 107.7.
 constexpr int64_t kWarpStageBudget = 8 * 1024;
 
 // Stage bytes, stages and shared memory per CTA for T tokens at state length L.
