@@ -97,6 +97,9 @@ WIDTH_WORKLOADS = {
                             name="large_n4096_d16384_w3_l2_perm_pad5_silu", W=3, L=2),
         dataclasses.replace(WORKLOADS["large_n4096_d16384_l3_perm_pad5_silu"],
                             name="large_n4096_d16384_w2_l1_perm_pad5_silu", W=2, L=1),
+        # a width above the page's four (the scalar kernel)
+        dataclasses.replace(WORKLOADS["large_n4096_d16384_l3_perm_pad5_silu"],
+                            name="large_n4096_d16384_w5_l4_perm_pad5_silu", W=5, L=4),
     ]
 }
 

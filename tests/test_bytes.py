@@ -66,6 +66,9 @@ def test_ring_and_width_bytes():
     w2 = synthetic.WIDTH_WORKLOADS["large_n4096_d16384_w2_l1_perm_pad5_silu"]
     # L = 1: 2 + 2 + 2 + 2 = 8 B; weight [D, 2]
     assert synthetic.algorithmic_bytes(w2, _indices(w2)) == base * 8 + pad + 16384 * 2 * 2 + 32768 + 16384
+    w5 = synthetic.WIDTH_WORKLOADS["large_n4096_d16384_w5_l4_perm_pad5_silu"]
+    # L = 4: 2 + 8 + 8 + 2 = 20 B; weight [D, 5]
+    assert synthetic.algorithmic_bytes(w5, _indices(w5)) == base * 20 + pad + 16384 * 5 * 2 + 32768 + 16384
 
 
 def test_multi_token_bytes():
