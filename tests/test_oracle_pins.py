@@ -107,6 +107,18 @@ MUTATIONS += [
 ]
 
 
+# Mistakes that only a width above four shows: the window capped at the newest four taps
+# (the update, the ring update, the multi-token function, the direct convolution).
+_ALL_TAPS = "for (int64_t j = 0; j < W; ++j) {"
+_FOUR_TAPS = "for (int64_t j = (W > 4 ? W - 4 : 0); j < W; ++j) {"
+MUTATIONS += [
+    ("update: window capped at four taps", _ALL_TAPS, _FOUR_TAPS, 1),
+    ("ring update: window capped at four taps", _ALL_TAPS, _FOUR_TAPS, 2),
+    ("multi: window capped at four taps", _ALL_TAPS, _FOUR_TAPS, 3),
+    ("full conv: window capped at four taps", _ALL_TAPS, _FOUR_TAPS, 4),
+]
+
+
 def _replace_nth(src, old, new, nth):
     at = -1
     for _ in range(nth):
